@@ -1,0 +1,386 @@
+"""Benchmark: bitmap-SpMM decode GB/s (fraction of HBM peak) at N = 1..16.
+
+Workload: the four projections of an OPT-13B decoder layer (QKV 15360x5120,
+out 5120x5120, FC1 20480x5120, FC2 5120x20480), fp16, 50% magnitude-style
+unstructured mask, synthetic N(0, 0.02) weights (no checkpoints needed).
+One step = bsp_spmm on every layer at N = 1, 2, 8, 16, plus bsp_spmspv on
+FC2 with a post-ReLU activation (~85% zeros): 17 launches of the decode
+kernel.  The step's working set (354 MB of encoded weights) is larger than
+L2 (129 MB), and each layer is re-read only after the three others have
+passed through L2.
+
+GB/s counts algorithmic bytes: the encoded weight (Stor) + X + Y for each
+spmm, and bitmaps + offsets + the values of active K-octets + x + y for the
+spMspV.
+
+``--impl reference`` times the CPU oracle instead, on a bounded row sample
+of the same workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bitmap_encoded_unstructured_gb300 import synth  # noqa: E402
+
+LAYERS = [("qkv", 15360, 5120), ("out", 5120, 5120), ("fc1", 20480, 5120), ("fc2", 5120, 20480)]
+NS = (1, 2, 8, 16)
+METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def make_workload():
+    """Host-side synthetic inputs (numpy, seeded)."""
+    Ws, xs = {}, {}
+    for i, (name, M, K) in enumerate(LAYERS):
+        Ws[name] = synth.weights_f16(M, K, 0.5, "magnitude", synth.seed_for(2, i))
+        xs[name] = synth.activations_f16(16, K, synth.seed_for(2, 10 + i))
+    relu = synth.activations_relu_f16(LAYERS[3][2], synth.seed_for(2, 6))
+    return Ws, xs, relu
+
+
+def algorithmic_bytes(Ws, relu):
+    """Per-call algorithmic bytes for each (layer, N) and for the spMspV."""
+    out = {}
+    stor = {}
+    for name, M, K in LAYERS:
+        nnz = int(np.count_nonzero(Ws[name]))
+        ngt, nbt = (M // 64) * (K // 64), M * K // 64
+        stor[name] = 4 * (ngt + 1) + 8 * nbt + 2 * nnz
+        for N in NS:
+            out[(name, N)] = stor[name] + 2 * K * N + 2 * M * N
+    name, M, K = LAYERS[3]
+    W = Ws[name]
+    act = (relu.reshape(-1, 8).view(np.float16) != 0).any(axis=1)  # active K-octets
+    nnz_active = int(np.count_nonzero(W.reshape(M, -1, 8)[:, act, :]))
+    ngt, nbt = (M // 64) * (K // 64), M * K // 64
+    out[("fc2", "spmspv")] = 4 * (ngt + 1) + 8 * nbt + 2 * nnz_active + 2 * K + 2 * M
+    return out, stor, float(act.mean())
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.split(", ") for l in self.lines if l and not l.startswith("index")]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(Ws, xs, relu, bytes_per_call, stor, rows_per_layer=128):
+    """The oracle on a bounded row sample of the whole step; GB/s of the
+    equivalent algorithmic bytes (row fraction of each call's bytes)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    eq_bytes = 0.0
+    for N in NS:
+        for name, M, K in LAYERS:
+            rows = np.arange(rows_per_layer)
+            oracle.spmm_f16(Ws[name][rows], xs[name][:N])
+            eq_bytes += bytes_per_call[(name, N)] * rows_per_layer / M
+    name, M, K = LAYERS[3]
+    oracle.spmm_f16(Ws[name][:rows_per_layer], relu.reshape(1, -1))
+    eq_bytes += bytes_per_call[("fc2", "spmspv")] * rows_per_layer / M
+    dt = time.perf_counter() - t0
+    return {"value": eq_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"first {rows_per_layer} rows of each layer, every N in {list(NS)} plus the FC2 "
+                      f"spMspV (one pass of the step on {rows_per_layer}/M of the rows); fp64 dense "
+                      f"triple loop over fp16 inputs"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    Ws, xs, relu = make_workload()
+    bpc, stor, _ = algorithmic_bytes(Ws, relu)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(Ws, xs, relu, bpc, stor, rows_per_layer=16)
+        if i >= args.warmup:
+            vals.append(r)
+    value = statistics.median(v["value"] for v in vals)
+    secs = sum(v["seconds"] for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / len(vals) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"].replace("first 128", "first 16")},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def _config():
+    return {"workload": "OPT-13B decoder projections (QKV 15360x5120, out 5120x5120, FC1 20480x5120, "
+                        "FC2 5120x20480), fp16, 50% magnitude mask; bsp_spmm at N=1,2,8,16 + FC2 "
+                        "bsp_spmspv with ~85%-zero post-ReLU x",
+            "sparsity": 0.5, "batch_n": list(NS), "group_tile": [64, 64],
+            "l2": "inputs larger than L2: 354 MB of encoded weights rotate through a 129 MB L2 each step",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import bitmap_encoded_unstructured_gb300 as bsp
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    Ws, xs, relu = make_workload()
+    bpc, stor, act_frac = algorithmic_bytes(Ws, relu)
+    mats = {}
+    Xd, Yd = {}, {}
+    for name, M, K in LAYERS:
+        mats[name] = bsp.BitmapMatrix(torch.from_numpy(Ws[name].view(np.float16)).to(dev))
+        assert mats[name].storage_bytes() == stor[name]
+        Xd[name] = torch.from_numpy(xs[name].view(np.float16)).to(dev)
+        Yd[name] = torch.empty((16, M), dtype=torch.float16, device=dev)
+    xr = torch.from_numpy(relu.view(np.float16)).to(dev)
+    yr = torch.empty(LAYERS[3][1], dtype=torch.float16, device=dev)
+    Xn = {(name, N): Xd[name][:N].contiguous() for name, _, _ in LAYERS for N in NS}
+    Yn = {(name, N): torch.empty((N, M), dtype=torch.float16, device=dev) for name, M, _ in LAYERS for N in NS}
+
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    calls = []
+    for N in NS:
+        for name, _, _ in LAYERS:
+            calls.append(((name, N), lambda name=name, N=N: bsp.bsp_spmm(
+                mats[name].h, Xn[(name, N)].data_ptr(), N, Yn[(name, N)].data_ptr(), sh)))
+    calls.append((("fc2", "spmspv"), lambda: bsp.bsp_spmspv(mats["fc2"].h, xr.data_ptr(), yr.data_ptr(), sh)))
+
+    def step(events=None):
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            if events is not None:
+                events[i].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    n_calls = len(calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls)] for _ in range(args.steps)]
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(args.steps):
+        ev0[s].record(stream)
+        step(ev[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    total_ms = _max_over_ranks(total_ms, ws)
+
+    # per-launch durations from consecutive events on the launching stream
+    per_call = {k: [] for k, _ in calls}
+    for s in range(args.steps):
+        prev = ev0[s]
+        for i, (k, _) in enumerate(calls):
+            per_call[k].append(prev.elapsed_time(ev[s][i]))
+            prev = ev[s][i]
+    step_bytes = sum(bpc[k] for k, _ in calls)
+    value = ws * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    launch_ms = sum(statistics.mean(v) for v in per_call.values())
+    achieved = step_bytes / (launch_ms * 1e-3) / 1e9
+
+    breakdown = {}
+    for N in NS:
+        b = sum(bpc[(n, N)] for n, _, _ in LAYERS)
+        t = sum(statistics.median(per_call[(n, N)]) for n, _, _ in LAYERS)
+        breakdown[f"N={N}"] = {
+            "GBps": round(b / (t * 1e-3) / 1e9, 1), "frac_hbm": round(b / (t * 1e-3) / 1e9 / peak, 4),
+            "us_per_layer": {n: round(statistics.median(per_call[(n, N)]) * 1e3, 2) for n, _, _ in LAYERS}}
+    t_sp = statistics.median(per_call[("fc2", "spmspv")])
+    breakdown["spmspv_fc2"] = {"GBps": round(bpc[("fc2", "spmspv")] / (t_sp * 1e-3) / 1e9, 1),
+                               "us": round(t_sp * 1e3, 2), "active_octets": round(act_frac, 4),
+                               "speedup_vs_spmm_n1": round(statistics.median(per_call[("fc2", 1)]) / t_sp, 3)}
+
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == _kernel_hash():
+            traffic = tr.get("dram_bytes_per_launch")
+
+    # ---- e2e: same step through the host-buffer C-ABI call
+    e2e = None
+    if not args.no_e2e:
+        Xh = {(n, N): torch.from_numpy(xs[n][:N].view(np.float16).copy()).pin_memory() for n, _, _ in LAYERS for N in NS}
+        Yh = {(n, N): torch.empty((N, M), dtype=torch.float16).pin_memory() for n, M, _ in LAYERS for N in NS}
+        h2d = sum(Xh[k].numel() * 2 for k in Xh)
+        d2h = sum(Yh[k].numel() * 2 for k in Yh)
+        for _ in range(2):
+            for (n, N) in Xh:
+                mats[n].spmm_host(Xh[(n, N)], Yh[(n, N)], stream=sh)
+        _barrier(ws)
+        t0 = time.perf_counter()
+        reps = max(3, args.steps // 5)
+        for _ in range(reps):
+            for (n, N) in Xh:
+                mats[n].spmm_host(Xh[(n, N)], Yh[(n, N)], stream=sh)
+        dt = _max_over_ranks(time.perf_counter() - t0, ws)
+        e2e_bytes = sum(bpc[k] for k in Xh)
+        e2e = {"value": round(ws * e2e_bytes * reps / dt / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "16 bsp_spmm_host calls per step (4 layers x N=1,2,8,16), pinned host X/Y, "
+                       "H2D + kernel + D2H + stream sync per call"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = time_oracle(Ws, xs, relu, bpc, stor)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                "data": "synthetic (seeded numpy: N(0,0.02) weights, magnitude 50% mask, N(0,1) X)",
+                "config": _config(), "frac_hbm": round(value / ws / peak, 4),
+                "breakdown": breakdown, "prefill": None,
+                "roofline": {"bound": "hbm", "kernel": "spmm_decode_kernel",
+                             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                             "unit": "GB/s", "frac": round(achieved / peak, 4),
+                             "algorithmic_bytes_per_launch": round(step_bytes / n_calls),
+                             "traffic": traffic},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * args.steps,
+                "clocks": clk}
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    p = os.path.join(ROOT, "bitmap_encoded_unstructured_gb300", "csrc", "spmm_decode.cu")
+    with open(p, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    from bitmap_encoded_unstructured_gb300.build import build_library
+    build_library()
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

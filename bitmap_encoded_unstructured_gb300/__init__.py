@@ -1,1 +1,263 @@
-"""bitmap_encoded_unstructured_gb300: bitmap-encoded unstructured sparse matmul on GB300."""
+"""bitmap_encoded_unstructured_gb300: bitmap-encoded unstructured sparse matmul on GB300.
+
+Thin Python binding over ``libbsp.so`` (the C ABI declared in
+``include/bsp.h``).  Every step of the computation runs in the library's
+CUDA kernels; this module only marshals arguments.  PyTorch supplies device
+memory and streams.
+
+Two layers:
+
+* ``bsp_*`` functions with the C names, taking raw pointers / ints;
+* ``BitmapMatrix``, a handle owner with tensor-level methods.
+
+The library is loaded on first use; if it is missing or fails to load, the
+call raises ``RuntimeError`` (there is no fallback of any kind).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsp.so")
+
+BSP_FP16 = 0
+BSP_INT8 = 1
+BSP_DECODE_MAX_N = 16
+
+STATUS = {
+    0: "BSP_OK", 1: "BSP_ERR_INVALID_ARG", 2: "BSP_ERR_SHAPE", 3: "BSP_ERR_DTYPE",
+    4: "BSP_ERR_ALIGN", 5: "BSP_ERR_OOM", 6: "BSP_ERR_CUDA", 7: "BSP_ERR_TIMEOUT",
+    8: "BSP_ERR_INTERNAL",
+}
+
+# Entry points declared in include/bsp.h: name -> (restype, argtypes).
+_P = C.c_void_p
+_I64 = C.c_int64
+SIGNATURES = {
+    "bsp_status_string": (C.c_char_p, [C.c_int]),
+    "bsp_encode": (C.c_int, [_P, C.c_int, _I64, _I64, _P, C.POINTER(_P)]),
+    "bsp_destroy": (C.c_int, [_P]),
+    "bsp_spmm": (C.c_int, [_P, _P, _I64, _P, _P]),
+    "bsp_spmm_scaled": (C.c_int, [_P, _P, _I64, _P, _P, _P]),
+    "bsp_spmspv": (C.c_int, [_P, _P, _P, _P]),
+    "bsp_spmm_host": (C.c_int, [_P, _P, _I64, _P, _P]),
+    "bsp_storage_bytes": (C.c_int, [_P, C.POINTER(C.c_uint64)]),
+    "bsp_cr": (C.c_int, [_P, C.POINTER(C.c_double)]),
+    "bsp_info": (C.c_int, [_P, _P]),
+    "bsp_decode": (C.c_int, [_P, _P, _P]),
+    "bsp_export": (C.c_int, [_P, _P, _P, _P, _P]),
+}
+
+
+class bsp_info_t(C.Structure):
+    _fields_ = [("M", C.c_int64), ("K", C.c_int64), ("dtype", C.c_int32),
+                ("gt_m", C.c_int32), ("gt_k", C.c_int32), ("device", C.c_int32),
+                ("NGT", C.c_int64), ("NBT", C.c_int64), ("NNZ", C.c_uint64),
+                ("bitmaps", C.c_void_p), ("offsets", C.c_void_p), ("values", C.c_void_p)]
+
+
+class BspError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> C.CDLL:
+    """Load libbsp.so (built by ``build.build_library`` / ``__graft_entry__.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing")
+            L = C.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise BspError(fn, st)
+
+
+# ---------------------------------------------------------------- raw C names
+
+def bsp_status_string(status: int) -> str:
+    return lib().bsp_status_string(status).decode()
+
+
+def bsp_encode(W_ptr: int, dtype: int, M: int, K: int, stream: int = 0) -> int:
+    h = C.c_void_p()
+    _check("bsp_encode", lib().bsp_encode(W_ptr, dtype, M, K, stream, C.byref(h)))
+    return h.value
+
+
+def bsp_destroy(h: int) -> None:
+    _check("bsp_destroy", lib().bsp_destroy(h))
+
+
+def bsp_spmm(h: int, X_ptr: int, N: int, Y_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmm", lib().bsp_spmm(h, X_ptr, N, Y_ptr, stream))
+
+
+def bsp_spmm_scaled(h: int, X_ptr: int, N: int, scale_ptr: int, Y_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmm_scaled", lib().bsp_spmm_scaled(h, X_ptr, N, scale_ptr, Y_ptr, stream))
+
+
+def bsp_spmspv(h: int, x_ptr: int, y_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmspv", lib().bsp_spmspv(h, x_ptr, y_ptr, stream))
+
+
+def bsp_spmm_host(h: int, X_host_ptr: int, N: int, Y_host_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmm_host", lib().bsp_spmm_host(h, X_host_ptr, N, Y_host_ptr, stream))
+
+
+def bsp_storage_bytes(h: int) -> int:
+    v = C.c_uint64()
+    _check("bsp_storage_bytes", lib().bsp_storage_bytes(h, C.byref(v)))
+    return v.value
+
+
+def bsp_cr(h: int) -> float:
+    v = C.c_double()
+    _check("bsp_cr", lib().bsp_cr(h, C.byref(v)))
+    return v.value
+
+
+def bsp_info(h: int) -> bsp_info_t:
+    o = bsp_info_t()
+    _check("bsp_info", lib().bsp_info(h, C.byref(o)))
+    return o
+
+
+def bsp_decode(h: int, W_out_ptr: int, stream: int = 0) -> None:
+    _check("bsp_decode", lib().bsp_decode(h, W_out_ptr, stream))
+
+
+def bsp_export(h: int, bitmaps_ptr, offsets_ptr, values_ptr, stream: int = 0) -> None:
+    _check("bsp_export", lib().bsp_export(h, bitmaps_ptr, offsets_ptr, values_ptr, stream))
+
+
+# ---------------------------------------------------------------- tensor layer
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class BitmapMatrix:
+    """An encoded weight W (M x K) living on one GPU.
+
+    ``BitmapMatrix(W)`` encodes a CUDA tensor ``W`` (float16 or int8,
+    row-major [M][K], M and K multiples of 64).  ``spmm(X)`` takes
+    X [N][K] and returns Y [N][M] (= (W @ X.T).T, the [tokens, features]
+    layout).
+    """
+
+    def __init__(self, W, stream=None):
+        import torch
+        if not W.is_cuda or W.dim() != 2:
+            raise ValueError("W must be a 2-D CUDA tensor")
+        if W.dtype == torch.float16:
+            self.dtype = BSP_FP16
+        elif W.dtype == torch.int8:
+            self.dtype = BSP_INT8
+        else:
+            raise TypeError("W must be float16 or int8")
+        W = W.contiguous()
+        self.M, self.K = W.shape
+        self.device = W.device
+        self.torch_dtype = W.dtype
+        self.h = bsp_encode(W.data_ptr(), self.dtype, self.M, self.K, _stream(stream))
+
+    def close(self):
+        if getattr(self, "h", None):
+            bsp_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- accounting
+    def storage_bytes(self) -> int:
+        return bsp_storage_bytes(self.h)
+
+    def cr(self) -> float:
+        return bsp_cr(self.h)
+
+    def info(self) -> dict:
+        o = bsp_info(self.h)
+        return {f: getattr(o, f) for f, _ in bsp_info_t._fields_}
+
+    @property
+    def nnz(self) -> int:
+        return int(bsp_info(self.h).NNZ)
+
+    # -- arrays of the format (copies)
+    def arrays(self, stream=None):
+        """Copies of (bitmaps int64 [NBT], offsets int32 [NGT+1], values [NNZ])."""
+        import torch
+        o = bsp_info(self.h)
+        dev = self.device
+        bm = torch.empty(o.NBT, dtype=torch.int64, device=dev)
+        off = torch.empty(o.NGT + 1, dtype=torch.int32, device=dev)
+        vals = torch.empty(o.NNZ, dtype=self.torch_dtype, device=dev)
+        bsp_export(self.h, bm.data_ptr(), off.data_ptr(), vals.data_ptr() if o.NNZ else None,
+                   _stream(stream))
+        return bm, off, vals
+
+    # -- compute
+    def _out(self, N, out, dtype):
+        import torch
+        if out is None:
+            out = torch.empty((N, self.M), dtype=dtype, device=self.device)
+        return out
+
+    def spmm(self, X, out=None, stream=None):
+        import torch
+        N = X.shape[0]
+        ydt = torch.float16 if self.dtype == BSP_FP16 else torch.int32
+        Y = self._out(N, out, ydt)
+        bsp_spmm(self.h, X.data_ptr(), N, Y.data_ptr(), _stream(stream))
+        return Y
+
+    def spmm_scaled(self, X, row_scale, out=None, stream=None):
+        import torch
+        N = X.shape[0]
+        Y = self._out(N, out, torch.float32)
+        bsp_spmm_scaled(self.h, X.data_ptr(), N, row_scale.data_ptr(), Y.data_ptr(), _stream(stream))
+        return Y
+
+    def spmspv(self, x, out=None, stream=None):
+        import torch
+        ydt = torch.float16 if self.dtype == BSP_FP16 else torch.int32
+        y = out if out is not None else torch.empty(self.M, dtype=ydt, device=self.device)
+        bsp_spmspv(self.h, x.data_ptr(), y.data_ptr(), _stream(stream))
+        return y
+
+    def spmm_host(self, X_host, Y_host, stream=None):
+        bsp_spmm_host(self.h, X_host.data_ptr(), X_host.shape[0], Y_host.data_ptr(), _stream(stream))
+        return Y_host
+
+    def decode(self, out=None, stream=None):
+        import torch
+        W = out if out is not None else torch.empty((self.M, self.K), dtype=self.torch_dtype,
+                                                    device=self.device)
+        bsp_decode(self.h, W.data_ptr(), _stream(stream))
+        return W

@@ -1,0 +1,256 @@
+// C-ABI entry points of libbsp (declared in include/bsp.h): argument
+// checks, handle lifetime and dispatch to the kernels.  No exception or
+// abort crosses the boundary; every failure is a bsp_status_t.
+#include "bsp_internal.cuh"
+
+#include <cstdlib>
+#include <new>
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid(const bsp_handle* h) { return h != nullptr && h->magic == BSP_MAGIC; }
+
+// Run on the handle's device, restoring the caller's current device after.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+void free_handle(bsp_handle* h)
+{
+    if (!h) return;
+    cudaFree(h->bitmaps);
+    cudaFree(h->offsets);
+    cudaFree(h->values);
+    cudaFree(h->ws);
+    cudaFree(h->counters);
+    cudaFree(h->stage_x);
+    cudaFree(h->stage_y);
+    h->magic = 0;
+    delete h;
+}
+
+bsp_status_t grow(void** p, size_t* have, size_t need)
+{
+    if (*have >= need) return BSP_OK;
+    cudaFree(*p);
+    *p = nullptr;
+    *have = 0;
+    if (cudaMalloc(p, need) != cudaSuccess) { *p = nullptr; return BSP_ERR_OOM; }
+    *have = need;
+    return BSP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bsp_status_string(bsp_status_t s)
+{
+    switch (s) {
+    case BSP_OK: return "ok";
+    case BSP_ERR_INVALID_ARG: return "invalid argument";
+    case BSP_ERR_SHAPE: return "M and K must be positive multiples of 64 (and NNZ < 2^32)";
+    case BSP_ERR_DTYPE: return "dtype does not match the handle";
+    case BSP_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case BSP_ERR_OOM: return "allocation failed";
+    case BSP_ERR_CUDA: return "CUDA runtime error";
+    case BSP_ERR_TIMEOUT: return "device-side wait timed out";
+    case BSP_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+bsp_status_t bsp_encode(const void* W, bsp_dtype_t dtype, int64_t M, int64_t K,
+                        bsp_stream_t stream, bsp_handle_t* out)
+{
+    if (!out) return BSP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!W) return BSP_ERR_INVALID_ARG;
+    if (dtype != BSP_FP16 && dtype != BSP_INT8) return BSP_ERR_DTYPE;
+    if (M <= 0 || K <= 0 || (M % 64) || (K % 64)) return BSP_ERR_SHAPE;
+    if (!aligned16(W)) return BSP_ERR_ALIGN;
+    bsp_handle* h = new (std::nothrow) bsp_handle{};
+    if (!h) return BSP_ERR_OOM;
+    h->magic = BSP_MAGIC;
+    h->dtype = dtype;
+    h->M = M;
+    h->K = K;
+    h->NGT = (M / 64) * (K / 64);
+    h->NBT = M * K / 64;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        free_handle(h);
+        return BSP_ERR_CUDA;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    bsp_status_t st = bsp_run_encode(h, W, s);
+    if (st != BSP_OK) { free_handle(h); return st; }
+    const size_t ws_bytes = (size_t)BSP_DECODE_MAX_N * (size_t)M * 4;
+    if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess ||
+        cudaMalloc(&h->counters, (size_t)(M / 64) * 4) != cudaSuccess) {
+        free_handle(h);
+        return BSP_ERR_OOM;
+    }
+    if (cudaMemsetAsync(h->ws, 0, ws_bytes, s) != cudaSuccess ||
+        cudaMemsetAsync(h->counters, 0, (size_t)(M / 64) * 4, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        free_handle(h);
+        return BSP_ERR_CUDA;
+    }
+    *out = h;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_destroy(bsp_handle_t h)
+{
+    if (!valid(h)) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    free_handle(h);
+    return BSP_OK;
+}
+
+bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_stream_t stream)
+{
+    if (!valid(h) || !X || !Y || N < 1 || N > (int64_t)1 << 30) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y)) return BSP_ERR_ALIGN;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
+    if (N <= BSP_DECODE_MAX_N)
+        return bsp_run_spmm_decode(h, X, (int)N, Y, mode, nullptr, false, s);
+    // Larger N: the decode kernel over column blocks of 16 tokens.
+    const int eb = bsp_elem_bytes(h->dtype);
+    const int ob = h->dtype == BSP_INT8 ? 4 : 2;
+    for (int64_t n0 = 0; n0 < N; n0 += BSP_DECODE_MAX_N) {
+        const int nb = (int)((N - n0) < BSP_DECODE_MAX_N ? (N - n0) : BSP_DECODE_MAX_N);
+        const bsp_status_t st = bsp_run_spmm_decode(
+            h, (const uint8_t*)X + n0 * h->K * eb, nb, (uint8_t*)Y + n0 * h->M * ob, mode, nullptr, false, s);
+        if (st != BSP_OK) return st;
+    }
+    return BSP_OK;
+}
+
+bsp_status_t bsp_spmm_scaled(bsp_handle_t h, const int8_t* X, int64_t N, const float* row_scale,
+                             float* Y, bsp_stream_t stream)
+{
+    if (!valid(h) || !X || !Y || !row_scale) return BSP_ERR_INVALID_ARG;
+    if (h->dtype != BSP_INT8) return BSP_ERR_DTYPE;
+    if (N < 1 || N > BSP_DECODE_MAX_N) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y)) return BSP_ERR_ALIGN;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    return bsp_run_spmm_decode(h, X, (int)N, Y, BSP_OUT_F32_SCALED, row_scale, false,
+                               (cudaStream_t)stream);
+}
+
+bsp_status_t bsp_spmspv(bsp_handle_t h, const void* x, void* y, bsp_stream_t stream)
+{
+    if (!valid(h) || !x || !y) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return BSP_ERR_ALIGN;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
+    return bsp_run_spmm_decode(h, x, 1, y, mode, nullptr, true, (cudaStream_t)stream);
+}
+
+bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,
+                           bsp_stream_t stream)
+{
+    if (!valid(h) || !X_host || !Y_host || N < 1 || N > (int64_t)1 << 30) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xb = (size_t)N * h->K * bsp_elem_bytes(h->dtype);
+    const size_t yb = (size_t)N * h->M * (h->dtype == BSP_INT8 ? 4 : 2);
+    bsp_status_t st = grow(&h->stage_x, &h->stage_x_bytes, xb);
+    if (st != BSP_OK) return st;
+    st = grow(&h->stage_y, &h->stage_y_bytes, yb);
+    if (st != BSP_OK) return st;
+    if (cudaMemcpyAsync(h->stage_x, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    st = bsp_spmm(h, h->stage_x, N, h->stage_y, stream);
+    if (st != BSP_OK) return st;
+    if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_storage_bytes(bsp_handle_t h, uint64_t* bytes)
+{
+    if (!valid(h) || !bytes) return BSP_ERR_INVALID_ARG;
+    *bytes = 4ull * (uint64_t)(h->NGT + 1) + 8ull * (uint64_t)h->NBT +
+             (uint64_t)bsp_elem_bytes(h->dtype) * h->NNZ;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_cr(bsp_handle_t h, double* cr)
+{
+    uint64_t stor = 0;
+    const bsp_status_t st = bsp_storage_bytes(h, &stor);
+    if (st != BSP_OK) return st;
+    if (!cr) return BSP_ERR_INVALID_ARG;
+    *cr = (double)bsp_elem_bytes(h->dtype) * (double)h->M * (double)h->K / (double)stor;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_info(bsp_handle_t h, bsp_info_t* o)
+{
+    if (!valid(h) || !o) return BSP_ERR_INVALID_ARG;
+    o->M = h->M;
+    o->K = h->K;
+    o->dtype = h->dtype;
+    o->gt_m = 64;
+    o->gt_k = 64;
+    o->device = h->device;
+    o->NGT = h->NGT;
+    o->NBT = h->NBT;
+    o->NNZ = h->NNZ;
+    o->bitmaps = h->bitmaps;
+    o->offsets = h->offsets;
+    o->values = h->values;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_export(bsp_handle_t h, uint64_t* bitmaps, uint32_t* offsets, void* values,
+                        bsp_stream_t stream)
+{
+    if (!valid(h)) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (bitmaps && cudaMemcpyAsync(bitmaps, h->bitmaps, (size_t)h->NBT * 8, cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (offsets && cudaMemcpyAsync(offsets, h->offsets, (size_t)(h->NGT + 1) * 4, cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (values && h->NNZ &&
+        cudaMemcpyAsync(values, h->values, (size_t)h->NNZ * bsp_elem_bytes(h->dtype), cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_decode(bsp_handle_t h, void* W_out, bsp_stream_t stream)
+{
+    if (!valid(h) || !W_out) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(W_out)) return BSP_ERR_ALIGN;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    return bsp_run_decode(h, W_out, (cudaStream_t)stream);
+}
+
+}  // extern "C"

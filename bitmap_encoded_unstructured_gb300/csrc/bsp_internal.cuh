@@ -1,0 +1,56 @@
+// Internal declarations shared by the library's translation units.
+// Nothing here is part of the public C ABI (include/bsp.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include "../../include/bsp.h"
+
+#define BSP_MAGIC 0xB5B17A9Eu
+
+struct bsp_handle {
+    uint32_t magic;
+    int device;
+    bsp_dtype_t dtype;
+    int64_t M, K;         // multiples of 64
+    int64_t NGT, NBT;     // GroupTiles (64x64), BitmapTiles (8x8)
+    uint64_t NNZ;
+    uint64_t* bitmaps;    // [NBT]
+    uint32_t* offsets;    // [NGT + 1]
+    void* values;         // [NNZ] elements + >= 16 B zeroed tail slack
+    size_t values_alloc;  // bytes allocated for values
+    // split-K workspace of the decode path: [BSP_DECODE_MAX_N][M] fp32 or
+    // int32, all zero between calls (the last arriving CTA of a row strip
+    // reads and clears its slice); one arrival counter per 64-row strip.
+    void* ws;
+    uint32_t* counters;
+    int num_sms;
+    // staging for bsp_spmm_host, grown on demand
+    void* stage_x;
+    size_t stage_x_bytes;
+    void* stage_y;
+    size_t stage_y_bytes;
+};
+
+static inline int bsp_elem_bytes(bsp_dtype_t d) { return d == BSP_INT8 ? 1 : 2; }
+
+// Output modes of the decode-path kernel.
+enum bsp_out_mode { BSP_OUT_F16 = 0, BSP_OUT_I32 = 1, BSP_OUT_F32_SCALED = 2 };
+
+// ---- encoder / decoder (encode.cu) ----
+bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s);
+bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s);
+
+// ---- CUDA-core decode-path product (spmm_decode.cu) ----
+// X: [N][K] (fp16 or int8), N in 1..BSP_DECODE_MAX_N.  Output by mode:
+// F16 -> Y half [N][M]; I32 -> Y int32 [N][M]; F32_SCALED -> Y float [N][M]
+// with row_scale[M].  skip_zero_octets: spMspV mode (N must be 1).
+bsp_status_t bsp_run_spmm_decode(const bsp_handle* h, const void* X, int N,
+                                 void* Y, bsp_out_mode mode,
+                                 const float* row_scale, bool skip_zero_octets,
+                                 cudaStream_t s);
+
+// Split-K factor chosen for a handle (exposed for tests and tuning).
+int bsp_decode_splits(const bsp_handle* h, int N);

@@ -1,0 +1,196 @@
+/*
+ * bsp.h - bitmap-encoded unstructured sparse matmul on one GB300 (sm_103a).
+ *
+ * Computes Y = W * X for an unstructured-pruned weight W (M x K, any zero
+ * pattern) held in a bitmap-indexed tile format, and a dense activation
+ * block X (K x N).
+ *
+ * Format (TCA-BME, from "SpInfer: How bitmaps make sparse LLMs actually
+ * fast", sections "How TCA-BME addresses the indexing overhead" and "The
+ * Values array and why it's confusing at first"):
+ *   - BitmapTile (BT): 8x8 elements, one uint64 bitmap, bit set <=> the
+ *     element's raw bits are nonzero; bit p = 8*row + col inside the BT.
+ *   - TCTile: 16x16 = 2x2 BTs, stored in mma A-register order
+ *     (rows 0-7/cols 0-7, rows 8-15/cols 0-7, rows 0-7/cols 8-15,
+ *      rows 8-15/cols 8-15).
+ *   - GroupTile (GT): 64x64 = 4x4 TCTiles, row-major; GTs row-major over the
+ *     (M/64) x (K/64) grid.  BT g = (t*16 + tc)*4 + b for GT t, TCTile tc.
+ *   - values: the nonzeros only, packed in GT -> TCTile -> BT -> bit order.
+ *   - offsets: uint32 [NGT+1], offsets[t] = nonzeros stored before GT t.
+ *   A value's index is offsets[t] + (nonzeros of the earlier BTs of its GT)
+ *   + popcount(bitmap & ((1 << p) - 1)) (the masked popcount of the
+ *   section "Shared Memory Bitmap Decoding (SMBD)").
+ *
+ * Layouts: W is row-major [M][K].  X is [N][K] and Y is [N][M] with K and M
+ * contiguous (PyTorch's [tokens, features]); that is the column-major view
+ * of the pages' K x N and M x N, so row n of Y is W times row n of X.
+ *
+ * Pointers: arguments documented "device" must be device memory of the
+ * current device (or managed memory); "host" arguments are ordinary host
+ * memory.  No call keeps a pointer to caller memory after it returns,
+ * except that kernels launched on `stream` read and write it until they
+ * complete.
+ *
+ * Errors: every entry point returns a bsp_status_t and never aborts or
+ * throws.  A launch failure reports BSP_ERR_CUDA (the CUDA error is also
+ * left for cudaGetLastError()).  Calls that launch work are asynchronous
+ * with respect to the host unless stated otherwise.
+ *
+ * Threading: a handle is immutable after bsp_encode except for its split-K
+ * workspace; calls that compute with one handle must be serialised on one
+ * stream (as with a cuBLAS handle).  Distinct handles are independent.
+ */
+#ifndef BSP_H
+#define BSP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *bsp_stream_t;
+
+typedef struct bsp_handle *bsp_handle_t;
+
+typedef enum {
+    BSP_OK = 0,
+    BSP_ERR_INVALID_ARG = 1, /* null pointer, N out of range, bad handle   */
+    BSP_ERR_SHAPE = 2,       /* M or K not a positive multiple of 64       */
+    BSP_ERR_DTYPE = 3,       /* call does not match the handle's dtype     */
+    BSP_ERR_ALIGN = 4,       /* X / Y / W not 16-byte aligned              */
+    BSP_ERR_OOM = 5,         /* device or host allocation failed           */
+    BSP_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed       */
+    BSP_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up         */
+    BSP_ERR_INTERNAL = 8     /* an invariant of the format was violated    */
+} bsp_status_t;
+
+typedef enum {
+    BSP_FP16 = 0, /* IEEE binary16 values, fp32 accumulation, fp16 output */
+    BSP_INT8 = 1  /* int8 values, int32 accumulation (exact)             */
+} bsp_dtype_t;
+
+/* Largest N taken by the CUDA-core decode path; larger N use tensor cores. */
+#define BSP_DECODE_MAX_N 16
+
+typedef struct {
+    int64_t M, K;
+    int32_t dtype;        /* bsp_dtype_t                                   */
+    int32_t gt_m, gt_k;   /* GroupTile shape: 64, 64                        */
+    int32_t device;       /* CUDA device the arrays live on                */
+    int64_t NGT, NBT;     /* GroupTiles, BitmapTiles                        */
+    uint64_t NNZ;         /* stored nonzeros                                */
+    const uint64_t *bitmaps; /* device, [NBT]                              */
+    const uint32_t *offsets; /* device, [NGT + 1]                          */
+    const void *values;      /* device, [NNZ] (+16 B tail slack, not counted) */
+} bsp_info_t;
+
+/* Short static description of a status code (never NULL). */
+const char *bsp_status_string(bsp_status_t s);
+
+/*
+ * Encode a dense weight into the format, on the device.
+ *   W      device, row-major [M][K] fp16 or int8 (raw bits are examined:
+ *          an element is stored iff its bits are nonzero, so -0.0 / NaN /
+ *          Inf are kept as payload); 16-byte aligned.  Not retained.
+ *   M, K   positive multiples of 64 (BSP_ERR_SHAPE otherwise); the total
+ *          nonzero count must fit in uint32.
+ *   stream work is ordered on it; the call synchronises `stream` once (to
+ *          learn NNZ and size the values array), so W may be freed when it
+ *          returns.
+ *   out    receives the new handle, which owns every device array it uses.
+ * Encoding is an offline step; the pages exclude it from kernel timings
+ * (UnionSparse, "Baselines and Fairness").
+ */
+bsp_status_t bsp_encode(const void *W, bsp_dtype_t dtype, int64_t M, int64_t K,
+                        bsp_stream_t stream, bsp_handle_t *out);
+
+/* Free a handle and its device arrays (synchronises the device first). */
+bsp_status_t bsp_destroy(bsp_handle_t h);
+
+/*
+ * Y = W * X.  ("Unified Static-Dynamic Pruning for Efficient LLM
+ * Inference", section 3.1: W in R^{MxK}, X in R^{KxN}.)
+ *   X  device [N][K], fp16 (BSP_FP16 handle) or int8 (BSP_INT8), 16-B aligned.
+ *   Y  device [N][M], fp16 (BSP_FP16) or int32 (BSP_INT8), 16-B aligned.
+ *   N  >= 1.  N <= BSP_DECODE_MAX_N runs the CUDA-core decode kernel
+ *      (split-K over GroupTiles, fp32 / int32 accumulation); larger N runs
+ *      the tcgen05 tensor-core kernel (fp16 only; BSP_ERR_DTYPE for int8).
+ * fp16: Y = fp16(round-to-nearest of an fp32 sum in unspecified order).
+ * int8: Y is the exact int32 sum.
+ */
+bsp_status_t bsp_spmm(bsp_handle_t h, const void *X, int64_t N, void *Y,
+                      bsp_stream_t stream);
+
+/*
+ * INT8 with per-row dequantisation: Y[n][m] = fp32(acc[n][m]) * row_scale[m],
+ * one round-to-nearest int->float conversion and one fp32 multiply.
+ *   X device int8 [N][K]; row_scale device fp32 [M]; Y device fp32 [N][M].
+ *   1 <= N <= BSP_DECODE_MAX_N.  BSP_ERR_DTYPE on an fp16 handle.
+ */
+bsp_status_t bsp_spmm_scaled(bsp_handle_t h, const int8_t *X, int64_t N,
+                             const float *row_scale, float *Y,
+                             bsp_stream_t stream);
+
+/*
+ * Sparse-matrix times sparse-vector: y = W * x for one activation vector,
+ * skipping the weight tiles whose activations are all zero ("Unified
+ * Static-Dynamic Pruning for Efficient LLM Inference", sections 4.2-4.2.1:
+ * inactive columns are neither loaded nor decoded).  The skip unit is an
+ * 8-column BitmapTile column (a K-octet): its values are not read when
+ * x[8j .. 8j+7] are all exactly zero.  The result equals bsp_spmm with N=1.
+ *   x device [K] (fp16 or int8), y device [M] (fp16 or int32), 16-B aligned.
+ */
+bsp_status_t bsp_spmspv(bsp_handle_t h, const void *x, void *y,
+                        bsp_stream_t stream);
+
+/*
+ * Same product as bsp_spmm, from and to HOST memory: copies X in, runs the
+ * product and copies Y out on `stream`, then synchronises `stream`.  Uses a
+ * device staging buffer owned by the handle (grown on demand, so this call
+ * may allocate).  X host [N][K]; Y host [N][M]; pinned memory is fastest.
+ */
+bsp_status_t bsp_spmm_host(bsp_handle_t h, const void *X_host, int64_t N,
+                           void *Y_host, bsp_stream_t stream);
+
+/*
+ * Footprint of the encoded weight in bytes, exactly
+ *   Stor = 4*(NGT+1) + 8*NBT + B_v*NNZ   (B_v = 2 fp16, 1 int8),
+ * the closed form on the SpInfer page ("How TCA-BME addresses the indexing
+ * overhead").  The 16 B of tail slack of the values allocation is not
+ * counted.
+ */
+bsp_status_t bsp_storage_bytes(bsp_handle_t h, uint64_t *bytes);
+
+/*
+ * Compression ratio CR = B_v*M*K / Stor ("Unified Static-Dynamic Pruning
+ * for Efficient LLM Inference", eq. (1), which is written for fp16 with
+ * B_v = 2; int8 handles use B_v = 1, the same-dtype dense size).
+ */
+bsp_status_t bsp_cr(bsp_handle_t h, double *cr);
+
+/* Shapes, counts and device pointers of the encoded arrays (read only). */
+bsp_status_t bsp_info(bsp_handle_t h, bsp_info_t *out);
+
+/*
+ * Copy the three encoded arrays into caller buffers (device memory, or any
+ * memory cudaMemcpyAsync with cudaMemcpyDefault accepts): bitmaps u64
+ * [NBT], offsets u32 [NGT+1], values [NNZ] elements.  Any pointer may be
+ * NULL to skip that array.  Ordered on `stream`; does not synchronise.
+ */
+bsp_status_t bsp_export(bsp_handle_t h, uint64_t *bitmaps, uint32_t *offsets,
+                        void *values, bsp_stream_t stream);
+
+/*
+ * Decode back to dense: W_out device row-major [M][K] (fp16 or int8 bits),
+ * 16-B aligned.  decode(encode(W)) == W bit for bit.
+ */
+bsp_status_t bsp_decode(bsp_handle_t h, void *W_out, bsp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSP_H */

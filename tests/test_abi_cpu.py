@@ -1,0 +1,62 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h declares.
+
+No compute call is made (there may be no GPU here).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import bitmap_encoded_unstructured_gb300 as bsp
+from bitmap_encoded_unstructured_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(bsp_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return ctypes.CDLL(bsp.LIB_PATH)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "bsp_encode" in names and "bsp_spmm" in names and "bsp_spmspv" in names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_covers_every_symbol():
+    assert _declared() == set(bsp.SIGNATURES)
+
+
+def test_status_strings_without_gpu():
+    for s in range(9):
+        assert bsp.bsp_status_string(s)
+    assert bsp.bsp_status_string(0) == "ok"
+
+
+def test_argument_errors_without_gpu():
+    # Calls rejected before any CUDA work return their status codes.
+    L = bsp.lib()
+    h = ctypes.c_void_p()
+    assert L.bsp_encode(None, 0, 64, 64, None, ctypes.byref(h)) == 1   # null W
+    assert L.bsp_encode(16, 0, 65, 64, None, ctypes.byref(h)) == 2     # M % 64
+    assert L.bsp_encode(16, 7, 64, 64, None, ctypes.byref(h)) == 3     # dtype
+    assert L.bsp_encode(8, 0, 64, 64, None, ctypes.byref(h)) == 4      # alignment
+    assert L.bsp_spmm(None, 16, 1, 16, None) == 1
+    assert L.bsp_spmspv(None, 16, 16, None) == 1
+    assert L.bsp_destroy(None) == 1
+    v = ctypes.c_uint64()
+    assert L.bsp_storage_bytes(None, ctypes.byref(v)) == 1

@@ -1,0 +1,343 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+Encode/decode and int8 are compared bit for bit; fp16 products within
+|y - y_ref| <= 4e-3 * sum_k |w_mk x_kn| + 1e-5 per element; products whose
+partial sums are small integers must be exact.
+"""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import bitmap_encoded_unstructured_gb300 as bsp
+from bitmap_encoded_unstructured_gb300 import synth
+
+from helpers import assert_within_bound, sample_rows, to_dev, to_dev_f16
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if DEV is None:
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture
+def splitk(monkeypatch):
+    """Force the split-K factor of the decode kernel for one test."""
+    def set_(v):
+        if v is None:
+            monkeypatch.delenv("BSP_SPLITK", raising=False)
+        else:
+            monkeypatch.setenv("BSP_SPLITK", str(v))
+    yield set_
+    monkeypatch.delenv("BSP_SPLITK", raising=False)
+
+
+def _encode(W):
+    if W.dtype == np.uint16:
+        return bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    return bsp.BitmapMatrix(to_dev(W, DEV))
+
+
+def _arrays_np(A):
+    bm, off, vals = A.arrays()
+    torch.cuda.synchronize()
+    v = vals.cpu().numpy()
+    v = v.view(np.uint16) if v.dtype == np.float16 else v
+    return bm.cpu().numpy().view(np.uint64), off.cpu().numpy().view(np.uint32), v
+
+
+# ------------------------------------------------------------------ format
+
+ENC_CASES = [
+    ("c1_256_bern50", lambda: synth.weights_f16(256, 256, 0.5, "bernoulli", synth.seed_for(1, 0))),
+    ("sweep_30", lambda: synth.weights_f16(512, 1024, 0.3, "uniform", synth.seed_for(3, 0))),
+    ("sweep_70", lambda: synth.weights_f16(512, 1024, 0.7, "uniform", synth.seed_for(3, 4))),
+    ("magnitude_50", lambda: synth.weights_f16(384, 640, 0.5, "magnitude", synth.seed_for(2, 0))),
+    ("int8_60", lambda: synth.weights_i8(256, 512, 0.6, synth.seed_for(5, 1))),
+    ("all_zero", lambda: np.zeros((128, 192), dtype=np.uint16)),
+    ("dense", lambda: synth.weights_f16(64, 128, 0.0, "none", 5)),
+    ("single_nz", lambda: _single_nonzero()),
+]
+
+
+def _single_nonzero():
+    W = np.zeros((192, 128), dtype=np.uint16)
+    W[77, 99] = 0x3C00
+    return W
+
+
+@pytest.mark.parametrize("name,make", ENC_CASES, ids=[c[0] for c in ENC_CASES])
+def test_encode_matches_oracle_bytes(name, make):
+    W = make()
+    enc = oracle.encode(W)
+    A = _encode(W)
+    bm, off, vals = _arrays_np(A)
+    assert A.nnz == enc["NNZ"]
+    np.testing.assert_array_equal(bm, enc["bitmaps"])
+    np.testing.assert_array_equal(off, enc["offsets"])
+    np.testing.assert_array_equal(vals, enc["values"])
+    assert A.storage_bytes() == oracle.storage_bytes(enc)
+    assert abs(A.cr() - oracle.compression_ratio(enc)) < 1e-12
+    Wd = A.decode()
+    torch.cuda.synchronize()
+    got = Wd.cpu().numpy()
+    got = got.view(np.uint16) if got.dtype == np.float16 else got
+    np.testing.assert_array_equal(got, W)
+
+
+def test_decode_special_payloads_bitwise():
+    W = np.zeros((64, 128), dtype=np.uint16)
+    for i, v in enumerate([0x8000, 0x7C00, 0xFC00, 0x7E00, 0x7C01, 0x0001, 0x8001]):
+        W[5 * i, 3 * i + 2] = v
+    A = _encode(W)
+    assert A.nnz == 7
+    got = A.decode().cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, W)
+
+
+# ------------------------------------------------------------------ fp16 products
+
+@pytest.mark.parametrize("N", [1, 8])
+def test_spmm_tiny_config(N):
+    """256x256 fp16, 50% Bernoulli zeros, X N(0,1)."""
+    W = synth.weights_f16(256, 256, 0.5, "bernoulli", synth.seed_for(1, 0))
+    X = synth.activations_f16(N, 256, synth.seed_for(1, 1))
+    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Y, Yref, S, f"tiny N={N}")
+
+
+@pytest.mark.parametrize("N", list(range(1, 17)))
+def test_spmm_every_n_ragged(N, splitk):
+    """Every N in 1..16 (padded register tiles), several tiles, odd split."""
+    W = synth.weights_f16(384, 1472, 0.5, "uniform", 77)   # K/64 = 23 GT columns
+    X = synth.activations_f16(N, 1472, 78 + N)
+    Yref, S = oracle.spmm_f16(W, X)
+    A = _encode(W)
+    for s in (1, 3, None):
+        splitk(s)
+        Y = A.spmm(to_dev_f16(X, DEV)).cpu().numpy()
+        assert_within_bound(Y, Yref, S, f"N={N} splitk={s}")
+
+
+@pytest.mark.parametrize("s", [0.3, 0.4, 0.5, 0.6, 0.7])
+def test_spmm_sparsity_sweep_small(s):
+    W = synth.weights_f16(512, 1024, s, "uniform", synth.seed_for(3, int(s * 10)))
+    X = synth.activations_f16(16, 1024, 5)
+    Yref, S = oracle.spmm_f16(W, X)
+    for N in (1, 4, 8, 16):
+        Y = _encode(W).spmm(to_dev_f16(X[:N].copy(), DEV)).cpu().numpy()
+        assert_within_bound(Y, Yref[:N], S[:N], f"s={s} N={N}")
+
+
+@pytest.mark.parametrize("N", [1, 3, 16])
+def test_spmm_small_integers_exact(N, splitk):
+    """|w|,|x| <= 8, K = 256: every partial sum is an exact integer, so the
+    fp16 output has exactly one correct value, in any summation order."""
+    W = synth.small_int_f16((320, 256), -8, 8, seed=41, sparsity=0.5)
+    X = synth.small_int_f16((N, 256), -8, 8, seed=42)
+    Yref, _ = oracle.spmm_f16(W, X)
+    A = _encode(W)
+    for s in (1, 2, 4):
+        splitk(s)
+        for _ in range(2):  # second call: workspace and counters were cleared
+            Y = A.spmm(to_dev_f16(X, DEV)).cpu().numpy().astype(np.float64)
+            np.testing.assert_array_equal(Y, Yref)
+
+
+def test_spmm_permutation_exact():
+    M = K = 256
+    perm = synth.rng(5).permutation(K)
+    W = np.zeros((M, K), dtype=np.uint16)
+    W[np.arange(M), perm] = 0x3C00
+    X = synth.activations_f16(8, K, 6)
+    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    np.testing.assert_array_equal(Y.view(np.uint16), X[:, perm])
+
+
+def test_spmm_all_zero_weight():
+    W = np.zeros((128, 256), dtype=np.uint16)
+    X = synth.activations_f16(4, 256, 1)
+    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    assert np.all(Y == 0)
+
+
+def test_spmm_dense_weight_vs_library():
+    """s = 0 reduces to a dense GEMM: also hold it against torch.matmul in fp64 on CPU."""
+    W = synth.weights_f16(256, 512, 0.0, "none", 9)
+    X = synth.activations_f16(8, 512, 10)
+    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    ref = (torch.from_numpy(X.view(np.float16)).double() @ torch.from_numpy(W.view(np.float16)).double().T).numpy()
+    Yref, S = oracle.spmm_f16(W, X)
+    np.testing.assert_allclose(Yref, ref, rtol=1e-12, atol=1e-12)
+    assert_within_bound(Y, Yref, S, "dense")
+
+
+def test_spmm_large_n_column_blocks():
+    W = synth.weights_f16(256, 512, 0.5, "uniform", 19)
+    X = synth.activations_f16(40, 512, 20)
+    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Y, Yref, S, "N=40")
+
+
+def test_spmm_guard_bands():
+    """Canaries around Y are untouched; only Y[N][M] is written."""
+    W = synth.weights_f16(192, 256, 0.5, "uniform", 23)
+    X = synth.activations_f16(5, 256, 24)
+    A = _encode(W)
+    pad = 64
+    buf = torch.full((pad + 5 * 192 + pad,), 12345.0, dtype=torch.float16, device=DEV)
+    Y = buf[pad:pad + 5 * 192].view(5, 192)
+    A.spmm(to_dev_f16(X, DEV), out=Y)
+    b = buf.cpu().numpy()
+    assert np.all(b[:pad] == np.float16(12345.0)) and np.all(b[-pad:] == np.float16(12345.0))
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Y.cpu().numpy(), Yref, S, "guard")
+
+
+# ------------------------------------------------------------------ int8
+
+@pytest.mark.parametrize("N", [1, 8, 16])
+@pytest.mark.parametrize("s", [0.5, 0.6])
+def test_spmm_int8_exact(N, s, splitk):
+    W = synth.weights_i8(256, 1088, s, synth.seed_for(5, int(s * 10)))
+    X = synth.activations_i8(N, 1088, synth.seed_for(5, 7))
+    Yref = oracle.spmm_i8(W, X)
+    A = _encode(W)
+    for k in (1, 5, None):
+        splitk(k)
+        Y = A.spmm(to_dev(X, DEV)).cpu().numpy()
+        assert Y.dtype == np.int32
+        np.testing.assert_array_equal(Y.astype(np.int64), Yref)
+
+
+@pytest.mark.parametrize("N", [1, 16])
+def test_spmm_int8_scaled_bitexact(N):
+    W = synth.weights_i8(192, 512, 0.5, synth.seed_for(5, 2))
+    X = synth.activations_i8(N, 512, synth.seed_for(5, 3))
+    scale = synth.row_scales(192, synth.seed_for(5, 4))
+    ref = oracle.scale_i8(oracle.spmm_i8(W, X), scale)
+    Y = _encode(W).spmm_scaled(to_dev(X, DEV), to_dev(scale, DEV)).cpu().numpy()
+    np.testing.assert_array_equal(Y.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ spMspV
+
+@pytest.mark.parametrize("zero_frac_shift", [None, -3.0, 0.5])
+def test_spmspv_matches_n1_product(zero_frac_shift):
+    M, K = 320, 2048
+    W = synth.weights_f16(M, K, 0.5, "magnitude", synth.seed_for(2, 3))
+    if zero_frac_shift is None:
+        x = synth.activations_relu_f16(K, synth.seed_for(2, 4))
+    else:
+        x = synth.activations_relu_f16(K, 9, shift=zero_frac_shift)
+    yref, s = oracle.spmspv_f16(W, x)
+    A = _encode(W)
+    y = A.spmspv(to_dev_f16(x, DEV)).cpu().numpy()
+    assert_within_bound(y, yref, s, "spmspv")
+
+
+def test_spmspv_all_zero_and_dense_x():
+    M, K = 192, 1024
+    W = synth.weights_f16(M, K, 0.5, "uniform", 31)
+    A = _encode(W)
+    y = A.spmspv(torch.zeros(K, dtype=torch.float16, device=DEV)).cpu().numpy()
+    assert np.all(y == 0)
+    x = synth.activations_f16(1, K, 32)[0]
+    yref, s = oracle.spmspv_f16(W, x)
+    assert_within_bound(A.spmspv(to_dev_f16(x, DEV)).cpu().numpy(), yref, s, "dense x")
+
+
+def test_spmspv_small_integers_exact():
+    W = synth.small_int_f16((256, 256), -8, 8, seed=51, sparsity=0.5)
+    x = synth.small_int_f16((256,), 0, 8, seed=52, sparsity=0.8)
+    yref, _ = oracle.spmspv_f16(W, x)
+    y = _encode(W).spmspv(to_dev_f16(x, DEV)).cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(y, yref)
+
+
+def test_spmspv_int8_exact():
+    W = synth.weights_i8(256, 1024, 0.5, 61)
+    x = synth.activations_i8(1, 1024, 62)[0]
+    x[synth.rng(63).random(1024) < 0.85] = 0
+    yref = oracle.spmm_i8(W, x.reshape(1, -1))[0]
+    y = _encode(W).spmspv(to_dev(x, DEV)).cpu().numpy()
+    np.testing.assert_array_equal(y.astype(np.int64), yref)
+
+
+# ------------------------------------------------------------------ host-buffer API
+
+def test_spmm_host_buffers():
+    W = synth.weights_f16(256, 512, 0.5, "uniform", 71)
+    X = synth.activations_f16(8, 512, 72)
+    A = _encode(W)
+    Xh = torch.from_numpy(X.view(np.float16)).pin_memory()
+    Yh = torch.empty((8, 256), dtype=torch.float16).pin_memory()
+    A.spmm_host(Xh, Yh)
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Yh.numpy(), Yref, S, "host")
+
+
+# ------------------------------------------------------------------ ABI errors
+
+def test_abi_error_paths():
+    W = synth.weights_f16(128, 128, 0.5, "uniform", 81)
+    Wd = to_dev_f16(W, DEV)
+    L = bsp.lib()
+    h = ctypes.c_void_p()
+    assert L.bsp_encode(Wd.data_ptr(), 0, 100, 128, None, ctypes.byref(h)) == 2
+    assert L.bsp_encode(Wd.data_ptr() + 2, 0, 64, 64, None, ctypes.byref(h)) == 4
+    A = bsp.BitmapMatrix(Wd)
+    X = torch.zeros((4, 128), dtype=torch.float16, device=DEV)
+    Y = torch.zeros((4, 128), dtype=torch.float16, device=DEV)
+    assert L.bsp_spmm(A.h, X.data_ptr(), 0, Y.data_ptr(), None) == 1
+    assert L.bsp_spmm(A.h, X.data_ptr() + 2, 1, Y.data_ptr(), None) == 4
+    assert L.bsp_spmm_scaled(A.h, X.data_ptr(), 1, Y.data_ptr(), Y.data_ptr(), None) == 3
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ full-size layers, sampled rows
+
+OPT13B = {"qkv": (15360, 5120), "out": (5120, 5120), "fc1": (20480, 5120), "fc2": (5120, 20480)}
+
+
+@pytest.mark.parametrize("layer", list(OPT13B))
+def test_opt13b_layers_sampled_rows(layer):
+    """Full OPT-13B-shaped layers at the benchmark's launch configuration;
+    the oracle checks 4 sampled rows of every 64-row strip, all N."""
+    M, K = OPT13B[layer]
+    li = list(OPT13B).index(layer)
+    W = synth.weights_f16(M, K, 0.5, "magnitude", synth.seed_for(2, li))
+    X = synth.activations_f16(16, K, synth.seed_for(2, 5))
+    A = _encode(W)
+    rows = sample_rows(M, 4, seed=li)
+    Yref, S = oracle.spmm_f16(W[rows], X)
+    for N in (1, 2, 8, 16):
+        Y = A.spmm(to_dev_f16(X[:N].copy(), DEV)).cpu().numpy()
+        assert_within_bound(Y[:, rows], Yref[:N], S[:N], f"{layer} N={N}")
+    if layer == "fc2":
+        x = synth.activations_relu_f16(K, synth.seed_for(2, 6))
+        yref, s = oracle.spmm_f16(W[rows], x.reshape(1, -1))
+        y = A.spmspv(to_dev_f16(x, DEV)).cpu().numpy()
+        assert_within_bound(y[rows], yref[0], s[0], "fc2 spmspv")
+
+
+def test_int8_full_size_sampled():
+    M, K = 4096, 11008
+    W = synth.weights_i8(M, K, 0.5, synth.seed_for(5, 0))
+    X = synth.activations_i8(16, K, synth.seed_for(5, 5))
+    rows = sample_rows(M, 4, seed=3)
+    Yref = oracle.spmm_i8(W[rows], X)
+    A = _encode(W)
+    for N in (1, 8, 16):
+        Y = A.spmm(to_dev(X[:N].copy(), DEV)).cpu().numpy()
+        np.testing.assert_array_equal(Y[:, rows].astype(np.int64), Yref[:N])
