@@ -48,6 +48,7 @@ SIGNATURES = {
     "bsp_info": (C.c_int, [_P, _P]),
     "bsp_decode": (C.c_int, [_P, _P, _P]),
     "bsp_export": (C.c_int, [_P, _P, _P, _P, _P]),
+    "bsp_check": (C.c_int, [_P, _P]),
 }
 
 
@@ -147,6 +148,10 @@ def bsp_export(h: int, bitmaps_ptr, offsets_ptr, values_ptr, stream: int = 0) ->
     _check("bsp_export", lib().bsp_export(h, bitmaps_ptr, offsets_ptr, values_ptr, stream))
 
 
+def bsp_check(h: int, stream: int = 0) -> None:
+    _check("bsp_check", lib().bsp_check(h, stream))
+
+
 # ---------------------------------------------------------------- tensor layer
 
 def _stream(stream):
@@ -221,6 +226,10 @@ class BitmapMatrix:
         bsp_export(self.h, bm.data_ptr(), off.data_ptr(), vals.data_ptr() if o.NNZ else None,
                    _stream(stream))
         return bm, off, vals
+
+    def check(self, stream=None):
+        """Synchronise and raise if a kernel on this handle gave up a wait."""
+        bsp_check(self.h, _stream(stream))
 
     # -- compute
     def _out(self, N, out, dtype):

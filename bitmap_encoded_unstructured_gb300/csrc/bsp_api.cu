@@ -36,6 +36,7 @@ void free_handle(bsp_handle* h)
     cudaFree(h->values);
     cudaFree(h->ws);
     cudaFree(h->counters);
+    cudaFree(h->err);
     cudaFree(h->stage_x);
     cudaFree(h->stage_y);
     h->magic = 0;
@@ -100,12 +101,14 @@ bsp_status_t bsp_encode(const void* W, bsp_dtype_t dtype, int64_t M, int64_t K,
     if (st != BSP_OK) { free_handle(h); return st; }
     const size_t ws_bytes = (size_t)BSP_DECODE_MAX_N * (size_t)M * 4;
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess ||
-        cudaMalloc(&h->counters, (size_t)(M / 64) * 4) != cudaSuccess) {
+        cudaMalloc(&h->counters, (size_t)(M / 64) * 4) != cudaSuccess ||
+        cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) {
         free_handle(h);
         return BSP_ERR_OOM;
     }
     if (cudaMemsetAsync(h->ws, 0, ws_bytes, s) != cudaSuccess ||
         cudaMemsetAsync(h->counters, 0, (size_t)(M / 64) * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         free_handle(h);
         return BSP_ERR_CUDA;
@@ -242,6 +245,20 @@ bsp_status_t bsp_export(bsp_handle_t h, uint64_t* bitmaps, uint32_t* offsets, vo
         cudaMemcpyAsync(values, h->values, (size_t)h->NNZ * bsp_elem_bytes(h->dtype), cudaMemcpyDefault, s) != cudaSuccess)
         return BSP_ERR_CUDA;
     return BSP_OK;
+}
+
+bsp_status_t bsp_check(bsp_handle_t h, bsp_stream_t stream)
+{
+    if (!valid(h)) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int e = 0;
+    if (cudaMemcpyAsync(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    return e ? (bsp_status_t)e : BSP_OK;
 }
 
 bsp_status_t bsp_decode(bsp_handle_t h, void* W_out, bsp_stream_t stream)

@@ -26,6 +26,9 @@ struct bsp_handle {
     // reads and clears its slice); one arrival counter per 64-row strip.
     void* ws;
     uint32_t* counters;
+    // device error word: a kernel whose bounded wait gave up stores
+    // BSP_ERR_TIMEOUT here; bsp_check reads and clears it
+    int* err;
     int num_sms;
     // staging for bsp_spmm_host, grown on demand
     void* stage_x;

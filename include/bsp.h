@@ -184,6 +184,15 @@ bsp_status_t bsp_export(bsp_handle_t h, uint64_t *bitmaps, uint32_t *offsets,
                         void *values, bsp_stream_t stream);
 
 /*
+ * Synchronise `stream` and report device-side failures of earlier calls on
+ * this handle: every wait inside the kernels is bounded, and a wait that
+ * gives up makes its kernel store BSP_ERR_TIMEOUT in the handle's error
+ * word and return early (its output is then incomplete).  Returns that
+ * status (and clears it), or BSP_OK.
+ */
+bsp_status_t bsp_check(bsp_handle_t h, bsp_stream_t stream);
+
+/*
  * Decode back to dense: W_out device row-major [M][K] (fp16 or int8 bits),
  * 16-B aligned.  decode(encode(W)) == W bit for bit.
  */

@@ -341,3 +341,39 @@ def test_int8_full_size_sampled():
     for N in (1, 8, 16):
         Y = A.spmm(to_dev(X[:N].copy(), DEV)).cpu().numpy()
         np.testing.assert_array_equal(Y[:, rows].astype(np.int64), Yref[:N])
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_check_ok_after_normal_calls():
+    W = synth.weights_f16(128, 256, 0.5, "uniform", 91)
+    A = _encode(W)
+    A.spmm(to_dev_f16(synth.activations_f16(2, 256, 92), DEV))
+    A.check()
+
+
+@pytest.mark.parametrize("spmspv", [False, True])
+def test_wait_that_runs_out_reports_timeout(spmspv, monkeypatch):
+    """Each warp's producer skips its first GT's copies (a barrier nothing
+    completes); the consumers' bounded wait gives up, the kernel records
+    BSP_ERR_TIMEOUT and returns; the context stays usable."""
+    W = synth.weights_f16(256, 1024, 0.5, "uniform", 93)
+    X = synth.activations_f16(1, 1024, 94)
+    A = _encode(W)
+    Xd = to_dev_f16(X, DEV)
+    monkeypatch.setenv("BSP_TEST_STALL", "1")
+    monkeypatch.setenv("BSP_SPIN_CAP", "2000")
+    if spmspv:
+        A.spmspv(Xd[0].contiguous())
+    else:
+        A.spmm(Xd)
+    with pytest.raises(bsp.BspError) as e:
+        A.check()
+    assert e.value.status == 7
+    monkeypatch.delenv("BSP_TEST_STALL")
+    monkeypatch.delenv("BSP_SPIN_CAP")
+    A.check()  # cleared
+    Y = A.spmm(Xd).cpu().numpy()
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Y, Yref, S, "after timeout")
+    A.check()
