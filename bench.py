@@ -50,10 +50,12 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def make_workload():
+def make_workload(only=None):
     """Host-side synthetic inputs (numpy, seeded)."""
     Ws, xs = {}, {}
     for i, (name, M, K) in enumerate(LAYERS):
+        if only and name not in only:
+            continue
         Ws[name] = synth.weights_f16(M, K, 0.5, "magnitude", synth.seed_for(2, i))
         xs[name] = synth.activations_f16(16, K, synth.seed_for(2, 10 + i))
     relu = synth.activations_relu_f16(LAYERS[3][2], synth.seed_for(2, 6))
@@ -65,12 +67,16 @@ def algorithmic_bytes(Ws, relu):
     out = {}
     stor = {}
     for name, M, K in LAYERS:
+        if name not in Ws:
+            continue
         nnz = int(np.count_nonzero(Ws[name]))
         ngt, nbt = (M // 64) * (K // 64), M * K // 64
         stor[name] = 4 * (ngt + 1) + 8 * nbt + 2 * nnz
         for N in NS:
             out[(name, N)] = stor[name] + 2 * K * N + 2 * M * N
     name, M, K = LAYERS[3]
+    if name not in Ws:
+        return out, stor, 0.0
     W = Ws[name]
     act = (relu.reshape(-1, 8).view(np.float16) != 0).any(axis=1)  # active K-octets
     nnz_active = int(np.count_nonzero(W.reshape(M, -1, 8)[:, act, :]))
@@ -207,6 +213,44 @@ def _config():
 
 
 # ---------------------------------------------------------------- GPU arm
+
+def run_case(args):
+    """One (layer, N) configuration only, for profiler captures: encode the
+    layer, run `warmup + steps` calls of bsp_spmm (or bsp_spmspv with N=0)."""
+    import torch
+    import bitmap_encoded_unstructured_gb300 as bsp
+    layer, n = args.case.split(":")
+    N = int(n)
+    Ws, xs, relu = make_workload(only={layer})
+    (name, M, K), = [l for l in LAYERS if l[0] == layer]
+    dev = torch.device("cuda", 0)
+    A = bsp.BitmapMatrix(torch.from_numpy(Ws[name].view(np.float16)).to(dev))
+    if N == 0:
+        x = torch.from_numpy(relu.view(np.float16)).to(dev) if name == "fc2" else \
+            torch.from_numpy(xs[name][0].view(np.float16).copy()).to(dev)
+        y = torch.empty(M, dtype=torch.float16, device=dev)
+        fn = lambda: A.spmspv(x, out=y)
+    else:
+        X = torch.from_numpy(xs[name][:N].view(np.float16).copy()).to(dev)
+        Y = torch.empty((N, M), dtype=torch.float16, device=dev)
+        fn = lambda: A.spmm(X, out=Y)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    A.check()
+    us = s.elapsed_time(e) * 1e3 / args.steps
+    stor = A.storage_bytes()
+    b = stor + 2 * K * max(N, 1) + 2 * M * max(N, 1)
+    print(json.dumps({"case": args.case, "us_per_call": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                      "note": "same layer every call: L2-warm for layers under 129 MB"}))
+    return 0
+
 
 def run_gpu(args):
     import torch
@@ -372,6 +416,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="LAYER:N, one configuration only (N=0: spMspV), for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -379,6 +425,8 @@ def main():
         return run_reference(args)
     from bitmap_encoded_unstructured_gb300.build import build_library
     build_library()
+    if args.case:
+        return run_case(args)
     return run_gpu(args)
 
 

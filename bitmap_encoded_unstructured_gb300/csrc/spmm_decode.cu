@@ -66,8 +66,8 @@ struct DecCfg {
     static constexpr int EB = I8 ? 1 : 2;
     static constexpr int E16 = 16 / EB;                // elements per 16-B chunk
     static constexpr int VAL_CHUNKS = 4096 / E16 + 1;  // dense GT + misalignment
-    static constexpr int XS = (NT >= 8) ? NT + 4 : NT; // widened X-tile row stride
-    static constexpr int VW = NT < 4 ? NT : 4;         // vector width of X-tile rows
+    static constexpr bool WIDE_X = !I8 && NT >= 4;     // fp32 X tile + packed fp32x2 FMA
+    static constexpr int XS = WIDE_X ? NT + 4 : 4;     // widened X-tile row stride (floats)
     static constexpr int XRAW = NT * 64 * EB;          // raw X tile bytes [NT][64]
     // stage layout
     static constexpr int ST_BM = 0;
@@ -81,34 +81,10 @@ struct DecCfg {
     static constexpr int W_BAR = W_BASE + 64 * 4;
     static constexpr int WARP_BYTES = (W_BAR + 2 * S * 8 + 15) & ~15;
     static constexpr int SMEM = WARPS * WARP_BYTES;
-    static_assert(64 * NT * 4 <= 64 * XS * 4, "reduction buffer must fit the X tile");
+    static constexpr int RED_BYTES = 64 * NT * 4;      // per-warp reduction buffer (aliases stage 0)
+    static_assert(RED_BYTES <= STAGE, "reduction buffer must fit a stage");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
-
-template <typename Acc, int VW>
-struct Vec;
-template <> struct Vec<float, 1> { using T = float; };
-template <> struct Vec<float, 2> { using T = float2; };
-template <> struct Vec<float, 4> { using T = float4; };
-template <> struct Vec<int, 1> { using T = int; };
-template <> struct Vec<int, 2> { using T = int2; };
-template <> struct Vec<int, 4> { using T = int4; };
-
-template <typename V, typename A, int W>
-__device__ __forceinline__ V pack_vec(const A* a)
-{
-    if constexpr (W == 1) return a[0];
-    else if constexpr (W == 2) return V{a[0], a[1]};
-    else return V{a[0], a[1], a[2], a[3]};
-}
-
-template <typename A, typename V>
-__device__ __forceinline__ A vec_get(const V& v, int e)
-{
-    if constexpr (std::is_same_v<V, A>) return v;
-    else if constexpr (sizeof(V) == 2 * sizeof(A)) return e == 0 ? v.x : v.y;
-    else return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
-}
 
 // two consecutive raw X elements from shared memory, widened
 __device__ __forceinline__ void x_pair(const uint8_t* xraw, int idx, float& a, float& b)
@@ -125,19 +101,6 @@ __device__ __forceinline__ void x_pair(const uint8_t* xraw, int idx, int& a, int
     b = (int)(int8_t)(v >> 8);
 }
 
-__device__ __forceinline__ float load_val(const uint8_t* vals, uint32_t i, float)
-{
-    return __half2float(reinterpret_cast<const __half*>(vals)[i]);
-}
-
-__device__ __forceinline__ int load_val(const uint8_t* vals, uint32_t i, int)
-{
-    return (int)reinterpret_cast<const int8_t*>(vals)[i];
-}
-
-__device__ __forceinline__ void mac(float& acc, float w, float x) { acc = fmaf(w, x, acc); }
-__device__ __forceinline__ void mac(int& acc, int w, int x) { acc += w * x; }
-
 __device__ __forceinline__ void write_out(void* Y, int, int64_t idx, float v, float)
 {
     reinterpret_cast<__half*>(Y)[idx] = __float2half_rn(v);
@@ -149,6 +112,154 @@ __device__ __forceinline__ void write_out(void* Y, int mode, int64_t idx, int v,
         reinterpret_cast<float*>(Y)[idx] = __fmul_rn(__int2float_rn(v), scale);
     else
         reinterpret_cast<int*>(Y)[idx] = v;
+}
+
+// fp32 += fp16 * fp16, one rounding (the fp16 product is exact in fp32)
+__device__ __forceinline__ void fma_f16(float& acc, uint16_t w, uint16_t x)
+{
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(w), "h"(x));
+}
+
+// packed pair of fp32 FMAs: acc.{lo,hi} += w * x.{lo,hi}
+__device__ __forceinline__ uint64_t ffma2(uint64_t acc, uint64_t ww, uint64_t x)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ww), "l"(x), "l"(acc));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t dup2(float w)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(w));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t half_of(const uint4& q, int c)
+{
+    const uint32_t w = c < 2 ? q.x : c < 4 ? q.y : c < 6 ? q.z : q.w;
+    return (uint16_t)((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+// Accumulator storage of one lane: rows l and l+32, NT columns of Y.
+template <int NT, bool I8, bool WIDE>
+struct Accum;
+template <int NT>
+struct Accum<NT, false, false> { float v[2][NT]; };
+template <int NT>
+struct Accum<NT, false, true> { uint64_t v[2][NT / 2]; };  // packed fp32 pairs
+template <int NT>
+struct Accum<NT, true, false> { int v[2][NT]; };
+
+// Decode one GroupTile and multiply it into the lane's two rows.
+//
+// Lane l owns GT rows l and l+32 (BT rows l/8 and l/8+4, BT row-byte l%8).
+// BT columns (K-octets) are taken in turn; inside one, the positions
+// c = 0..7 of the lane's row-byte are a static loop: a set bit loads the
+// next packed value (the masked popcount gives the row-byte's first slot,
+// then a running index), a clear bit contributes zero.  So all 32 lanes
+// run the same instruction stream, and X can sit in registers.
+template <int NT, bool I8, bool SKIP, typename A>
+__device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t* base_s,
+                                          const uint8_t* vals, const uint8_t* xraw, const float* x_s,
+                                          int N, uint32_t act8, int lane, A& acc)
+{
+    using C = DecCfg<NT, I8>;
+    const int rr = lane & 7;
+    const uint64_t lowmask = (1ull << (8 * rr)) - 1ull;
+#pragma unroll 1
+    for (int bc = 0; bc < 8; ++bc) {
+        if (SKIP && !((act8 >> bc) & 1u)) continue;
+        uint32_t byte[2], idx[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int gl = bt_local((lane >> 3) + 4 * h, bc);
+            const uint64_t bm = bm_st[gl];
+            byte[h] = (uint32_t)(bm >> (8 * rr)) & 0xFFu;
+            idx[h] = base_s[gl] + (uint32_t)__popcll(bm & lowmask);
+        }
+        if constexpr (I8) {
+            // dense int8 row-byte packed into two words, then dp4a per column of Y
+            const int8_t* v8 = reinterpret_cast<const int8_t*>(vals);
+            uint32_t xlo[NT], xhi[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const uint2 q = *reinterpret_cast<const uint2*>(xraw + n * 64 + 8 * bc);
+                xlo[n] = n < N ? q.x : 0u;
+                xhi[n] = n < N ? q.y : 0u;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t wlo = 0, whi = 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if ((byte[h] >> c) & 1u) {
+                        const uint32_t b = (uint32_t)(uint8_t)v8[idx[h]];
+                        ++idx[h];
+                        if (c < 4) wlo |= b << (8 * c);
+                        else whi |= b << (8 * (c - 4));
+                    }
+                }
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    acc.v[h][n] = __dp4a((int)wlo, (int)xlo[n], acc.v[h][n]);
+                    acc.v[h][n] = __dp4a((int)whi, (int)xhi[n], acc.v[h][n]);
+                }
+            }
+        } else if constexpr (!C::WIDE_X) {
+            // N <= 2: fp16 X octet in registers, mixed-precision FMA
+            const uint16_t* vh = reinterpret_cast<const uint16_t*>(vals);
+            uint4 xq[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                xq[n] = n < N ? *reinterpret_cast<const uint4*>(xraw + (n * 64 + 8 * bc) * 2) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint16_t w = 0;
+                    if ((byte[h] >> c) & 1u) {
+                        w = vh[idx[h]];
+                        ++idx[h];
+                    }
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) fma_f16(acc.v[h][n], w, half_of(xq[n], c));
+                }
+            }
+        } else {
+            // N >= 4: fp32 X rows (broadcast loads), packed fp32x2 FMA
+            const uint16_t* vh = reinterpret_cast<const uint16_t*>(vals);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint64_t xv[NT / 2];
+                const float* xr = x_s + (bc * 8 + c) * C::XS;
+#pragma unroll
+                for (int j = 0; j < NT / 2; j += 2) {
+                    const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(xr + 2 * j);
+                    xv[j] = q.x;
+                    xv[j + 1] = q.y;
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float w = 0.f;
+                    if ((byte[h] >> c) & 1u) {
+                        w = __half2float(__ushort_as_half(vh[idx[h]]));
+                        ++idx[h];
+                    }
+                    const uint64_t ww = dup2(w);
+#pragma unroll
+                    for (int j = 0; j < NT / 2; ++j) acc.v[h][j] = ffma2(acc.v[h][j], ww, xv[j]);
+                }
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ float ws_take(float* p) { return atomicExch(p, 0.0f); }
@@ -178,14 +289,13 @@ spmm_decode_kernel(const Args a)
 {
     using C = DecCfg<NT, I8>;
     using Acc = std::conditional_t<I8, int, float>;
-    using XV = typename Vec<Acc, C::VW>::T;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     uint8_t* wb = smem + warp * C::WARP_BYTES;
-    Acc* x_s = reinterpret_cast<Acc*>(wb + C::W_XS);
+    float* x_s = reinterpret_cast<float*>(wb + C::W_XS);
     uint32_t* base_s = reinterpret_cast<uint32_t*>(wb + C::W_BASE);
     uint64_t* bar_a = reinterpret_cast<uint64_t*>(wb + C::W_BAR);      // [S]: bitmaps+x (+values)
     uint64_t* bar_v = bar_a + C::S;                                      // [S]: values (spMspV)
@@ -236,11 +346,11 @@ spmm_decode_kernel(const Args a)
             bspx::bulk_g2s(st + C::ST_VAL, a.values + (int64_t)ch0 * 16, nch * 16, bar_a + s);
     };
 
-    Acc acc[2][NT];
+    Accum<NT, I8, C::WIDE_X> acc;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) acc[h][n] = Acc(0);
+        for (int n = 0; n < (C::WIDE_X ? NT / 2 : NT); ++n) acc.v[h][n] = 0;
 
     bool failed = false;
 
@@ -324,7 +434,7 @@ spmm_decode_kernel(const Args a)
             if (!__all_sync(0xFFFFFFFFu, bspx::mbar_wait_bounded(bar_a + s, ph, a.spin_cap))) { failed = true; break; }
         }
 
-        // BT value bases
+        // BT value bases: popcounts and a warp exclusive scan
         const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + C::ST_BM);
         const uint64_t b0 = bm_st[2 * lane], b1 = bm_st[2 * lane + 1];
         const uint32_t c0 = __popcll(b0), c1 = __popcll(b1);
@@ -335,62 +445,43 @@ spmm_decode_kernel(const Args a)
             if (lane >= d) incl += o;
         }
         const uint32_t ex = incl - (c0 + c1);
-        base_s[2 * lane] = ex;
-        base_s[2 * lane + 1] = ex + c0;
+        const uint32_t shift = o0 - (o0 / C::E16) * C::E16;
+        // bases are stored with the span misalignment folded in
+        base_s[2 * lane] = ex + shift;
+        base_s[2 * lane + 1] = ex + c0 + shift;
 
-        // X tile -> [64][XS] widened; lane owns columns 2*lane, 2*lane+1
         const uint8_t* xraw = st + C::ST_X;
-        Acc xa[NT], xb[NT];
+        if constexpr (C::WIDE_X) {
+            // X tile widened to fp32 [64][XS]; lane owns columns 2*lane, 2*lane+1
+            float xa[NT], xb[NT];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            if (n < N) {
-                x_pair(xraw, n * 64 + 2 * lane, xa[n], xb[n]);
-            } else {
-                xa[n] = Acc(0);
-                xb[n] = Acc(0);
+            for (int n = 0; n < NT; ++n) {
+                if (n < N) {
+                    x_pair(xraw, n * 64 + 2 * lane, xa[n], xb[n]);
+                } else {
+                    xa[n] = 0.f;
+                    xb[n] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NT; j += 4) {
+                *reinterpret_cast<float4*>(x_s + (2 * lane) * C::XS + j) = make_float4(xa[j], xa[j + 1], xa[j + 2], xa[j + 3]);
+                *reinterpret_cast<float4*>(x_s + (2 * lane + 1) * C::XS + j) = make_float4(xb[j], xb[j + 1], xb[j + 2], xb[j + 3]);
             }
         }
         uint32_t act8 = 0xFFu;
         if constexpr (SKIP) {
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (xa[0] != Acc(0)) || (xb[0] != Acc(0)));
+            // K-octet j is active iff one of x[8j .. 8j+7] is nonzero
+            Acc va, vb;
+            x_pair(xraw, 2 * lane, va, vb);
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (va != Acc(0)) || (vb != Acc(0)));
             act8 = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) act8 |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
         }
-#pragma unroll
-        for (int j = 0; j < NT; j += C::VW) {
-            *reinterpret_cast<XV*>(x_s + (2 * lane) * C::XS + j) = pack_vec<XV, Acc, C::VW>(xa + j);
-            *reinterpret_cast<XV*>(x_s + (2 * lane + 1) * C::XS + j) = pack_vec<XV, Acc, C::VW>(xb + j);
-        }
         __syncwarp();
 
-        const uint32_t shift = o0 - (o0 / C::E16) * C::E16;
-        const uint8_t* val_b = st + C::ST_VAL;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = lane + 32 * h;
-            const int br = r >> 3, rr = r & 7;
-#pragma unroll
-            for (int bc = 0; bc < 8; ++bc) {
-                if (SKIP && !((act8 >> bc) & 1u)) continue;
-                const int gl = bt_local(br, bc);
-                const uint64_t bm = bm_st[gl];
-                uint32_t byte = (uint32_t)(bm >> (8 * rr)) & 0xFFu;
-                uint32_t idx = base_s[gl] + (uint32_t)__popcll(bm & ((1ull << (8 * rr)) - 1ull)) + shift;
-                while (byte) {
-                    const int c = __ffs(byte) - 1;
-                    byte &= byte - 1;
-                    const Acc w = load_val(val_b, idx++, Acc(0));
-                    const Acc* xr = x_s + (bc * 8 + c) * C::XS;
-#pragma unroll
-                    for (int j = 0; j < NT; j += C::VW) {
-                        const XV xv = *reinterpret_cast<const XV*>(xr + j);
-#pragma unroll
-                        for (int e = 0; e < C::VW; ++e) mac(acc[h][j + e], w, vec_get<Acc>(xv, e));
-                    }
-                }
-            }
-        }
+        decode_gt<NT, I8, SKIP>(bm_st, base_s, st + C::ST_VAL, xraw, x_s, N, act8, lane, acc);
         __syncwarp();
 
         // refill this stage with GT i+S
@@ -415,11 +506,21 @@ spmm_decode_kernel(const Args a)
 
     // ---- CTA reduction over warps, then output or split-K accumulation
     __syncthreads();
-    Acc* red = x_s;
+    Acc* red = reinterpret_cast<Acc*>(wb + C::W_STAGES);  // stage 0 is free now
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 2; ++h) {
+        if constexpr (C::WIDE_X) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) red[(lane + 32 * h) * NT + n] = acc[h][n];
+            for (int j = 0; j < NT / 2; ++j) {
+                const float2 f = unpack2(acc.v[h][j]);
+                red[(lane + 32 * h) * NT + 2 * j] = f.x;
+                red[(lane + 32 * h) * NT + 2 * j + 1] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) red[(lane + 32 * h) * NT + n] = acc.v[h][n];
+        }
+    }
     __syncthreads();
 
     Acc* ws = reinterpret_cast<Acc*>(a.ws);
@@ -428,7 +529,7 @@ spmm_decode_kernel(const Args a)
         Acc sum = Acc(0);
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w)
-            sum += reinterpret_cast<const Acc*>(smem + w * C::WARP_BYTES + C::W_XS)[i];
+            sum += reinterpret_cast<const Acc*>(smem + w * C::WARP_BYTES + C::W_STAGES)[i];
         if (n < N) {
             const int64_t m = gi * 64 + r;
             if (a.splits == 1)
