@@ -135,14 +135,14 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_str
     cudaStream_t s = (cudaStream_t)stream;
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     if (N <= BSP_DECODE_MAX_N)
-        return bsp_run_spmm_decode(h, X, (int)N, Y, mode, nullptr, false, s);
+        return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, mode, nullptr, false, s);
     // Larger N: the decode kernel over column blocks of 16 tokens.
     const int eb = bsp_elem_bytes(h->dtype);
     const int ob = h->dtype == BSP_INT8 ? 4 : 2;
     for (int64_t n0 = 0; n0 < N; n0 += BSP_DECODE_MAX_N) {
         const int nb = (int)((N - n0) < BSP_DECODE_MAX_N ? (N - n0) : BSP_DECODE_MAX_N);
-        const bsp_status_t st = bsp_run_spmm_decode(
-            h, (const uint8_t*)X + n0 * h->K * eb, nb, (uint8_t*)Y + n0 * h->M * ob, mode, nullptr, false, s);
+ const bsp_status_t st = bsp_run_spmm_decode(
+            bsp_problem_of(h), (const uint8_t*)X + n0 * h->K * eb, nb, (uint8_t*)Y + n0 * h->M * ob, mode, nullptr, false, s);
         if (st != BSP_OK) return st;
     }
     return BSP_OK;
@@ -157,7 +157,7 @@ bsp_status_t bsp_spmm_scaled(bsp_handle_t h, const int8_t* X, int64_t N, const f
     if (!aligned16(X) || !aligned16(Y)) return BSP_ERR_ALIGN;
     DeviceGuard g(h->device);
     if (!g.ok) return BSP_ERR_CUDA;
-    return bsp_run_spmm_decode(h, X, (int)N, Y, BSP_OUT_F32_SCALED, row_scale, false,
+    return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, BSP_OUT_F32_SCALED, row_scale, false,
                                (cudaStream_t)stream);
 }
 
@@ -168,7 +168,7 @@ bsp_status_t bsp_spmspv(bsp_handle_t h, const void* x, void* y, bsp_stream_t str
     DeviceGuard g(h->device);
     if (!g.ok) return BSP_ERR_CUDA;
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
-    return bsp_run_spmm_decode(h, x, 1, y, mode, nullptr, true, (cudaStream_t)stream);
+    return bsp_run_spmm_decode(bsp_problem_of(h), x, 1, y, mode, nullptr, true, (cudaStream_t)stream);
 }
 
 bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,

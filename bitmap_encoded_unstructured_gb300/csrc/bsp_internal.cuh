@@ -47,13 +47,31 @@ bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s);
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s);
 
 // ---- CUDA-core decode-path product (spmm_decode.cu) ----
+// Everything the decode kernel reads and writes besides X and Y: the
+// encoded arrays, the shape, and the split-K scratch (workspace
+// [BSP_DECODE_MAX_N][M] fp32/int32 that is all zero between calls, one
+// arrival counter per 64-row strip, zeroed; an error word).
+struct bsp_decode_problem {
+    const uint64_t* bitmaps;
+    const uint32_t* offsets;
+    const void* values;
+    bsp_dtype_t dtype;
+    int64_t M, K;
+    int device, num_sms;
+    void* ws;
+    uint32_t* counters;
+    int* err;
+};
+
+bsp_decode_problem bsp_problem_of(const bsp_handle* h);
+
 // X: [N][K] (fp16 or int8), N in 1..BSP_DECODE_MAX_N.  Output by mode:
 // F16 -> Y half [N][M]; I32 -> Y int32 [N][M]; F32_SCALED -> Y float [N][M]
 // with row_scale[M].  skip_zero_octets: spMspV mode (N must be 1).
-bsp_status_t bsp_run_spmm_decode(const bsp_handle* h, const void* X, int N,
+bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int N,
                                  void* Y, bsp_out_mode mode,
                                  const float* row_scale, bool skip_zero_octets,
                                  cudaStream_t s);
 
-// Split-K factor chosen for a handle (exposed for tests and tuning).
-int bsp_decode_splits(const bsp_handle* h, int N);
+// Split-K factor chosen for a problem (exposed for tests and tuning).
+int bsp_decode_splits(const bsp_decode_problem& p, int N);
