@@ -49,6 +49,7 @@ SIGNATURES = {
     "bsp_decode": (C.c_int, [_P, _P, _P]),
     "bsp_export": (C.c_int, [_P, _P, _P, _P, _P]),
     "bsp_check": (C.c_int, [_P, _P]),
+    "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
 }
 
 
@@ -150,6 +151,14 @@ def bsp_export(h: int, bitmaps_ptr, offsets_ptr, values_ptr, stream: int = 0) ->
 
 def bsp_check(h: int, stream: int = 0) -> None:
     _check("bsp_check", lib().bsp_check(h, stream))
+
+
+def bsp_spmm_noalloc(bitmaps_ptr: int, offsets_ptr: int, values_ptr: int, dtype: int, M: int, K: int,
+                     X_ptr: int, N: int, Y_ptr: int, stream: int = 0) -> None:
+    """Decode-path product from caller-owned encoded arrays; allocates nothing
+    (for callers that may not call cudaMalloc).  See include/bsp.h."""
+    _check("bsp_spmm_noalloc", lib().bsp_spmm_noalloc(bitmaps_ptr, offsets_ptr, values_ptr, dtype, M, K,
+                                                      X_ptr, N, Y_ptr, stream))
 
 
 # ---------------------------------------------------------------- tensor layer

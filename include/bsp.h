@@ -198,6 +198,47 @@ bsp_status_t bsp_check(bsp_handle_t h, bsp_stream_t stream);
  */
 bsp_status_t bsp_decode(bsp_handle_t h, void *W_out, bsp_stream_t stream);
 
+/*
+ * Largest M that bsp_spmm_noalloc accepts.  Its scratch is a fixed
+ * [BSP_DECODE_MAX_N][BSP_NOALLOC_MAX_M] fp32 workspace plus one counter
+ * per 64 rows: about 2 MiB that every GPU which loads the library keeps
+ * until the process exits.
+ */
+#define BSP_NOALLOC_MAX_M 32768
+
+/*
+ * bsp_spmm_noalloc: Y = W * X on the decode path (1 <= N <= 16) without
+ * allocating anything.  The pages have no counterpart: this exists for
+ * callers that cannot call cudaMalloc, such as an operator that a host
+ * framework gives only its input and output buffers, a real-time loop in
+ * which allocation (and the device synchronisation of cudaFree) is not
+ * allowed, or code whose device memory must all come from an arena that a
+ * direct cudaMalloc would bypass.  Such a caller encodes once (bsp_encode)
+ * and keeps copies of the encoded arrays in its own memory (bsp_export), or
+ * receives them already encoded.
+ *   bitmaps  device u64 [M*K/64], 16-B aligned.
+ *   offsets  device u32 [M/64 * K/64 + 1], 4-B aligned.
+ *   values   device [NNZ] fp16 or int8, 16-B aligned, and readable for at
+ *            least 16 bytes past the last value (bulk copies read whole
+ *            16-B chunks); the slack bytes' contents do not matter.
+ *   X, Y     device [N][K] and [N][M] as for bsp_spmm (fp16 -> fp16,
+ *            int8 -> int32), 16-B aligned.
+ *   M, K     multiples of 64, M <= BSP_NOALLOC_MAX_M; N in 1..16.  Larger
+ *            M or N returns BSP_ERR_SHAPE before any device work.
+ * The split-K scratch is one array compiled into the library, shared by
+ * every call on a device; each call first clears the part it uses (on
+ * `stream`), so calls that overlap on the GPU (different streams, or other
+ * threads) race and must not be issued.  The first call on a device, with
+ * that device current, looks up the array's device address and zeroes it
+ * synchronously: make that first call before any stream capture.  Results
+ * match bsp_spmm.  A device-side wait that gives up leaves Y incomplete and
+ * is not reported here (bsp_spmm with bsp_check reports it).
+ */
+bsp_status_t bsp_spmm_noalloc(const uint64_t *bitmaps, const uint32_t *offsets,
+                              const void *values, bsp_dtype_t dtype, int64_t M,
+                              int64_t K, const void *X, int64_t N, void *Y,
+                              bsp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
