@@ -37,8 +37,14 @@ from bitmap_encoded_unstructured_gb300 import synth  # noqa: E402
 
 LAYERS = [("qkv", 15360, 5120), ("out", 5120, 5120), ("fc1", 20480, 5120), ("fc2", 5120, 20480)]
 NS = (1, 2, 8, 16)
+# Llama-2-70B FFN projections for the prefill leg (fp16, 50% uniform mask)
+PREFILL_LAYERS = [("llama_up", 28672, 8192), ("llama_down", 8192, 28672)]
+PREFILL_NS = (256, 1024, 4096)
 METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
+
+
+FALLBACK_TFLOPS = 1900.0
 
 
 def _peaks():
@@ -48,6 +54,23 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def _tensor_peak():
+    """Dense fp16 tensor peak: the measured bf16 burst figure (fp16 and bf16
+    have the same nominal dense rate), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (bf16 burst, same nominal rate as fp16)"
+    return FALLBACK_TFLOPS, "fallback"
+
+
+def prefill_weights(name, M, K):
+    i = [l[0] for l in PREFILL_LAYERS].index(name)
+    return synth.weights_f16(M, K, 0.5, "uniform", synth.seed_for(4, i))
 
 
 def make_workload(only=None):
@@ -221,9 +244,29 @@ def run_case(args):
     import bitmap_encoded_unstructured_gb300 as bsp
     layer, n = args.case.split(":")
     N = int(n)
+    dev = torch.device("cuda", 0)
+    if layer in dict((l[0], l) for l in PREFILL_LAYERS):
+        (name, M, K), = [l for l in PREFILL_LAYERS if l[0] == layer]
+        A = bsp.BitmapMatrix(torch.from_numpy(prefill_weights(name, M, K).view(np.float16)).to(dev))
+        X = torch.from_numpy(synth.activations_f16(N, K, synth.seed_for(4, 2)).view(np.float16)).to(dev)
+        Y = torch.empty((N, M), dtype=torch.float16, device=dev)
+        for _ in range(args.warmup):
+            A.spmm(X, out=Y)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            A.spmm(X, out=Y)
+        e.record()
+        torch.cuda.synchronize()
+        A.check()
+        us = s.elapsed_time(e) * 1e3 / args.steps
+        tf = 2.0 * M * K * N / (us * 1e-6) / 1e12
+        print(json.dumps({"case": args.case, "us_per_call": round(us, 2), "TFLOPs": round(tf, 1),
+                          "frac_tensor_peak": round(tf / _tensor_peak()[0], 4)}))
+        return 0
     Ws, xs, relu = make_workload(only={layer})
     (name, M, K), = [l for l in LAYERS if l[0] == layer]
-    dev = torch.device("cuda", 0)
     A = bsp.BitmapMatrix(torch.from_numpy(Ws[name].view(np.float16)).to(dev))
     if N == 0:
         x = torch.from_numpy(relu.view(np.float16)).to(dev) if name == "fc2" else \
@@ -374,6 +417,10 @@ def run_gpu(args):
                "note": "16 bsp_spmm_host calls per step (4 layers x N=1,2,8,16), pinned host X/Y, "
                        "H2D + kernel + D2H + stream sync per call"}
 
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill_leg(bsp, torch, dev, stream, ws)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = time_oracle(Ws, xs, relu, bpc, stor)
@@ -384,7 +431,7 @@ def run_gpu(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
                 "data": "synthetic (seeded numpy: N(0,0.02) weights, magnitude 50% mask, N(0,1) X)",
                 "config": _config(), "frac_hbm": round(value / ws / peak, 4),
-                "breakdown": breakdown, "prefill": None,
+                "breakdown": breakdown, "prefill": prefill,
                 "roofline": {"bound": "hbm", "kernel": "spmm_decode_kernel",
                              "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                              "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -397,6 +444,47 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_prefill_leg(bsp, torch, dev, stream, ws, reps=5):
+    """Prefill TFLOP/s (tcgen05 kernel) on the Llama-2-70B FFN shapes.
+
+    Executed flops = 2*M*K*N (the decoded tile is multiplied densely, zeros
+    included, as on the pages); useful flops = 2*NNZ*N.  Each (layer, N) is
+    timed over `reps` calls with CUDA events after 3 warm-up calls; the
+    encoded weight (264 MB) is larger than L2."""
+    peak, peak_kind = _tensor_peak()
+    out = {"unit": "TFLOP/s", "peak": peak, "peak_kind": peak_kind, "points": {}}
+    best = None
+    for name, M, K in PREFILL_LAYERS:
+        W = prefill_weights(name, M, K)
+        nnz = int(np.count_nonzero(W))
+        A = bsp.BitmapMatrix(torch.from_numpy(W.view(np.float16)).to(dev))
+        del W
+        for N in PREFILL_NS:
+            X = torch.from_numpy(synth.activations_f16(N, K, synth.seed_for(4, 2)).view(np.float16)).to(dev)
+            Y = torch.empty((N, M), dtype=torch.float16, device=dev)
+            for _ in range(3):
+                A.spmm(X, out=Y, stream=stream)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s.record(stream)
+            for _ in range(reps):
+                A.spmm(X, out=Y, stream=stream)
+            e.record(stream)
+            torch.cuda.synchronize()
+            ms = _max_over_ranks(s.elapsed_time(e) / reps, ws)
+            tf = 2.0 * M * K * N / (ms * 1e-3) / 1e12
+            out["points"][f"{name} {M}x{K} N={N}"] = {
+                "ms": round(ms, 4), "TFLOPs": round(tf, 1), "frac": round(tf / peak, 4),
+                "useful_TFLOPs": round(2.0 * nnz * N / (ms * 1e-3) / 1e12, 1)}
+            if best is None or tf > best[0]:
+                best = (tf, f"{name} N={N}")
+            del X, Y
+        A.check()
+        A.close()
+    out["best"] = {"TFLOPs": round(best[0], 1), "frac": round(best[0] / peak, 4), "at": best[1]}
+    return out
 
 
 def _kernel_hash():
@@ -416,6 +504,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--case", default=None,
                     help="LAYER:N, one configuration only (N=0: spMspV), for profiler captures")
     args = ap.parse_args()

@@ -136,7 +136,9 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_str
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     if (N <= BSP_DECODE_MAX_N)
         return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, mode, nullptr, false, s);
-    // Larger N: the decode kernel over column blocks of 16 tokens.
+    // Larger N, fp16: the tcgen05 prefill kernel.
+    if (h->dtype == BSP_FP16) return bsp_run_spmm_prefill(bsp_problem_of(h), X, N, Y, s);
+    // Larger N, int8 (no int8 tensor-core path): the decode kernel over column blocks of 16 tokens.
     const int eb = bsp_elem_bytes(h->dtype);
     const int ob = h->dtype == BSP_INT8 ? 4 : 2;
     for (int64_t n0 = 0; n0 < N; n0 += BSP_DECODE_MAX_N) {

@@ -75,3 +75,8 @@ bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int
 
 // Split-K factor chosen for a problem (exposed for tests and tuning).
 int bsp_decode_splits(const bsp_decode_problem& p, int N);
+
+// ---- tcgen05 prefill-path product (spmm_prefill.cu), fp16 only ----
+// X: [N][K] fp16, Y: [N][M] fp16, any N >= 1 (used for N > BSP_DECODE_MAX_N).
+bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
+                                  cudaStream_t s);

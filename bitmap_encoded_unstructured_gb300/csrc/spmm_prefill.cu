@@ -1,0 +1,412 @@
+// Prefill-path product Y = W * X for N > 16 on the 5th-generation tensor
+// cores (tcgen05), fp16 inputs, fp32 accumulation in tensor memory.
+//
+// Method: "load as sparse, compute as dense" ("Unified Static-Dynamic
+// Pruning for Efficient LLM Inference", section 4.3; "SpInfer: How bitmaps
+// make sparse LLMs actually fast", sections "Shared Memory Bitmap Decoding
+// (SMBD)" and "The async pipeline"): the compressed GroupTiles are streamed
+// into shared memory, decoded into a dense fp16 tile there, and that tile
+// feeds a dense tensor-core contraction.  Where the pages decode into mma
+// register fragments (and SPDP adds a transpose stage), here the decoder
+// warps write each 8-element row-byte of a BitmapTile as one 16-byte chunk
+// straight into the K-major 128-byte-swizzled shared-memory layout that
+// tcgen05.mma reads: a BT row-byte is exactly one swizzle chunk.
+//
+// CTA tile: 128 rows of W (two GT row strips) x 256 columns of Y (tokens);
+// one GT column (K = 64) per pipeline step, 3 stages:
+//   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB)
+//   B  X tile           256 x 64 fp16, K-major, SWIZZLE_128B (32 KB, TMA)
+//   C  compressed data  bitmaps + value spans of the two GTs (bulk copies)
+// Warp roles (10 warps):
+//   warp 0     producer: TMA tensor load of B, bulk copies of C, per stage
+//              on a "full" mbarrier; waits the stage's "empty" barrier.
+//   warp 1     allocates 256 TMEM columns; lane 0 issues 4 x
+//              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) per
+//              step and commits them to the stage's "empty" barrier.
+//   warps 2-9  decoders: each takes one GT and a quarter of its rows, scans
+//              the BT popcounts (shfl) for the value bases and writes the
+//              dense row-bytes into A; then arrive on "a_full".
+//   warps 4-7  after the K loop: epilogue, tcgen05.ld of their TMEM lane
+//              quadrant, fp32 -> fp16, stores to Y[n][m].
+// Every wait is bounded; a wait that gives up stores BSP_ERR_TIMEOUT in the
+// error word, and the CTA still drains its copies, waits for its MMAs and
+// frees its tensor memory before it exits.
+#include "bsp_internal.cuh"
+#include "bsp_ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <mutex>
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int S = 3;
+constexpr int A_BYTES = BM * BK * 2;          // 16384
+constexpr int B_BYTES = BN * BK * 2;          // 32768
+constexpr int VAL_BYTES = 513 * 16;           // dense GT value span + misalignment
+constexpr int SLOT = 512 + VAL_BYTES;         // bitmaps + values of one GT
+constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_C = A_BYTES + B_BYTES;
+constexpr int OFF_H = OFF_C + 2 * SLOT;       // stage header: shifts, second-GT flag
+constexpr int STAGE = ((OFF_H + 16) + 1023) & ~1023;
+constexpr int DEC_WARPS = 8;
+constexpr int WARPS = 2 + DEC_WARPS;
+constexpr int THREADS = WARPS * 32;
+constexpr int OFF_BASE = S * STAGE;           // decoder warps' BT bases, 64 u32 each
+constexpr int OFF_BAR = OFF_BASE + DEC_WARPS * 256;
+constexpr int NBAR = 3 * S + 1;               // full[S], a_full[S], empty[S], acc
+constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr int SMEM_USED = OFF_TMEM + 16;
+constexpr int SMEM = SMEM_USED + 1024;        // slack to align the base to 1024 B
+constexpr uint32_t TMEM_COLS = 256;
+static_assert(SMEM <= 227 * 1024, "shared memory");
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte
+// swizzled canonical layout: rows of 128 B, 8-row atoms of 1 KB (stride
+// 1024 B between atoms), atoms 1024-B aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
+    d |= (uint64_t)1u << 16;                         // leading offset (unused for swizzled K-major)
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;   // stride offset: 1024 B between 8-row atoms
+    d |= (uint64_t)1u << 46;                         // descriptor version of sm_100
+    d |= (uint64_t)2u << 61;                         // SWIZZLE_128B
+    return d;
+}
+
+__device__ __forceinline__ int bt_local(int br, int bc)
+{
+    return (((br >> 1) * 4 + (bc >> 1)) << 2) + (br & 1) + ((bc & 1) << 1);
+}
+
+struct PrefillArgs {
+    const uint64_t* bitmaps;
+    const uint32_t* offsets;
+    const uint8_t* values;
+    __half* Y;
+    int64_t M, N, K;
+    int* err;
+    uint32_t spin_cap;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            bspx::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bspx::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bspx::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane (32x32b shape, x32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-B alignment of the shared-window offset (the 128-B swizzle atoms)
+    uint8_t* smem = smem_raw + ((1024u - (bspx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr uint32_t FULL = 0xFFFFFFFFu;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* a_full = full + S;
+    uint64_t* empty = full + 2 * S;
+    uint64_t* acc_bar = full + 3 * S;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+
+    const int64_t M = a.M, N = a.N, K = a.K;
+    const int64_t KT = K >> 6;
+    const int64_t mt = blockIdx.y;
+    const int64_t n0 = (int64_t)blockIdx.x * BN;
+    const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
+    const bool has_b = strip1 * 64 < M;  // second GT row strip of the tile exists
+    const uint32_t cap = a.spin_cap;
+
+    if (warp == 1) {
+        // allocate the accumulator: 128 lanes x 256 fp32 columns
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         bspx::smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            bspx::mbar_init(full + s, 1);
+            bspx::mbar_init(a_full + s, DEC_WARPS);
+            bspx::mbar_init(empty + s, 1);
+        }
+        bspx::mbar_init(acc_bar, 1);
+        bspx::fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    bool failed = false;
+
+    if (warp == 0) {
+        // ---------------- producer
+        const int64_t ta = strip0 * KT, tb = strip1 * KT;
+        uint32_t offa = 0, offb = 0;
+        int64_t wbase = -64;
+        int64_t issued = 0;
+        for (int64_t kb = 0; kb < KT; ++kb) {
+            const int s = (int)(kb % S);
+            if (kb >= S) {
+                const uint32_t ph = (uint32_t)(((kb / S) - 1) & 1);
+                if (!__all_sync(FULL, bspx::mbar_wait_bounded(empty + s, ph, cap))) { failed = true; break; }
+            }
+            if (kb - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
+                wbase = kb;
+                const int64_t i = wbase + lane;
+                offa = (i <= KT) ? __ldg(a.offsets + ta + i) : 0u;
+                offb = (has_b && i <= KT) ? __ldg(a.offsets + tb + i) : 0u;
+            }
+            const int w = (int)(kb - wbase);
+            const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
+            const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
+            if (lane == 0) {
+                uint8_t* st = smem + s * STAGE;
+                uint32_t* hdr = reinterpret_cast<uint32_t*>(st + OFF_H);
+                const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
+                const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                hdr[0] = oa0 - cha * 8;
+                hdr[1] = ob0 - chb * 8;
+                uint32_t bytes = B_BYTES + 512 + nca * 16;
+                if (has_b) bytes += 512 + ncb * 16;
+                bspx::mbar_arrive_expect_tx(full + s, bytes);
+                tma_load_2d(st + OFF_B, &tmX, (int)(kb * BK), (int)n0, full + s);
+                bspx::bulk_g2s(st + OFF_C, a.bitmaps + (ta + kb) * 64, 512, full + s);
+                if (nca) bspx::bulk_g2s(st + OFF_C + 512, a.values + (int64_t)cha * 16, nca * 16, full + s);
+                if (has_b) {
+                    bspx::bulk_g2s(st + OFF_C + SLOT, a.bitmaps + (tb + kb) * 64, 512, full + s);
+                    if (ncb)
+                        bspx::bulk_g2s(st + OFF_C + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, full + s);
+                }
+            }
+            issued = kb + 1;
+        }
+        // let the last copies land before the CTA can exit (bounded)
+        for (int64_t kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+            bspx::mbar_wait_bounded(full + (kb % S), (uint32_t)((kb / S) & 1), cap);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        for (int64_t kb = 0; kb < KT; ++kb) {
+            const int s = (int)(kb % S);
+            const uint32_t ph = (uint32_t)((kb / S) & 1);
+            const bool ok = bspx::mbar_wait_bounded(a_full + s, ph, cap) && bspx::mbar_wait_bounded(full + s, ph, cap);
+            if (!__all_sync(FULL, ok)) { failed = true; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t abase = bspx::smem_u32(smem + s * STAGE + OFF_A);
+                const uint32_t bbase = bspx::smem_u32(smem + s * STAGE + OFF_B);
+                const uint64_t ad = smem_desc_sw128(abase), bd = smem_desc_sw128(bbase);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
+                    umma_f16(tmem_base, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), (kb | j) ? 1u : 0u);
+                umma_commit(empty + s);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
+        __syncwarp();
+        bspx::mbar_wait_bounded(acc_bar, 0, cap);
+    } else {
+        // ---------------- decoders
+        const int dw = warp - 2;
+        const int gsel = dw >> 2, q = dw & 3;
+        uint32_t* base_s = reinterpret_cast<uint32_t*>(smem + OFF_BASE + dw * 256);
+        const int row = 16 * q + (lane & 15);       // row inside the GT
+        const int trow = 64 * gsel + row;           // row inside the 128-row tile
+        const int br = row >> 3, rr = row & 7;
+        const int bc0 = 4 * (lane >> 4);
+        const uint32_t rsh = 8u * (uint32_t)(rr & 3);
+        const bool hi = rr >= 4;
+        const uint32_t lowm = (1u << rsh) - 1u;
+        const bool active = gsel == 0 || has_b;
+        for (int64_t kb = 0; kb < KT; ++kb) {
+            const int s = (int)(kb % S);
+            const uint32_t ph = (uint32_t)((kb / S) & 1);
+            if (!__all_sync(FULL, bspx::mbar_wait_bounded(full + s, ph, cap))) { failed = true; break; }
+            uint8_t* st = smem + s * STAGE;
+            if (active) {
+                const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + OFF_C + gsel * SLOT);
+                const uint16_t* vh = reinterpret_cast<const uint16_t*>(st + OFF_C + gsel * SLOT + 512);
+                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + OFF_H)[gsel];
+                const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(bm_st)[lane];
+                const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
+                uint32_t incl = c0 + c1;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t o = __shfl_up_sync(FULL, incl, d);
+                    if (lane >= d) incl += o;
+                }
+                const uint32_t ex = incl - (c0 + c1) + shift;
+                base_s[2 * lane] = ex;
+                base_s[2 * lane + 1] = ex + c0;
+                __syncwarp();
+                uint8_t* arow = st + OFF_A + (trow >> 3) * 1024 + (trow & 7) * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int bc = bc0 + j;
+                    const int g = bt_local(br, bc);
+                    const uint2 bm = *reinterpret_cast<const uint2*>(bm_st + g);
+                    const uint32_t w32 = hi ? bm.y : bm.x;
+                    const uint32_t byte = (w32 >> rsh) & 0xFFu;
+                    uint32_t idx = base_s[g] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
+                    uint32_t h[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t bit = (byte >> c) & 1u;
+                        uint32_t v = 0;
+                        if (bit) v = vh[idx];
+                        idx += bit;
+                        h[c] = v;
+                    }
+                    const uint4 chunk = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                                   h[6] | (h[7] << 16));
+                    // row-byte = one 16-B chunk; 128-B swizzle: chunk index ^ (row % 8)
+                    *reinterpret_cast<uint4*>(arow + ((bc ^ (trow & 7)) << 4)) = chunk;
+                }
+                __syncwarp();
+            }
+            // make the generic-proxy writes of A visible to the tensor cores
+            bspx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) bspx::mbar_arrive(a_full + s);
+        }
+        // ---------------- epilogue (warps 4-7 own TMEM lane quadrants 0-3)
+        if (warp >= 4 && warp < 8) {
+            const bool ok = __all_sync(FULL, bspx::mbar_wait_bounded(acc_bar, 0, cap));
+            if (!ok) {
+                failed = true;
+            } else if (!failed) {
+                tc_fence_after();
+                const int quad = warp & 3;
+                const int64_t m = mt * BM + 32 * quad + lane;
+#pragma unroll 1
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(32 * quad) << 16) + (uint32_t)(cb * 32), r);
+                    if (m < M) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int64_t n = n0 + cb * 32 + j;
+                            if (n < N) a.Y[n * M + m] = __float2half_rn(__uint_as_float(r[j]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    if (failed && lane == 0) atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
+{
+    if (p.dtype != BSP_FP16) return BSP_ERR_DTYPE;
+    if (N < 1 || N > (int64_t)0x7FFFFFFF || p.K > (int64_t)0x7FFFFFFF) return BSP_ERR_INVALID_ARG;
+    auto encode = get_encode_fn();
+    if (!encode) return BSP_ERR_CUDA;
+    // X: [N][K] fp16, K contiguous; box = 64 (K) x 256 (N) with the 128-B swizzle
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BSP_ERR_INVALID_ARG;
+    static bool attr_done[64] = {};
+    if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
+    if (!attr_done[p.device]) {
+        if (cudaFuncSetAttribute(spmm_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+            cudaSuccess)
+            return BSP_ERR_CUDA;
+        attr_done[p.device] = true;
+    }
+    PrefillArgs a;
+    a.bitmaps = p.bitmaps;
+    a.offsets = p.offsets;
+    a.values = (const uint8_t*)p.values;
+    a.Y = (__half*)Y;
+    a.M = p.M;
+    a.N = N;
+    a.K = p.K;
+    a.err = p.err;
+    a.spin_cap = bspx::kSpinCap;
+    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM));
+    spmm_prefill_kernel<<<grid, THREADS, SMEM, s>>>(map, a);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}

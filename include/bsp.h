@@ -116,8 +116,10 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  *   X  device [N][K], fp16 (BSP_FP16 handle) or int8 (BSP_INT8), 16-B aligned.
  *   Y  device [N][M], fp16 (BSP_FP16) or int32 (BSP_INT8), 16-B aligned.
  *   N  >= 1.  N <= BSP_DECODE_MAX_N runs the CUDA-core decode kernel
- *      (split-K over GroupTiles, fp32 / int32 accumulation); larger N runs
- *      the tcgen05 tensor-core kernel (fp16 only; BSP_ERR_DTYPE for int8).
+ *      (split-K over GroupTiles, fp32 / int32 accumulation).  Larger N:
+ *      fp16 runs the tcgen05 tensor-core prefill kernel (decoded tiles, fp32
+ *      accumulation in tensor memory); int8 runs the decode kernel over
+ *      blocks of 16 columns (there is no int8 tensor-core path).
  * fp16: Y = fp16(round-to-nearest of an fp32 sum in unspecified order).
  * int8: Y is the exact int32 sum.
  */

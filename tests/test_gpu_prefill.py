@@ -1,0 +1,76 @@
+"""GPU parity of the tcgen05 prefill path (fp16, N > 16) against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import bitmap_encoded_unstructured_gb300 as bsp
+from bitmap_encoded_unstructured_gb300 import synth
+
+from helpers import assert_within_bound, sample_rows, to_dev_f16
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+DEV = torch.device("cuda:0")
+
+
+def _run(W, X):
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    Y = A.spmm(to_dev_f16(X, DEV))
+    A.check()
+    return Y.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 32),      # one k-block, one ragged N tile
+                                   (128, 320, 256),    # more k-blocks than stages
+                                   (192, 256, 17),     # M % 128 == 64: half tile
+                                   (384, 640, 300),    # two N tiles, the second ragged
+                                   (256, 1024, 513)])
+def test_prefill_small_shapes(M, K, N):
+    W = synth.weights_f16(M, K, 0.5, "uniform", 300 + M + K + N)
+    X = synth.activations_f16(N, K, 301 + N)
+    Y = _run(W, X)
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(Y, Yref, S, f"prefill {M}x{K} N={N}")
+
+
+def test_prefill_small_integers_exact():
+    """Every partial sum is a small integer: one correct fp16 result."""
+    W = synth.small_int_f16((256, 256), -8, 8, seed=311, sparsity=0.5)
+    X = synth.small_int_f16((40, 256), -8, 8, seed=312)
+    Y = _run(W, X).astype(np.float64)
+    Yref, _ = oracle.spmm_f16(W, X)
+    np.testing.assert_array_equal(Y, Yref)
+
+
+@pytest.mark.parametrize("s", [0.0, 0.3, 0.7])
+def test_prefill_sparsity_levels(s):
+    W = synth.weights_f16(256, 512, s, "uniform" if s else "none", 320 + int(10 * s))
+    X = synth.activations_f16(64, 512, 321)
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(_run(W, X), Yref, S, f"prefill s={s}")
+
+
+def test_prefill_all_zero_weight():
+    W = np.zeros((128, 256), dtype=np.uint16)
+    X = synth.activations_f16(33, 256, 331)
+    assert np.all(_run(W, X) == 0)
+
+
+@pytest.mark.parametrize("M,K", [(28672, 8192), (8192, 28672)])
+def test_prefill_llama70b_ffn_sampled_rows(M, K):
+    """Llama-2-70B FFN shapes at 50%, N = 256, the oracle on 2 sampled rows
+    of every 64-row strip."""
+    W = synth.weights_f16(M, K, 0.5, "uniform", synth.seed_for(4, 0 if M > K else 1))
+    X = synth.activations_f16(256, K, synth.seed_for(4, 2))
+    Y = _run(W, X)
+    rows = sample_rows(M, 2, seed=M)
+    Yref, S = oracle.spmm_f16(W[rows], X)
+    assert_within_bound(Y[:, rows], Yref, S, f"llama {M}x{K}")
