@@ -42,26 +42,33 @@
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int S = 3;
+constexpr int BM = 128, BN = 256, BK = 64;    // BN: columns of one MMA / one TMEM accumulator
 constexpr int A_BYTES = BM * BK * 2;          // 16384
-constexpr int B_BYTES = BN * BK * 2;          // 32768
+constexpr int B_BYTES = BN * BK * 2;          // 32768 per 256-column sub-tile
 constexpr int VAL_BYTES = 513 * 16;           // dense GT value span + misalignment
 constexpr int SLOT = 512 + VAL_BYTES;         // bitmaps + values of one GT
-constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_C = A_BYTES + B_BYTES;
-constexpr int OFF_H = OFF_C + 2 * SLOT;       // stage header: shifts, second-GT flag
-constexpr int STAGE = ((OFF_H + 16) + 1023) & ~1023;
 constexpr int DEC_WARPS = 8;
 constexpr int WARPS = 2 + DEC_WARPS;
 constexpr int THREADS = WARPS * 32;
-constexpr int OFF_BASE = S * STAGE;           // decoder warps' BT bases, 64 u32 each
-constexpr int OFF_BAR = OFF_BASE + DEC_WARPS * 256;
-constexpr int NBAR = 3 * S + 1;               // full[S], a_full[S], empty[S], acc
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-constexpr int SMEM_USED = OFF_TMEM + 16;
-constexpr int SMEM = SMEM_USED + 1024;        // slack to align the base to 1024 B
-constexpr uint32_t TMEM_COLS = 256;
-static_assert(SMEM <= 227 * 1024, "shared memory");
+
+// NSUB 256-column sub-tiles of N per CTA, each with its own TMEM
+// accumulator: every decoded A tile feeds NSUB x 4 MMAs.
+template <int NSUB>
+struct PCfg {
+    static constexpr int S = NSUB == 1 ? 3 : 2;  // pipeline stages
+    static constexpr int BN_CTA = BN * NSUB;
+    static constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_C = A_BYTES + NSUB * B_BYTES;
+    static constexpr int OFF_H = OFF_C + 2 * SLOT;  // stage header: the two span shifts
+    static constexpr int STAGE = ((OFF_H + 16) + 1023) & ~1023;
+    static constexpr int OFF_BASE = S * STAGE;      // decoder warps' BT bases, 64 u32 each
+    static constexpr int OFF_BAR = OFF_BASE + DEC_WARPS * 256;
+    static constexpr int NBAR = 3 * S + 1;          // full[S], a_full[S], empty[S], acc
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_USED = OFF_TMEM + 16;
+    static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the base to 1024 B
+    static constexpr uint32_t TMEM_COLS = 256 * NSUB;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
 // N = 256, M = 128.
@@ -141,9 +148,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <int NSUB>
 __global__ void __launch_bounds__(THREADS, 1)
 spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a)
 {
+    using P = PCfg<NSUB>;
+    constexpr int S = P::S, STAGE = P::STAGE, OFF_A = P::OFF_A, OFF_B = P::OFF_B, OFF_C = P::OFF_C;
+    constexpr int OFF_H = P::OFF_H, OFF_BASE = P::OFF_BASE, OFF_BAR = P::OFF_BAR, OFF_TMEM = P::OFF_TMEM;
+    constexpr uint32_t TMEM_COLS = P::TMEM_COLS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-B alignment of the shared-window offset (the 128-B swizzle atoms)
     uint8_t* smem = smem_raw + ((1024u - (bspx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -160,7 +172,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     const int64_t M = a.M, N = a.N, K = a.K;
     const int64_t KT = K >> 6;
     const int64_t mt = blockIdx.y;
-    const int64_t n0 = (int64_t)blockIdx.x * BN;
+    const int64_t n0 = (int64_t)blockIdx.x * P::BN_CTA;
     const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
     const bool has_b = strip1 * 64 < M;  // second GT row strip of the tile exists
     const uint32_t cap = a.spin_cap;
@@ -216,10 +228,11 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
                 hdr[0] = oa0 - cha * 8;
                 hdr[1] = ob0 - chb * 8;
-                uint32_t bytes = B_BYTES + 512 + nca * 16;
+                uint32_t bytes = NSUB * B_BYTES + 512 + nca * 16;
                 if (has_b) bytes += 512 + ncb * 16;
                 bspx::mbar_arrive_expect_tx(full + s, bytes);
-                tma_load_2d(st + OFF_B, &tmX, (int)(kb * BK), (int)n0, full + s);
+                for (int u = 0; u < NSUB; ++u)
+                    tma_load_2d(st + OFF_B + u * B_BYTES, &tmX, (int)(kb * BK), (int)(n0 + u * BN), full + s);
                 bspx::bulk_g2s(st + OFF_C, a.bitmaps + (ta + kb) * 64, 512, full + s);
                 if (nca) bspx::bulk_g2s(st + OFF_C + 512, a.values + (int64_t)cha * 16, nca * 16, full + s);
                 if (has_b) {
@@ -242,12 +255,15 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t abase = bspx::smem_u32(smem + s * STAGE + OFF_A);
-                const uint32_t bbase = bspx::smem_u32(smem + s * STAGE + OFF_B);
-                const uint64_t ad = smem_desc_sw128(abase), bd = smem_desc_sw128(bbase);
+                const uint64_t ad = smem_desc_sw128(bspx::smem_u32(smem + s * STAGE + OFF_A));
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
-                    umma_f16(tmem_base, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), (kb | j) ? 1u : 0u);
+                for (int u = 0; u < NSUB; ++u) {
+                    const uint64_t bd = smem_desc_sw128(bspx::smem_u32(smem + s * STAGE + OFF_B + u * B_BYTES));
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
+                        umma_f16(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
+                                 (kb | j) ? 1u : 0u);
+                }
                 umma_commit(empty + s);
             }
             __syncwarp();
@@ -260,10 +276,17 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         const int dw = warp - 2;
         const int gsel = dw >> 2, q = dw & 3;
         uint32_t* base_s = reinterpret_cast<uint32_t*>(smem + OFF_BASE + dw * 256);
+        // lane: row 16q + (lane & 15) of the GT, octets 2p + half (p = 0..3), so
+        // one step of a warp reads a single TCTile (rows 16q.., octets 2p, 2p+1)
         const int row = 16 * q + (lane & 15);       // row inside the GT
         const int trow = 64 * gsel + row;           // row inside the 128-row tile
         const int br = row >> 3, rr = row & 7;
-        const int bc0 = 4 * (lane >> 4);
+        const int half = lane >> 4;
+        // The two half-warps read the two column halves of a TCTile, about
+        // 32 words apart: one bank cycle.  The upper half walks its
+        // positions rotated by 4 (4..7 then 0..3) so that the lanes of one
+        // step do not meet in the same bank.
+        const bool rot = half != 0;
         const uint32_t rsh = 8u * (uint32_t)(rr & 3);
         const bool hi = rr >= 4;
         const uint32_t lowm = (1u << rsh) - 1u;
@@ -292,23 +315,27 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 uint8_t* arow = st + OFF_A + (trow >> 3) * 1024 + (trow & 7) * 128;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int bc = bc0 + j;
+                    const int bc = 2 * j + half;
                     const int g = bt_local(br, bc);
                     const uint2 bm = *reinterpret_cast<const uint2*>(bm_st + g);
                     const uint32_t w32 = hi ? bm.y : bm.x;
                     const uint32_t byte = (w32 >> rsh) & 0xFFu;
-                    uint32_t idx = base_s[g] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
+                    const uint32_t start = base_s[g] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
+                    const uint32_t rbyte = rot ? ((byte >> 4) | (byte << 4)) & 0xFFu : byte;
+                    uint32_t idx = rot ? start + (uint32_t)__popc(byte & 0xFu) : start;
                     uint32_t h[8];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint32_t bit = (byte >> c) & 1u;
+                        if (c == 4 && rot) idx = start;
+                        const uint32_t bit = (rbyte >> c) & 1u;
                         uint32_t v = 0;
                         if (bit) v = vh[idx];
                         idx += bit;
                         h[c] = v;
                     }
-                    const uint4 chunk = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                                                   h[6] | (h[7] << 16));
+                    const uint32_t w0 = h[0] | (h[1] << 16), w1 = h[2] | (h[3] << 16);
+                    const uint32_t w2 = h[4] | (h[5] << 16), w3 = h[6] | (h[7] << 16);
+                    const uint4 chunk = rot ? make_uint4(w2, w3, w0, w1) : make_uint4(w0, w1, w2, w3);
                     // row-byte = one 16-B chunk; 128-B swizzle: chunk index ^ (row % 8)
                     *reinterpret_cast<uint4*>(arow + ((bc ^ (trow & 7)) << 4)) = chunk;
                 }
@@ -329,7 +356,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const int quad = warp & 3;
                 const int64_t m = mt * BM + 32 * quad + lane;
 #pragma unroll 1
-                for (int cb = 0; cb < BN / 32; ++cb) {
+                for (int cb = 0; cb < P::BN_CTA / 32; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tmem_base + ((uint32_t)(32 * quad) << 16) + (uint32_t)(cb * 32), r);
                     if (m < M) {
@@ -387,13 +414,16 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return BSP_ERR_INVALID_ARG;
-    static bool attr_done[64] = {};
     if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
-    if (!attr_done[p.device]) {
-        if (cudaFuncSetAttribute(spmm_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
-            cudaSuccess)
-            return BSP_ERR_CUDA;
-        attr_done[p.device] = true;
+    // one 256-column sub-tile per CTA for N <= 256, two (512 columns) above
+    const int nsub = N > BN ? 2 : 1;
+    static bool attr_done[2][64] = {};
+    if (!attr_done[nsub - 1][p.device]) {
+        const cudaError_t e = nsub == 2
+            ? cudaFuncSetAttribute(spmm_prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<2>::SMEM)
+            : cudaFuncSetAttribute(spmm_prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<1>::SMEM);
+        if (e != cudaSuccess) return BSP_ERR_CUDA;
+        attr_done[nsub - 1][p.device] = true;
     }
     PrefillArgs a;
     a.bitmaps = p.bitmaps;
@@ -406,7 +436,11 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     a.err = p.err;
     a.spin_cap = bspx::kSpinCap;
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
-    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM));
-    spmm_prefill_kernel<<<grid, THREADS, SMEM, s>>>(map, a);
+    const int64_t bn_cta = (int64_t)BN * nsub;
+    dim3 grid((unsigned)((N + bn_cta - 1) / bn_cta), (unsigned)((p.M + BM - 1) / BM));
+    if (nsub == 2)
+        spmm_prefill_kernel<2><<<grid, THREADS, PCfg<2>::SMEM, s>>>(map, a);
+    else
+        spmm_prefill_kernel<1><<<grid, THREADS, PCfg<1>::SMEM, s>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
