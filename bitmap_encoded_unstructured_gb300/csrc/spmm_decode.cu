@@ -60,6 +60,7 @@ __device__ __forceinline__ int bt_local(int br, int bc)
 
 constexpr int kMaxRun = 31;  // GTs per team run (offsets of a run fit one warp register)
 constexpr int kTeams = 2;    // teams (runs) per CTA
+constexpr int kSelMax = 3;   // spMspV: at most this many active K-octets of 8 -> selective fetch
 
 template <int NT, bool I8>
 struct DecCfg {
@@ -444,10 +445,49 @@ spmm_decode_kernel(const Args a)
         for (int n = 0; n < (C::WIDE_X ? NT / 2 : (I8 ? NT : 2 * NT)); ++n) acc.v[h][n] = 0;
 
     bool failed = false;
-    int issued = 0;   // GTs whose metadata copies were issued (producer warp)
-    int valued = 0;   // spMspV: GTs whose value copies were issued
+    int issued = 0;          // GTs whose metadata copies were issued (producer warp)
+    uint32_t vpend = 0;      // spMspV, producer: stages with value copies in flight on full_v
+    uint32_t vpar = 0;       // spMspV: parity expected at the next wait on full_v[s], bit s
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(FULL, bspx::mbar_wait_bounded(bar, parity, a.spin_cap));
+    };
+
+    // spMspV: the producer learns every GT's active K-octets up front from x
+    // (one coalesced pass: lane i keeps the 8-bit mask of GT i).  A GT with
+    // at most kSelMax active octets of 8 is fetched selectively in two steps
+    // (metadata first, then only the active value segments); a busier GT is
+    // fetched whole in one step: skipped segments are ~128 B, close to the
+    // DRAM fetch granularity, so selecting them saves little bandwidth and
+    // costs a round trip.  Inactive octets are never decoded either way.
+    uint32_t my_act = 0xFFu;
+    if constexpr (SKIP) {
+        if (producer_warp) {
+            uint32_t xv[kMaxRun];
+#pragma unroll
+            for (int i = 0; i < kMaxRun; ++i) {
+                xv[i] = 0u;
+                if (i < cnt) {
+                    const uint8_t* xp = a.X + ((g0 + i) * 64 + 2 * lane) * C::EB;
+                    xv[i] = C::EB == 2 ? (__ldg(reinterpret_cast<const uint32_t*>(xp)) & 0x7FFF7FFFu)
+                                       : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(xp));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxRun; ++i) {
+                if (i < cnt) {
+                    const uint32_t bal = __ballot_sync(FULL, xv[i] != 0u);
+                    uint32_t act = 0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) act |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
+                    if (lane == i) my_act = act;
+                }
+            }
+        }
+    }
+    // producer warp only (all lanes): is GT i fetched selectively?
+    auto selective = [&](int i) {
+        if constexpr (!SKIP) return false;
+        return __popc(__shfl_sync(FULL, my_act, i)) <= kSelMax;
     };
 
     // prologue: fill the ring
@@ -455,13 +495,14 @@ spmm_decode_kernel(const Args a)
         for (int i = 0; i < C::S && i < cnt; ++i) {
             const uint32_t p0 = __shfl_sync(FULL, offv, i);
             const uint32_t p1 = __shfl_sync(FULL, offv, i + 1);
-            if (lane == 0 && !(a.stall_first && i == 0)) issue_meta(i, i, !SKIP, p0, p1);
+            const bool sel = selective(i);
+            if (lane == 0 && !(a.stall_first && i == 0)) issue_meta(i, i, !sel, p0, p1);
         }
         issued = cnt < C::S ? cnt : C::S;
         if constexpr (SKIP) {
-            if (cnt > 0) {
+            if (cnt > 0 && selective(0)) {
                 if (!wait(full + 0, 0)) failed = true;
-                else { issue_values_skip(0, 0); valued = 1; }
+                else { issue_values_skip(0, 0); vpend |= 1u; }
             }
         }
     }
@@ -475,17 +516,15 @@ spmm_decode_kernel(const Args a)
         const uint32_t o0 = __shfl_sync(FULL, offv, i);
 
         if constexpr (SKIP) {
-            // producer: the metadata of GT i+1 is (or will be) in; fetch its active values
-            if (producer_warp && i + 1 < cnt) {
+            // producer: once the metadata of a selective GT i+1 is in, fetch its active values
+            if (producer_warp && i + 1 < cnt && selective(i + 1)) {
                 const int s1 = (i + 1) % C::S;
                 if (!wait(full + s1, (uint32_t)(((i + 1) / C::S) & 1))) { failed = true; break; }
                 issue_values_skip(i + 1, s1);
-                valued = i + 2;
+                vpend |= 1u << s1;
             }
-            if (!wait(full + s, ph) || !wait(full_v + s, ph)) { failed = true; break; }
-        } else {
-            if (!wait(full + s, ph)) { failed = true; break; }
         }
+        if (!wait(full + s, ph)) { failed = true; break; }
 
         // BT value bases (all 64 BTs; each warp keeps its own copy)
         const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + C::ST_BM);
@@ -522,6 +561,11 @@ spmm_decode_kernel(const Args a)
             act8 = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) act8 |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
+            if (__popc(act8) <= kSelMax) {  // selective GT: its values came on full_v[s]
+                if (!wait(full_v + s, (vpar >> s) & 1u)) { failed = true; break; }
+                vpar ^= 1u << s;
+                vpend &= ~(1u << s);
+            }
         }
         __syncwarp();
 
@@ -538,7 +582,8 @@ spmm_decode_kernel(const Args a)
                 if (!wait(empty + sj, (uint32_t)((j / C::S) & 1))) { failed = true; break; }
                 const uint32_t p0 = __shfl_sync(FULL, offv, j + C::S);
                 const uint32_t p1 = __shfl_sync(FULL, offv, j + C::S + 1);
-                if (lane == 0) issue_meta(j + C::S, sj, !SKIP, p0, p1);
+                const bool sel = selective(j + C::S);
+                if (lane == 0) issue_meta(j + C::S, sj, !sel, p0, p1);
                 issued = j + C::S + 1;
             }
         }
@@ -552,8 +597,8 @@ spmm_decode_kernel(const Args a)
             for (int j = i_fail; j < issued; ++j)
                 bspx::mbar_wait_bounded(full + (j % C::S), (uint32_t)((j / C::S) & 1), a.spin_cap);
             if constexpr (SKIP)
-                for (int j = i_fail; j < valued; ++j)
-                    bspx::mbar_wait_bounded(full_v + (j % C::S), (uint32_t)((j / C::S) & 1), a.spin_cap);
+                for (int t = 0; t < C::S; ++t)
+                    if ((vpend >> t) & 1u) bspx::mbar_wait_bounded(full_v + t, (vpar >> t) & 1u, a.spin_cap);
         }
     }
 

@@ -377,3 +377,27 @@ def test_wait_that_runs_out_reports_timeout(spmspv, monkeypatch):
     Yref, S = oracle.spmm_f16(W, X)
     assert_within_bound(Y, Yref, S, "after timeout")
     A.check()
+
+
+def test_spmspv_mixed_selective_and_whole_fetch():
+    """GTs whose x is mostly zero take the selective two-step fetch, busy
+    ones the one-step fetch: alternate them along K."""
+    M, K = 256, 64 * 24
+    W = synth.weights_f16(M, K, 0.5, "uniform", 401)
+    x = synth.activations_f16(1, K, 402)[0].copy()
+    g = synth.rng(403)
+    for gj in range(K // 64):
+        seg = x[gj * 64:(gj + 1) * 64]
+        if gj % 3 == 1:      # two active octets: selective
+            keep = np.zeros(64, dtype=bool)
+            keep[8 * g.integers(0, 8)] = True
+            keep[8 * g.integers(0, 8) + 3] = True
+            seg[~keep] = 0
+        elif gj % 3 == 2:    # no active octet
+            seg[:] = 0
+    yref, s = oracle.spmspv_f16(W, x)
+    A = _encode(W)
+    for _ in range(2):
+        y = A.spmspv(to_dev_f16(x, DEV)).cpu().numpy()
+        assert_within_bound(y, yref, s, "mixed spmspv")
+    A.check()
