@@ -214,10 +214,16 @@ __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t*
     const uint32_t rsh = 8u * (uint32_t)(rr & 3);
     const bool hi = rr >= 4;
     const uint32_t lowm = (1u << rsh) - 1u;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    // spMspV: a real loop over the warp's active octets only (a warp-uniform
+    // branch, so skipped octets cost no instructions); otherwise all four,
+    // unrolled
+    uint32_t todo = SKIP ? ((act8 >> bc0) & 0xFu) : 0xFu;
+#pragma unroll(SKIP ? 1 : 4)
+    for (int it = 0; it < 4; ++it) {
+        if (SKIP && todo == 0u) break;
+        const int k = SKIP ? __ffs(todo) - 1 : it;
+        if (SKIP) todo &= todo - 1u;
         const int bc = bc0 + k;
-        if (SKIP && !((act8 >> bc) & 1u)) continue;
         uint32_t byte[2], idx[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -452,42 +458,20 @@ spmm_decode_kernel(const Args a)
         return __all_sync(FULL, bspx::mbar_wait_bounded(bar, parity, a.spin_cap));
     };
 
-    // spMspV: the producer learns every GT's active K-octets up front from x
-    // (one coalesced pass: lane i keeps the 8-bit mask of GT i).  A GT with
-    // at most kSelMax active octets of 8 is fetched selectively in two steps
-    // (metadata first, then only the active value segments); a busier GT is
-    // fetched whole in one step: skipped segments are ~128 B, close to the
-    // DRAM fetch granularity, so selecting them saves little bandwidth and
-    // costs a round trip.  Inactive octets are never decoded either way.
+    // spMspV: a GT with at most kSelMax active K-octets of 8 is fetched
+    // selectively in two steps (metadata first, then only the active value
+    // segments); a busier GT is fetched whole in one step: skipped segments
+    // are ~128 B, close to the DRAM fetch granularity, so selecting them saves
+    // little bandwidth and costs a round trip.  Inactive octets are never
+    // decoded either way.  The first S GTs of a run are always fetched whole,
+    // so the ring starts at once; meanwhile the producer reads the K-octet
+    // activity of the later GTs from x (lane i keeps the 8-bit mask of GT i).
+    // Consumers apply the same rule from the x tile in shared memory.
     uint32_t my_act = 0xFFu;
-    if constexpr (SKIP) {
-        if (producer_warp) {
-            uint32_t xv[kMaxRun];
-#pragma unroll
-            for (int i = 0; i < kMaxRun; ++i) {
-                xv[i] = 0u;
-                if (i < cnt) {
-                    const uint8_t* xp = a.X + ((g0 + i) * 64 + 2 * lane) * C::EB;
-                    xv[i] = C::EB == 2 ? (__ldg(reinterpret_cast<const uint32_t*>(xp)) & 0x7FFF7FFFu)
-                                       : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(xp));
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kMaxRun; ++i) {
-                if (i < cnt) {
-                    const uint32_t bal = __ballot_sync(FULL, xv[i] != 0u);
-                    uint32_t act = 0;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) act |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
-                    if (lane == i) my_act = act;
-                }
-            }
-        }
-    }
     // producer warp only (all lanes): is GT i fetched selectively?
     auto selective = [&](int i) {
         if constexpr (!SKIP) return false;
-        return __popc(__shfl_sync(FULL, my_act, i)) <= kSelMax;
+        return i >= C::S && __popc(__shfl_sync(FULL, my_act, i)) <= kSelMax;
     };
 
     // prologue: fill the ring
@@ -495,14 +479,28 @@ spmm_decode_kernel(const Args a)
         for (int i = 0; i < C::S && i < cnt; ++i) {
             const uint32_t p0 = __shfl_sync(FULL, offv, i);
             const uint32_t p1 = __shfl_sync(FULL, offv, i + 1);
-            const bool sel = selective(i);
-            if (lane == 0 && !(a.stall_first && i == 0)) issue_meta(i, i, !sel, p0, p1);
+            if (lane == 0 && !(a.stall_first && i == 0)) issue_meta(i, i, true, p0, p1);
         }
         issued = cnt < C::S ? cnt : C::S;
         if constexpr (SKIP) {
-            if (cnt > 0 && selective(0)) {
-                if (!wait(full + 0, 0)) failed = true;
-                else { issue_values_skip(0, 0); vpend |= 1u; }
+            // lane i reads the 64 activations of GT i (one octet per 16-B or
+            // 8-B load) and keeps their K-octet activity mask
+            if (lane >= C::S && lane < cnt) {
+                const uint8_t* xp = a.X + (g0 + lane) * 64 * C::EB;
+                uint32_t act = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    bool nz;
+                    if constexpr (C::EB == 2) {
+                        const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + j);
+                        nz = ((q.x | q.y | q.z | q.w) & 0x7FFF7FFFu) != 0u;  // +-0 count as zero
+                    } else {
+                        const uint2 q = __ldg(reinterpret_cast<const uint2*>(xp) + j);
+                        nz = (q.x | q.y) != 0u;
+                    }
+                    act |= (nz ? 1u : 0u) << j;
+                }
+                my_act = act;
             }
         }
     }
@@ -561,7 +559,7 @@ spmm_decode_kernel(const Args a)
             act8 = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) act8 |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
-            if (__popc(act8) <= kSelMax) {  // selective GT: its values came on full_v[s]
+            if (i >= C::S && __popc(act8) <= kSelMax) {  // selective GT: its values came on full_v[s]
                 if (!wait(full_v + s, (vpar >> s) & 1u)) { failed = true; break; }
                 vpar ^= 1u << s;
                 vpend &= ~(1u << s);
