@@ -12,20 +12,25 @@
 // straight into the K-major 128-byte-swizzled shared-memory layout that
 // tcgen05.mma reads: a BT row-byte is exactly one swizzle chunk.
 //
-// CTA tile: 128 rows of W (two GT row strips) x 256 columns of Y (tokens);
-// one GT column (K = 64) per pipeline step, 3 stages:
-//   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB)
-//   B  X tile           256 x 64 fp16, K-major, SWIZZLE_128B (32 KB, TMA)
-//   C  compressed data  bitmaps + value spans of the two GTs (bulk copies)
+// CTA tile: 128 rows of W (two GT row strips) x 256 * NSUB columns of Y
+// (tokens); one GT column (K = 64) per pipeline step, three rings:
+//   C  compressed data  bitmaps + value spans of the two GTs (bulk copies),
+//                       3 stages, producer -> decoders
+//   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB),
+//                       2 stages, decoders -> MMA
+//   B  X tile(s)        NSUB x 256 x 64 fp16, K-major, SWIZZLE_128B (TMA),
+//                       2-3 stages, producer -> MMA
+// each with a "full" and an "empty" mbarrier per stage, so decoding step
+// k+1 overlaps the MMAs of step k and the compressed data runs ahead.
 // Warp roles (10 warps):
-//   warp 0     producer: TMA tensor load of B, bulk copies of C, per stage
-//              on a "full" mbarrier; waits the stage's "empty" barrier.
-//   warp 1     allocates 256 TMEM columns; lane 0 issues 4 x
+//   warp 0     producer: bulk copies of C (up to 3 steps ahead) and TMA
+//              tensor loads of B.
+//   warp 1     allocates 256 * NSUB TMEM columns; lane 0 issues NSUB x 4
 //              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) per
-//              step and commits them to the stage's "empty" barrier.
+//              step and commits them to the A and B "empty" barriers.
 //   warps 2-9  decoders: each takes one GT and a quarter of its rows, scans
 //              the BT popcounts (shfl) for the value bases and writes the
-//              dense row-bytes into A; then arrive on "a_full".
+//              dense row-bytes into A; then arrive on "a_full" / "c_empty".
 //   warps 4-7  after the K loop: epilogue, tcgen05.ld of their TMEM lane
 //              quadrant, fp32 -> fp16, stores to Y[n][m].
 // Every wait is bounded; a wait that gives up stores BSP_ERR_TIMEOUT in the
@@ -55,19 +60,26 @@ constexpr int THREADS = WARPS * 32;
 // accumulator: every decoded A tile feeds NSUB x 4 MMAs.
 template <int NSUB>
 struct PCfg {
-    static constexpr int S = NSUB == 1 ? 3 : 2;  // pipeline stages
     static constexpr int BN_CTA = BN * NSUB;
-    static constexpr int OFF_A = 0, OFF_B = A_BYTES, OFF_C = A_BYTES + NSUB * B_BYTES;
-    static constexpr int OFF_H = OFF_C + 2 * SLOT;  // stage header: the two span shifts
-    static constexpr int STAGE = ((OFF_H + 16) + 1023) & ~1023;
-    static constexpr int OFF_BASE = S * STAGE;      // decoder warps' BT bases, 64 u32 each
+    // three rings with their own depths
+    static constexpr int SB = NSUB == 1 ? 3 : 2;     // X tiles (TMA)          -> MMA
+    static constexpr int SA = 2;                      // decoded A tiles        -> MMA
+    static constexpr int SC = 3;                      // compressed GroupTiles  -> decoders
+    static constexpr int B_STAGE = NSUB * B_BYTES;
+    static constexpr int C_STAGE = ((2 * SLOT + 16) + 127) & ~127;  // two GTs + header (shifts)
+    static constexpr int OFF_B = 0;                   // 1024-B aligned regions first
+    static constexpr int OFF_A = OFF_B + SB * B_STAGE;
+    static constexpr int OFF_C = OFF_A + SA * A_BYTES;
+    static constexpr int OFF_BASE = OFF_C + SC * C_STAGE;  // decoder warps' BT bases, 64 u32 each
     static constexpr int OFF_BAR = OFF_BASE + DEC_WARPS * 256;
-    static constexpr int NBAR = 3 * S + 1;          // full[S], a_full[S], empty[S], acc
+    // barriers: c_full[SC] c_empty[SC] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc
+    static constexpr int NBAR = 2 * SC + 2 * SB + 2 * SA + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_TMEM + 16;
-    static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the base to 1024 B
+    static constexpr int SMEM = SMEM_USED + 1024;    // slack to align the base to 1024 B
     static constexpr uint32_t TMEM_COLS = 256 * NSUB;
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert((B_STAGE % 1024) == 0 && (A_BYTES % 1024) == 0, "swizzle atoms need 1024-B alignment");
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
@@ -153,8 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a)
 {
     using P = PCfg<NSUB>;
-    constexpr int S = P::S, STAGE = P::STAGE, OFF_A = P::OFF_A, OFF_B = P::OFF_B, OFF_C = P::OFF_C;
-    constexpr int OFF_H = P::OFF_H, OFF_BASE = P::OFF_BASE, OFF_BAR = P::OFF_BAR, OFF_TMEM = P::OFF_TMEM;
+    constexpr int SA = P::SA, SB = P::SB, SC = P::SC;
     constexpr uint32_t TMEM_COLS = P::TMEM_COLS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-B alignment of the shared-window offset (the 128-B swizzle atoms)
@@ -163,11 +174,17 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* a_full = full + S;
-    uint64_t* empty = full + 2 * S;
-    uint64_t* acc_bar = full + 3 * S;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    uint64_t* c_full = reinterpret_cast<uint64_t*>(smem + P::OFF_BAR);
+    uint64_t* c_empty = c_full + SC;
+    uint64_t* b_full = c_empty + SC;
+    uint64_t* b_empty = b_full + SB;
+    uint64_t* a_full = b_empty + SB;
+    uint64_t* a_empty = a_full + SA;
+    uint64_t* acc_bar = a_empty + SA;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::OFF_TMEM);
+    auto b_stage = [&](int s) { return smem + P::OFF_B + s * P::B_STAGE; };
+    auto a_stage = [&](int s) { return smem + P::OFF_A + s * A_BYTES; };
+    auto c_stage = [&](int s) { return smem + P::OFF_C + s * P::C_STAGE; };
 
     const int64_t M = a.M, N = a.N, K = a.K;
     const int64_t KT = K >> 6;
@@ -178,7 +195,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     const uint32_t cap = a.spin_cap;
 
     if (warp == 1) {
-        // allocate the accumulator: 128 lanes x 256 fp32 columns
+        // allocate the accumulators: 128 lanes x 256*NSUB fp32 columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          bspx::smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
@@ -186,10 +203,17 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            bspx::mbar_init(full + s, 1);
+        for (int s = 0; s < SC; ++s) {
+            bspx::mbar_init(c_full + s, 1);
+            bspx::mbar_init(c_empty + s, DEC_WARPS);
+        }
+        for (int s = 0; s < SB; ++s) {
+            bspx::mbar_init(b_full + s, 1);
+            bspx::mbar_init(b_empty + s, 1);
+        }
+        for (int s = 0; s < SA; ++s) {
             bspx::mbar_init(a_full + s, DEC_WARPS);
-            bspx::mbar_init(empty + s, 1);
+            bspx::mbar_init(a_empty + s, 1);
         }
         bspx::mbar_init(acc_bar, 1);
         bspx::fence_mbar_init();
@@ -201,70 +225,85 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     bool failed = false;
 
     if (warp == 0) {
-        // ---------------- producer
+        // ---------------- producer: compressed GTs up to SC steps ahead, X tiles up to SB
         const int64_t ta = strip0 * KT, tb = strip1 * KT;
         uint32_t offa = 0, offb = 0;
         int64_t wbase = -64;
-        int64_t issued = 0;
-        for (int64_t kb = 0; kb < KT; ++kb) {
-            const int s = (int)(kb % S);
-            if (kb >= S) {
-                const uint32_t ph = (uint32_t)(((kb / S) - 1) & 1);
-                if (!__all_sync(FULL, bspx::mbar_wait_bounded(empty + s, ph, cap))) { failed = true; break; }
-            }
-            if (kb - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
-                wbase = kb;
-                const int64_t i = wbase + lane;
-                offa = (i <= KT) ? __ldg(a.offsets + ta + i) : 0u;
-                offb = (has_b && i <= KT) ? __ldg(a.offsets + tb + i) : 0u;
-            }
-            const int w = (int)(kb - wbase);
-            const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
-            const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
-            if (lane == 0) {
-                uint8_t* st = smem + s * STAGE;
-                uint32_t* hdr = reinterpret_cast<uint32_t*>(st + OFF_H);
-                const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
-                const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
-                hdr[0] = oa0 - cha * 8;
-                hdr[1] = ob0 - chb * 8;
-                uint32_t bytes = NSUB * B_BYTES + 512 + nca * 16;
-                if (has_b) bytes += 512 + ncb * 16;
-                bspx::mbar_arrive_expect_tx(full + s, bytes);
-                for (int u = 0; u < NSUB; ++u)
-                    tma_load_2d(st + OFF_B + u * B_BYTES, &tmX, (int)(kb * BK), (int)(n0 + u * BN), full + s);
-                bspx::bulk_g2s(st + OFF_C, a.bitmaps + (ta + kb) * 64, 512, full + s);
-                if (nca) bspx::bulk_g2s(st + OFF_C + 512, a.values + (int64_t)cha * 16, nca * 16, full + s);
-                if (has_b) {
-                    bspx::bulk_g2s(st + OFF_C + SLOT, a.bitmaps + (tb + kb) * 64, 512, full + s);
-                    if (ncb)
-                        bspx::bulk_g2s(st + OFF_C + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, full + s);
+        int64_t kc = 0, kx = 0;  // next compressed step / next X step to issue
+        while ((kc < KT || kx < KT) && !failed) {
+            if (kc < KT && kc < kx + SC) {
+                const int s = (int)(kc % SC);
+                if (kc >= SC) {
+                    const uint32_t ph = (uint32_t)(((kc / SC) - 1) & 1);
+                    if (!__all_sync(FULL, bspx::mbar_wait_bounded(c_empty + s, ph, cap))) { failed = true; break; }
                 }
+                if (kc - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
+                    wbase = kc;
+                    const int64_t i = wbase + lane;
+                    offa = (i <= KT) ? __ldg(a.offsets + ta + i) : 0u;
+                    offb = (has_b && i <= KT) ? __ldg(a.offsets + tb + i) : 0u;
+                }
+                const int w = (int)(kc - wbase);
+                const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
+                const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
+                if (lane == 0) {
+                    uint8_t* st = c_stage(s);
+                    uint32_t* hdr = reinterpret_cast<uint32_t*>(st + 2 * SLOT);
+                    const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
+                    const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                    hdr[0] = oa0 - cha * 8;
+                    hdr[1] = ob0 - chb * 8;
+                    uint32_t bytes = 512 + nca * 16;
+                    if (has_b) bytes += 512 + ncb * 16;
+                    bspx::mbar_arrive_expect_tx(c_full + s, bytes);
+                    bspx::bulk_g2s(st, a.bitmaps + (ta + kc) * 64, 512, c_full + s);
+                    if (nca) bspx::bulk_g2s(st + 512, a.values + (int64_t)cha * 16, nca * 16, c_full + s);
+                    if (has_b) {
+                        bspx::bulk_g2s(st + SLOT, a.bitmaps + (tb + kc) * 64, 512, c_full + s);
+                        if (ncb)
+                            bspx::bulk_g2s(st + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, c_full + s);
+                    }
+                }
+                ++kc;
+            } else {
+                const int s = (int)(kx % SB);
+                if (kx >= SB) {
+                    const uint32_t ph = (uint32_t)(((kx / SB) - 1) & 1);
+                    if (!__all_sync(FULL, bspx::mbar_wait_bounded(b_empty + s, ph, cap))) { failed = true; break; }
+                }
+                if (lane == 0) {
+                    bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
+                    for (int u = 0; u < NSUB; ++u)
+                        tma_load_2d(b_stage(s) + u * B_BYTES, &tmX, (int)(kx * BK), (int)(n0 + u * BN), b_full + s);
+                }
+                ++kx;
             }
-            issued = kb + 1;
         }
         // let the last copies land before the CTA can exit (bounded)
-        for (int64_t kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-            bspx::mbar_wait_bounded(full + (kb % S), (uint32_t)((kb / S) & 1), cap);
+        for (int64_t k = (kc > SC ? kc - SC : 0); k < kc; ++k)
+            bspx::mbar_wait_bounded(c_full + (k % SC), (uint32_t)((k / SC) & 1), cap);
+        for (int64_t k = (kx > SB ? kx - SB : 0); k < kx; ++k)
+            bspx::mbar_wait_bounded(b_full + (k % SB), (uint32_t)((k / SB) & 1), cap);
     } else if (warp == 1) {
         // ---------------- MMA issuer
         for (int64_t kb = 0; kb < KT; ++kb) {
-            const int s = (int)(kb % S);
-            const uint32_t ph = (uint32_t)((kb / S) & 1);
-            const bool ok = bspx::mbar_wait_bounded(a_full + s, ph, cap) && bspx::mbar_wait_bounded(full + s, ph, cap);
+            const int sa = (int)(kb % SA), sb = (int)(kb % SB);
+            const bool ok = bspx::mbar_wait_bounded(a_full + sa, (uint32_t)((kb / SA) & 1), cap) &&
+                            bspx::mbar_wait_bounded(b_full + sb, (uint32_t)((kb / SB) & 1), cap);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint64_t ad = smem_desc_sw128(bspx::smem_u32(smem + s * STAGE + OFF_A));
+                const uint64_t ad = smem_desc_sw128(bspx::smem_u32(a_stage(sa)));
 #pragma unroll
                 for (int u = 0; u < NSUB; ++u) {
-                    const uint64_t bd = smem_desc_sw128(bspx::smem_u32(smem + s * STAGE + OFF_B + u * B_BYTES));
+                    const uint64_t bd = smem_desc_sw128(bspx::smem_u32(b_stage(sb) + u * B_BYTES));
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
                         umma_f16(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
                                  (kb | j) ? 1u : 0u);
                 }
-                umma_commit(empty + s);
+                umma_commit(a_empty + sa);  // each fires once the MMAs above are done
+                umma_commit(b_empty + sb);
             }
             __syncwarp();
         }
@@ -275,7 +314,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         // ---------------- decoders
         const int dw = warp - 2;
         const int gsel = dw >> 2, q = dw & 3;
-        uint32_t* base_s = reinterpret_cast<uint32_t*>(smem + OFF_BASE + dw * 256);
+        uint32_t* base_s = reinterpret_cast<uint32_t*>(smem + P::OFF_BASE + dw * 256);
         // lane: row 16q + (lane & 15) of the GT, octets 2p + half (p = 0..3), so
         // one step of a warp reads a single TCTile (rows 16q.., octets 2p, 2p+1)
         const int row = 16 * q + (lane & 15);       // row inside the GT
@@ -292,14 +331,15 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         const uint32_t lowm = (1u << rsh) - 1u;
         const bool active = gsel == 0 || has_b;
         for (int64_t kb = 0; kb < KT; ++kb) {
-            const int s = (int)(kb % S);
-            const uint32_t ph = (uint32_t)((kb / S) & 1);
-            if (!__all_sync(FULL, bspx::mbar_wait_bounded(full + s, ph, cap))) { failed = true; break; }
-            uint8_t* st = smem + s * STAGE;
+            const int sc = (int)(kb % SC), sa = (int)(kb % SA);
+            bool ok = bspx::mbar_wait_bounded(c_full + sc, (uint32_t)((kb / SC) & 1), cap);
+            if (kb >= SA) ok = ok && bspx::mbar_wait_bounded(a_empty + sa, (uint32_t)(((kb / SA) - 1) & 1), cap);
+            if (!__all_sync(FULL, ok)) { failed = true; break; }
+            const uint8_t* st = c_stage(sc);
             if (active) {
-                const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + OFF_C + gsel * SLOT);
-                const uint16_t* vh = reinterpret_cast<const uint16_t*>(st + OFF_C + gsel * SLOT + 512);
-                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + OFF_H)[gsel];
+                const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + gsel * SLOT);
+                const uint16_t* vh = reinterpret_cast<const uint16_t*>(st + gsel * SLOT + 512);
+                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + 2 * SLOT)[gsel];
                 const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(bm_st)[lane];
                 const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
                 uint32_t incl = c0 + c1;
@@ -312,7 +352,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 base_s[2 * lane] = ex;
                 base_s[2 * lane + 1] = ex + c0;
                 __syncwarp();
-                uint8_t* arow = st + OFF_A + (trow >> 3) * 1024 + (trow & 7) * 128;
+                uint8_t* arow = a_stage(sa) + (trow >> 3) * 1024 + (trow & 7) * 128;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int bc = 2 * j + half;
@@ -344,7 +384,10 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             // make the generic-proxy writes of A visible to the tensor cores
             bspx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) bspx::mbar_arrive(a_full + s);
+            if (lane == 0) {
+                bspx::mbar_arrive(a_full + sa);
+                bspx::mbar_arrive(c_empty + sc);
+            }
         }
         // ---------------- epilogue (warps 4-7 own TMEM lane quadrants 0-3)
         if (warp >= 4 && warp < 8) {
