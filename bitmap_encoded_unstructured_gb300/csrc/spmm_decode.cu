@@ -58,6 +58,15 @@ __device__ __forceinline__ int bt_local(int br, int bc)
     return (((br >> 1) * 4 + (bc >> 1)) << 2) + (br & 1) + ((bc & 1) << 1);
 }
 
+// Tuning of the narrow configurations (fp16 N <= 2, int8): ring stages per
+// team and the CTAs per SM that the register budget targets.
+#ifndef BSP_DEC_NARROW_STAGES
+#define BSP_DEC_NARROW_STAGES 2
+#endif
+#ifndef BSP_DEC_NARROW_MINB
+#define BSP_DEC_NARROW_MINB 4
+#endif
+
 constexpr int kMaxRun = 31;  // GTs per team run (offsets of a run fit one warp register)
 constexpr int kTeams = 2;    // teams (runs) per CTA
 constexpr int kSelMax = 3;   // spMspV: at most this many active K-octets of 8 -> selective fetch
@@ -68,8 +77,8 @@ struct DecCfg {
     static constexpr int WARPS = 2 * TEAMS;            // two warps per team
     static constexpr int THREADS = WARPS * 32;
     static constexpr bool WIDE_X = !I8 && NT >= 4;     // fp32 X tile + packed fp32x2 FMA
-    static constexpr int MINB = (NT >= 8) ? 2 : 4;     // CTAs per SM the register budget targets
-    static constexpr int S = WIDE_X ? 2 : 3;           // pipeline stages per team
+    static constexpr int MINB = (NT >= 8) ? 2 : (WIDE_X ? 4 : BSP_DEC_NARROW_MINB);  // CTAs per SM for the register budget
+    static constexpr int S = WIDE_X ? 2 : BSP_DEC_NARROW_STAGES;  // pipeline stages per team
     static constexpr int LAG = S >= 3 ? 1 : 0;         // refill the stage of GT i-LAG
     static constexpr int EB = I8 ? 1 : 2;
     static constexpr int E16 = 16 / EB;                // elements per 16-B chunk
