@@ -162,11 +162,13 @@ def _dist():
 
 
 def _max_over_ranks(v: float, ws: int) -> float:
+    """Max of a per-rank value over all ranks (the whole-job time)."""
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "bsp_decode": (C.c_int, [_P, _P, _P]),
     "bsp_export": (C.c_int, [_P, _P, _P, _P, _P]),
     "bsp_check": (C.c_int, [_P, _P]),
+    "bsp_import": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, C.c_uint64, _P, C.POINTER(_P)]),
     "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
 }
 
@@ -149,6 +150,14 @@ def bsp_export(h: int, bitmaps_ptr, offsets_ptr, values_ptr, stream: int = 0) ->
     _check("bsp_export", lib().bsp_export(h, bitmaps_ptr, offsets_ptr, values_ptr, stream))
 
 
+def bsp_import(bitmaps_ptr: int, offsets_ptr: int, values_ptr, dtype: int, M: int, K: int, nnz: int,
+               stream: int = 0) -> int:
+    h = C.c_void_p()
+    _check("bsp_import", lib().bsp_import(bitmaps_ptr, offsets_ptr, values_ptr, dtype, M, K, nnz, stream,
+                                          C.byref(h)))
+    return h.value
+
+
 def bsp_check(h: int, stream: int = 0) -> None:
     _check("bsp_check", lib().bsp_check(h, stream))
 
@@ -196,6 +205,33 @@ class BitmapMatrix:
         self.device = W.device
         self.torch_dtype = W.dtype
         self.h = bsp_encode(W.data_ptr(), self.dtype, self.M, self.K, _stream(stream))
+
+    @classmethod
+    def from_arrays(cls, bitmaps, offsets, values, M: int, K: int, device=None, stream=None):
+        """A handle from encoded arrays (tensors on the GPU or the CPU, or numpy
+        arrays): bitmaps int64/uint64 [M*K/64], offsets int32/uint32 [NGT+1],
+        values fp16 (or uint16 bits) / int8 [NNZ].  Validated on the device."""
+        import numpy as np
+        import torch
+
+        def ptr(a):
+            if isinstance(a, np.ndarray):
+                return np.ascontiguousarray(a).ctypes.data, a
+            a = a.contiguous()
+            return a.data_ptr(), a
+
+        vals = values
+        is_i8 = (vals.dtype == np.int8) if isinstance(vals, np.ndarray) else (vals.dtype == torch.int8)
+        obj = cls.__new__(cls)
+        obj.dtype = BSP_INT8 if is_i8 else BSP_FP16
+        obj.M, obj.K = M, K
+        obj.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        obj.torch_dtype = torch.int8 if is_i8 else torch.float16
+        (pb, kb), (po, ko), (pv, kv) = ptr(bitmaps), ptr(offsets), ptr(vals)
+        nnz = int(vals.shape[0])
+        obj.h = bsp_import(pb, po, pv if nnz else None, obj.dtype, M, K, nnz, _stream(stream))
+        del kb, ko, kv
+        return obj
 
     def close(self):
         if getattr(self, "h", None):

@@ -54,6 +54,34 @@ bsp_status_t grow(void** p, size_t* have, size_t need)
     return BSP_OK;
 }
 
+// Split-K workspace (zeroed), strip counters (zeroed) and error word.
+bsp_status_t alloc_scratch(bsp_handle* h, cudaStream_t s)
+{
+    const size_t ws_bytes = (size_t)BSP_DECODE_MAX_N * (size_t)h->M * 4;
+    const size_t cnt_bytes = (size_t)(h->M / 64) * 4;
+    if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess || cudaMalloc(&h->counters, cnt_bytes) != cudaSuccess ||
+        cudaMalloc(&h->err, sizeof(int)) != cudaSuccess)
+        return BSP_ERR_OOM;
+    if (cudaMemsetAsync(h->ws, 0, ws_bytes, s) != cudaSuccess ||
+        cudaMemsetAsync(h->counters, 0, cnt_bytes, s) != cudaSuccess ||
+        cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+
+bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
+{
+    bsp_handle* h = new (std::nothrow) bsp_handle{};
+    if (!h) return nullptr;
+    h->magic = BSP_MAGIC;
+    h->dtype = dtype;
+    h->M = M;
+    h->K = K;
+    h->NGT = (M / 64) * (K / 64);
+    h->NBT = M * K / 64;
+    return h;
+}
+
 }  // namespace
 
 extern "C" {
@@ -83,14 +111,8 @@ bsp_status_t bsp_encode(const void* W, bsp_dtype_t dtype, int64_t M, int64_t K,
     if (dtype != BSP_FP16 && dtype != BSP_INT8) return BSP_ERR_DTYPE;
     if (M <= 0 || K <= 0 || (M % 64) || (K % 64)) return BSP_ERR_SHAPE;
     if (!aligned16(W)) return BSP_ERR_ALIGN;
-    bsp_handle* h = new (std::nothrow) bsp_handle{};
+    bsp_handle* h = new_handle(dtype, M, K);
     if (!h) return BSP_ERR_OOM;
-    h->magic = BSP_MAGIC;
-    h->dtype = dtype;
-    h->M = M;
-    h->K = K;
-    h->NGT = (M / 64) * (K / 64);
-    h->NBT = M * K / 64;
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
         free_handle(h);
@@ -98,21 +120,8 @@ bsp_status_t bsp_encode(const void* W, bsp_dtype_t dtype, int64_t M, int64_t K,
     }
     cudaStream_t s = (cudaStream_t)stream;
     bsp_status_t st = bsp_run_encode(h, W, s);
+    if (st == BSP_OK) st = alloc_scratch(h, s);
     if (st != BSP_OK) { free_handle(h); return st; }
-    const size_t ws_bytes = (size_t)BSP_DECODE_MAX_N * (size_t)M * 4;
-    if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess ||
-        cudaMalloc(&h->counters, (size_t)(M / 64) * 4) != cudaSuccess ||
-        cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) {
-        free_handle(h);
-        return BSP_ERR_OOM;
-    }
-    if (cudaMemsetAsync(h->ws, 0, ws_bytes, s) != cudaSuccess ||
-        cudaMemsetAsync(h->counters, 0, (size_t)(M / 64) * 4, s) != cudaSuccess ||
-        cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
-        free_handle(h);
-        return BSP_ERR_CUDA;
-    }
     *out = h;
     return BSP_OK;
 }
@@ -246,6 +255,46 @@ bsp_status_t bsp_export(bsp_handle_t h, uint64_t* bitmaps, uint32_t* offsets, vo
     if (values && h->NNZ &&
         cudaMemcpyAsync(values, h->values, (size_t)h->NNZ * bsp_elem_bytes(h->dtype), cudaMemcpyDefault, s) != cudaSuccess)
         return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_import(const uint64_t* bitmaps, const uint32_t* offsets, const void* values, bsp_dtype_t dtype,
+                        int64_t M, int64_t K, uint64_t nnz, bsp_stream_t stream, bsp_handle_t* out)
+{
+    if (!out) return BSP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!bitmaps || !offsets || (nnz && !values)) return BSP_ERR_INVALID_ARG;
+    if (dtype != BSP_FP16 && dtype != BSP_INT8) return BSP_ERR_DTYPE;
+    if (M <= 0 || K <= 0 || (M % 64) || (K % 64) || nnz > 0xFFFFFFFFull || nnz > (uint64_t)M * (uint64_t)K)
+        return BSP_ERR_SHAPE;
+    bsp_handle* h = new_handle(dtype, M, K);
+    if (!h) return BSP_ERR_OOM;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        free_handle(h);
+        return BSP_ERR_CUDA;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const int eb = bsp_elem_bytes(dtype);
+    h->NNZ = nnz;
+    h->values_alloc = ((size_t)nnz * eb + 16 + 15) & ~(size_t)15;
+    if (cudaMalloc(&h->bitmaps, (size_t)h->NBT * 8) != cudaSuccess ||
+        cudaMalloc(&h->offsets, (size_t)(h->NGT + 1) * 4) != cudaSuccess ||
+        cudaMalloc(&h->values, h->values_alloc) != cudaSuccess) {
+        free_handle(h);
+        return BSP_ERR_OOM;
+    }
+    if (cudaMemcpyAsync(h->bitmaps, bitmaps, (size_t)h->NBT * 8, cudaMemcpyDefault, s) != cudaSuccess ||
+        cudaMemcpyAsync(h->offsets, offsets, (size_t)(h->NGT + 1) * 4, cudaMemcpyDefault, s) != cudaSuccess ||
+        cudaMemsetAsync(h->values, 0, h->values_alloc, s) != cudaSuccess ||
+        (nnz && cudaMemcpyAsync(h->values, values, (size_t)nnz * eb, cudaMemcpyDefault, s) != cudaSuccess)) {
+        free_handle(h);
+        return BSP_ERR_CUDA;
+    }
+    bsp_status_t st = bsp_run_validate(h, s);
+    if (st == BSP_OK) st = alloc_scratch(h, s);
+    if (st != BSP_OK) { free_handle(h); return st; }
+    *out = h;
     return BSP_OK;
 }
 

@@ -45,6 +45,8 @@ enum bsp_out_mode { BSP_OUT_F16 = 0, BSP_OUT_I32 = 1, BSP_OUT_F32_SCALED = 2 };
 // ---- encoder / decoder (encode.cu) ----
 bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s);
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s);
+// Check that offsets and bitmaps agree (imported arrays); synchronises s.
+bsp_status_t bsp_run_validate(const bsp_handle* h, cudaStream_t s);
 
 // ---- CUDA-core decode-path product (spmm_decode.cu) ----
 // Everything the decode kernel reads and writes besides X and Y: the

@@ -251,6 +251,27 @@ __global__ void dec_kernel(const uint64_t* __restrict__ bitmaps,
 
 inline unsigned grid_for(int64_t n, int block) { return (unsigned)((n + block - 1) / block); }
 
+// Validation of imported arrays: offsets[0] == 0 and, for every GT,
+// offsets[t+1] - offsets[t] == sum of the popcounts of its 64 bitmaps.
+// One warp per GT; any violation sets *bad.
+__global__ void validate_kernel(const uint64_t* __restrict__ bitmaps, const uint32_t* __restrict__ offsets,
+                                int64_t NGT, int* bad)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= NGT) return;
+    const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2*>(bitmaps + t * 64) + lane);
+    uint32_t c = __popcll(b.x) + __popcll(b.y);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
+    if (lane == 0) {
+        const uint32_t o0 = __ldg(offsets + t), o1 = __ldg(offsets + t + 1);
+        if (o1 < o0 || o1 - o0 != c || (t == 0 && o0 != 0)) atomicExch(bad, 1);
+    }
+}
+
+
+
 }  // namespace
 
 bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s)
@@ -320,4 +341,26 @@ bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s)
         dec_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(h->bitmaps, h->offsets, (const uint8_t*)h->values,
                                                                 n_rowbytes, h->K, W_out);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+bsp_status_t bsp_run_validate(const bsp_handle* h, cudaStream_t s)
+{
+    int* bad = nullptr;
+    int hbad = 0;
+    uint32_t last = 0;
+    bsp_status_t st = BSP_OK;
+    if (cudaMalloc(&bad, sizeof(int)) != cudaSuccess) return BSP_ERR_OOM;
+    if (cudaMemsetAsync(bad, 0, sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
+    validate_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->offsets, h->NGT, bad);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&last, h->offsets + h->NGT, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        st = BSP_ERR_CUDA;
+        goto done;
+    }
+    if (hbad || (uint64_t)last != h->NNZ) st = BSP_ERR_INVALID_ARG;
+done:
+    cudaFree(bad);
+    return st;
 }

@@ -186,6 +186,22 @@ bsp_status_t bsp_export(bsp_handle_t h, uint64_t *bitmaps, uint32_t *offsets,
                         void *values, bsp_stream_t stream);
 
 /*
+ * Build a handle from an existing encoding (for instance one cached on disk
+ * after bsp_export): copies bitmaps u64 [M*K/64], offsets u32
+ * [M/64 * K/64 + 1] and values [nnz] elements from device or host memory
+ * (anything cudaMemcpyAsync with cudaMemcpyDefault accepts) into arrays the
+ * new handle owns.  The copy is validated on the device (offsets[0] == 0,
+ * each GroupTile's offset step == the popcount of its bitmaps, last offset
+ * == nnz) before any kernel can read it; an inconsistent encoding returns
+ * BSP_ERR_INVALID_ARG and no handle.  Synchronises `stream`; the caller's
+ * arrays may be freed when it returns.
+ */
+bsp_status_t bsp_import(const uint64_t *bitmaps, const uint32_t *offsets,
+                        const void *values, bsp_dtype_t dtype, int64_t M,
+                        int64_t K, uint64_t nnz, bsp_stream_t stream,
+                        bsp_handle_t *out);
+
+/*
  * Synchronise `stream` and report device-side failures of earlier calls on
  * this handle: every wait inside the kernels is bounded, and a wait that
  * gives up makes its kernel store BSP_ERR_TIMEOUT in the handle's error

@@ -401,3 +401,52 @@ def test_spmspv_mixed_selective_and_whole_fetch():
         y = A.spmspv(to_dev_f16(x, DEV)).cpu().numpy()
         assert_within_bound(y, yref, s, "mixed spmspv")
     A.check()
+
+
+# ------------------------------------------------------------------ import of a cached encoding
+
+def test_import_roundtrip_device_arrays():
+    W = synth.weights_f16(256, 512, 0.5, "uniform", 501)
+    X = synth.activations_f16(8, 512, 502)
+    A = _encode(W)
+    bm, off, vals = A.arrays()
+    B = bsp.BitmapMatrix.from_arrays(bm, off, vals, 256, 512)
+    Xd = to_dev_f16(X, DEV)
+    Yref, S = oracle.spmm_f16(W, X)
+    assert_within_bound(B.spmm(Xd).cpu().numpy(), Yref, S, "imported")
+    got = B.decode().cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, W)
+    assert B.storage_bytes() == A.storage_bytes()
+
+
+@pytest.mark.parametrize("dt", ["f16", "i8"])
+def test_import_oracle_encoding_from_host(dt):
+    """The CPU oracle's own encoding, imported from host memory, runs on the GPU."""
+    if dt == "f16":
+        W = synth.weights_f16(192, 320, 0.6, "uniform", 511)
+        X = synth.activations_f16(5, 320, 512)
+    else:
+        W = synth.weights_i8(192, 320, 0.6, 513)
+        X = synth.activations_i8(5, 320, 514)
+    enc = oracle.encode(W)
+    B = bsp.BitmapMatrix.from_arrays(enc["bitmaps"], enc["offsets"], enc["values"], 192, 320)
+    if dt == "f16":
+        Yref, S = oracle.spmm_f16(W, X)
+        assert_within_bound(B.spmm(to_dev_f16(X, DEV)).cpu().numpy(), Yref, S, "oracle encoding")
+    else:
+        Y = B.spmm(to_dev(X, DEV)).cpu().numpy()
+        np.testing.assert_array_equal(Y.astype(np.int64), oracle.spmm_i8(W, X))
+
+
+def test_import_rejects_inconsistent_offsets():
+    W = synth.weights_f16(128, 256, 0.5, "uniform", 521)
+    enc = oracle.encode(W)
+    off = enc["offsets"].copy()
+    off[3] += 1  # no longer the prefix sum of the bitmaps
+    with pytest.raises(bsp.BspError) as e:
+        bsp.BitmapMatrix.from_arrays(enc["bitmaps"], off, enc["values"], 128, 256)
+    assert e.value.status == 1
+    bm = enc["bitmaps"].copy()
+    bm[5] ^= np.uint64(1)  # one more or one fewer nonzero than the offsets say
+    with pytest.raises(bsp.BspError):
+        bsp.BitmapMatrix.from_arrays(bm, enc["offsets"], enc["values"], 128, 256)
