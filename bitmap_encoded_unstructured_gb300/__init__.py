@@ -42,6 +42,7 @@ SIGNATURES = {
     "bsp_spmm": (C.c_int, [_P, _P, _I64, _P, _P]),
     "bsp_spmm_scaled": (C.c_int, [_P, _P, _I64, _P, _P, _P]),
     "bsp_spmspv": (C.c_int, [_P, _P, _P, _P]),
+    "bsp_spmspv_threshold": (C.c_int, [_P, _P, C.c_float, _P, _P]),
     "bsp_spmm_host": (C.c_int, [_P, _P, _I64, _P, _P]),
     "bsp_storage_bytes": (C.c_int, [_P, C.POINTER(C.c_uint64)]),
     "bsp_cr": (C.c_int, [_P, C.POINTER(C.c_double)]),
@@ -118,6 +119,10 @@ def bsp_spmm_scaled(h: int, X_ptr: int, N: int, scale_ptr: int, Y_ptr: int, stre
 
 def bsp_spmspv(h: int, x_ptr: int, y_ptr: int, stream: int = 0) -> None:
     _check("bsp_spmspv", lib().bsp_spmspv(h, x_ptr, y_ptr, stream))
+
+
+def bsp_spmspv_threshold(h: int, x_ptr: int, threshold: float, y_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmspv_threshold", lib().bsp_spmspv_threshold(h, x_ptr, threshold, y_ptr, stream))
 
 
 def bsp_spmm_host(h: int, X_host_ptr: int, N: int, Y_host_ptr: int, stream: int = 0) -> None:
@@ -303,6 +308,13 @@ class BitmapMatrix:
         ydt = torch.float16 if self.dtype == BSP_FP16 else torch.int32
         y = out if out is not None else torch.empty(self.M, dtype=ydt, device=self.device)
         bsp_spmspv(self.h, x.data_ptr(), y.data_ptr(), _stream(stream))
+        return y
+
+    def spmspv_threshold(self, x, threshold, out=None, stream=None):
+        import torch
+        ydt = torch.float16 if self.dtype == BSP_FP16 else torch.int32
+        y = out if out is not None else torch.empty(self.M, dtype=ydt, device=self.device)
+        bsp_spmspv_threshold(self.h, x.data_ptr(), float(threshold), y.data_ptr(), _stream(stream))
         return y
 
     def spmm_host(self, X_host, Y_host, stream=None):

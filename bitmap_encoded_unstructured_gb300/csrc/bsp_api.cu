@@ -182,6 +182,16 @@ bsp_status_t bsp_spmspv(bsp_handle_t h, const void* x, void* y, bsp_stream_t str
     return bsp_run_spmm_decode(bsp_problem_of(h), x, 1, y, mode, nullptr, true, (cudaStream_t)stream);
 }
 
+bsp_status_t bsp_spmspv_threshold(bsp_handle_t h, const void* x, float threshold, void* y, bsp_stream_t stream)
+{
+    if (!valid(h) || !x || !y || !(threshold >= 0.f)) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return BSP_ERR_ALIGN;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
+    return bsp_run_spmm_decode(bsp_problem_of(h), x, 1, y, mode, nullptr, true, (cudaStream_t)stream, threshold);
+}
+
 bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,
                            bsp_stream_t stream)
 {

@@ -69,11 +69,12 @@ bsp_decode_problem bsp_problem_of(const bsp_handle* h);
 
 // X: [N][K] (fp16 or int8), N in 1..BSP_DECODE_MAX_N.  Output by mode:
 // F16 -> Y half [N][M]; I32 -> Y int32 [N][M]; F32_SCALED -> Y float [N][M]
-// with row_scale[M].  skip_zero_octets: spMspV mode (N must be 1).
+// with row_scale[M].  skip_zero_octets: spMspV mode (N must be 1), where
+// activations with |x| <= tau are pruned (tau = 0: exact zeros).
 bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int N,
                                  void* Y, bsp_out_mode mode,
                                  const float* row_scale, bool skip_zero_octets,
-                                 cudaStream_t s);
+                                 cudaStream_t s, float tau = 0.0f);
 
 // Split-K factor chosen for a problem (exposed for tests and tuning).
 int bsp_decode_splits(const bsp_decode_problem& p, int N);

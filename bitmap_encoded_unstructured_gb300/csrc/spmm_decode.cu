@@ -119,6 +119,11 @@ __device__ __forceinline__ void x_pair(const uint8_t* xraw, int idx, int& a, int
     b = (int)(int8_t)(v >> 8);
 }
 
+// spMspV activity: an activation is pruned iff |x| <= tau (tau = 0: exact
+// zeros, +-0 included; NaN is never pruned)
+__device__ __forceinline__ bool active(float v, float tau) { return !(fabsf(v) <= tau); }
+__device__ __forceinline__ bool active(int v, float tau) { return !(fabsf((float)v) <= tau); }
+
 __device__ __forceinline__ void write_out(void* Y, int, int64_t idx, float v, float)
 {
     reinterpret_cast<__half*>(Y)[idx] = __float2half_rn(v);
@@ -343,6 +348,7 @@ struct Args {
     const float* row_scale;
     uint32_t spin_cap;  // polls before a wait gives up
     int stall_first;    // test only: skip the copies of each team's first GT
+    float tau;          // spMspV pruning threshold: |x| <= tau counts as zero
 };
 
 template <int NT, bool I8, bool SKIP>
@@ -436,7 +442,7 @@ spmm_decode_kernel(const Args a)
         for (int c = 0; c < 8; c += 2) {
             Acc v0, v1;
             x_pair(xr, (lane & 7) * 8 + c, v0, v1);
-            act |= (v0 != Acc(0)) || (v1 != Acc(0));
+            act |= active(v0, a.tau) || active(v1, a.tau);
         }
         uint32_t q0 = 0, q1 = 0;
         if (act && seg) {
@@ -499,13 +505,20 @@ spmm_decode_kernel(const Args a)
                 uint32_t act = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    bool nz;
+                    bool nz = false;
                     if constexpr (C::EB == 2) {
                         const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + j);
-                        nz = ((q.x | q.y | q.z | q.w) & 0x7FFF7FFFu) != 0u;  // +-0 count as zero
+                        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
+                            nz |= active(__low2float(h2), a.tau) || active(__high2float(h2), a.tau);
+                        }
                     } else {
                         const uint2 q = __ldg(reinterpret_cast<const uint2*>(xp) + j);
-                        nz = (q.x | q.y) != 0u;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            nz |= active((int)(int8_t)(((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xFFu), a.tau);
                     }
                     act |= (nz ? 1u : 0u) << j;
                 }
@@ -561,10 +574,10 @@ spmm_decode_kernel(const Args a)
         }
         uint32_t act8 = 0xFFu;
         if constexpr (SKIP) {
-            // K-octet j is active iff one of x[8j .. 8j+7] is nonzero
+            // K-octet j is active iff one of x[8j .. 8j+7] is not pruned
             Acc va, vb;
             x_pair(xraw, 2 * lane, va, vb);
-            const uint32_t bal = __ballot_sync(FULL, (va != Acc(0)) || (vb != Acc(0)));
+            const uint32_t bal = __ballot_sync(FULL, active(va, a.tau) || active(vb, a.tau));
             act8 = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) act8 |= (((bal >> (4 * j)) & 0xFu) ? 1u : 0u) << j;
@@ -572,6 +585,19 @@ spmm_decode_kernel(const Args a)
                 if (!wait(full_v + s, (vpar >> s) & 1u)) { failed = true; break; }
                 vpar ^= 1u << s;
                 vpend &= ~(1u << s);
+            }
+            if (a.tau > 0.f) {
+                // prune: this warp's 32 columns of the x tile, |x| <= tau -> 0
+                // (the other warp may read them meanwhile for its activity
+                // mask, which is the same either way)
+                const int col = 32 * wt + lane;
+                if constexpr (I8) {
+                    int8_t* xc = reinterpret_cast<int8_t*>(st + C::ST_X) + col;
+                    if (!active((int)*xc, a.tau)) *xc = 0;
+                } else {
+                    __half* xc = reinterpret_cast<__half*>(st + C::ST_X) + col;
+                    if (!active(__half2float(*xc), a.tau)) *xc = __ushort_as_half(0);
+                }
             }
         }
         __syncwarp();
@@ -668,7 +694,7 @@ spmm_decode_kernel(const Args a)
 
 template <int NT, bool I8, bool SKIP>
 bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, int mode,
-                    const float* row_scale, cudaStream_t s)
+                    const float* row_scale, float tau, cudaStream_t s)
 {
     using C = DecCfg<NT, I8>;
     // the opt-in shared-memory size is set once per device
@@ -703,6 +729,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
     a.spin_cap = bspx::kSpinCap;
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
     a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    a.tau = tau;
     dim3 grid((unsigned)splits, (unsigned)(p.M / 64));
     spmm_decode_kernel<NT, I8, SKIP><<<grid, C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
@@ -710,14 +737,14 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
 
 template <bool I8, bool SKIP>
 bsp_status_t dispatch_nt(const bsp_decode_problem& p, const void* X, int N, void* Y, int mode,
-                         const float* row_scale, cudaStream_t s)
+                         const float* row_scale, float tau, cudaStream_t s)
 {
-    if (N <= 1) return launch<1, I8, SKIP>(p, X, N, Y, mode, row_scale, s);
+    if (N <= 1) return launch<1, I8, SKIP>(p, X, N, Y, mode, row_scale, tau, s);
     if constexpr (!SKIP) {
-        if (N <= 2) return launch<2, I8, false>(p, X, N, Y, mode, row_scale, s);
-        if (N <= 4) return launch<4, I8, false>(p, X, N, Y, mode, row_scale, s);
-        if (N <= 8) return launch<8, I8, false>(p, X, N, Y, mode, row_scale, s);
-        return launch<16, I8, false>(p, X, N, Y, mode, row_scale, s);
+        if (N <= 2) return launch<2, I8, false>(p, X, N, Y, mode, row_scale, tau, s);
+        if (N <= 4) return launch<4, I8, false>(p, X, N, Y, mode, row_scale, tau, s);
+        if (N <= 8) return launch<8, I8, false>(p, X, N, Y, mode, row_scale, tau, s);
+        return launch<16, I8, false>(p, X, N, Y, mode, row_scale, tau, s);
     }
     return BSP_ERR_INVALID_ARG;
 }
@@ -747,16 +774,17 @@ int bsp_decode_splits(const bsp_decode_problem& p, int N)
 
 bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int N, void* Y,
                                  bsp_out_mode mode, const float* row_scale,
-                                 bool skip_zero_octets, cudaStream_t s)
+                                 bool skip_zero_octets, cudaStream_t s, float tau)
 {
     if (N < 1 || N > BSP_DECODE_MAX_N) return BSP_ERR_INVALID_ARG;
     if (skip_zero_octets && N != 1) return BSP_ERR_INVALID_ARG;
+    if (!(tau >= 0.f)) return BSP_ERR_INVALID_ARG;  // also rejects NaN
     const bool i8 = p.dtype == BSP_INT8;
     if (i8)
-        return skip_zero_octets ? dispatch_nt<true, true>(p, X, N, Y, mode, row_scale, s)
-                                : dispatch_nt<true, false>(p, X, N, Y, mode, row_scale, s);
-    return skip_zero_octets ? dispatch_nt<false, true>(p, X, N, Y, mode, row_scale, s)
-                            : dispatch_nt<false, false>(p, X, N, Y, mode, row_scale, s);
+        return skip_zero_octets ? dispatch_nt<true, true>(p, X, N, Y, mode, row_scale, tau, s)
+                                : dispatch_nt<true, false>(p, X, N, Y, mode, row_scale, tau, s);
+    return skip_zero_octets ? dispatch_nt<false, true>(p, X, N, Y, mode, row_scale, tau, s)
+                            : dispatch_nt<false, false>(p, X, N, Y, mode, row_scale, tau, s);
 }
 
 bsp_decode_problem bsp_problem_of(const bsp_handle* h)

@@ -149,6 +149,19 @@ bsp_status_t bsp_spmspv(bsp_handle_t h, const void *x, void *y,
                         bsp_stream_t stream);
 
 /*
+ * spMspV with magnitude pruning of the activations, the dynamic pruning of
+ * "Unified Static-Dynamic Pruning for Efficient LLM Inference" (section
+ * 3.2 and 4.2, a TEAL-style magnitude criterion):
+ *   y = W * x',  x'_k = 0 if |x_k| <= threshold, else x_k.
+ * K-octets whose eight activations are all pruned are skipped as in
+ * bsp_spmspv; threshold = 0 is exactly bsp_spmspv.  NaN activations are
+ * never pruned.  threshold must be >= 0 (BSP_ERR_INVALID_ARG otherwise).
+ * The comparison is |x| <= threshold with x widened exactly to fp32.
+ */
+bsp_status_t bsp_spmspv_threshold(bsp_handle_t h, const void *x, float threshold,
+                                  void *y, bsp_stream_t stream);
+
+/*
  * Same product as bsp_spmm, from and to HOST memory: copies X in, runs the
  * product and copies Y out on `stream`, then synchronises `stream`.  Uses a
  * device staging buffer owned by the handle (grown on demand, so this call

@@ -224,6 +224,31 @@ def spmspv_f16(W: np.ndarray, x: np.ndarray):
     return Y[0], S[0]
 
 
+def prune_activations_f16(x: np.ndarray, threshold: float) -> np.ndarray:
+    """Dynamic pruning by magnitude: x_k -> 0 where |x_k| <= threshold (the
+    activation-magnitude criterion of SPDP's dynamic pruning).  fp16 bits in,
+    fp16 bits out; the comparison is on the exact value (fp64); NaN is kept."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    t = np.float64(np.float32(threshold))
+    v = np.array([half_to_double(int(b)) for b in x.reshape(-1)]).reshape(x.shape)
+    out = x.copy()
+    out[np.abs(v) <= t] = 0
+    return out
+
+
+def prune_activations_i8(x: np.ndarray, threshold: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    t = np.float64(np.float32(threshold))
+    out = x.copy()
+    out[np.abs(x.astype(np.float64)) <= t] = 0
+    return out
+
+
+def spmspv_threshold_f16(W: np.ndarray, x: np.ndarray, threshold: float):
+    """y = W * x' with x' the magnitude-pruned activations."""
+    return spmspv_f16(W, prune_activations_f16(x, threshold))
+
+
 def num_threads() -> int:
     return _load().oracle_num_threads()
 

@@ -450,3 +450,39 @@ def test_import_rejects_inconsistent_offsets():
     bm[5] ^= np.uint64(1)  # one more or one fewer nonzero than the offsets say
     with pytest.raises(bsp.BspError):
         bsp.BitmapMatrix.from_arrays(bm, enc["offsets"], enc["values"], 128, 256)
+
+
+# ------------------------------------------------------------------ spMspV with a threshold
+
+@pytest.mark.parametrize("t", [0.0, 0.1, 0.5, 1.0, 2.0, 4.0])
+def test_spmspv_threshold_fp16(t):
+    """Magnitude pruning of x: from nearly all octets active (t = 0.1) to
+    mostly-idle GroupTiles on the selective fetch (t = 2, 4)."""
+    M, K = 256, 64 * 40
+    W = synth.weights_f16(M, K, 0.5, "uniform", 601)
+    x = synth.activations_f16(1, K, 602)[0]
+    yref, s = oracle.spmspv_threshold_f16(W, x, t)
+    A = _encode(W)
+    for _ in range(2):
+        y = A.spmspv_threshold(to_dev_f16(x, DEV), t).cpu().numpy()
+        assert_within_bound(y, yref, s, f"threshold {t}")
+    if t == 0.0:
+        y0 = A.spmspv(to_dev_f16(x, DEV)).cpu().numpy()
+        assert_within_bound(y0, yref, s, "spmspv")
+    A.check()
+
+
+def test_spmspv_threshold_int8_exact():
+    W = synth.weights_i8(192, 1024, 0.5, 611)
+    x = synth.activations_i8(1, 1024, 612)[0]
+    for t in (0.0, 60.0, 120.0):
+        yref = oracle.spmm_i8(W, oracle.prune_activations_i8(x, t).reshape(1, -1))[0]
+        y = _encode(W).spmspv_threshold(to_dev(x, DEV), t).cpu().numpy()
+        np.testing.assert_array_equal(y.astype(np.int64), yref)
+
+
+def test_spmspv_threshold_rejects_negative():
+    A = _encode(synth.weights_f16(64, 64, 0.5, "uniform", 621))
+    x = torch.zeros(64, dtype=torch.float16, device=DEV)
+    with pytest.raises(bsp.BspError):
+        A.spmspv_threshold(x, -1.0)

@@ -312,3 +312,34 @@ def test_synth_exact_counts():
     x = synth.activations_relu_f16(20480, seed=4)
     frac = np.count_nonzero(x == 0) / x.size
     assert 0.83 < frac < 0.87
+
+
+# ----------------------------------------------------------- dynamic pruning (threshold)
+
+def test_prune_activations_worked_values():
+    """|x| <= t is pruned: exact fp16 values around t = 0.25; NaN is kept."""
+    x = _f16([0.5, -0.25, 0.125, 0.375, -0.75, 0.0, -0.0])
+    x = np.concatenate([x, np.array([0x7E00], dtype=np.uint16)])  # NaN
+    got = oracle.prune_activations_f16(x, 0.25)
+    want = _f16([0.5, 0.0, 0.0, 0.375, -0.75, 0.0, 0.0])
+    np.testing.assert_array_equal(got[:7], want)
+    assert got[7] == 0x7E00
+    # threshold 0 keeps every nonzero value and clears only the two zeros
+    np.testing.assert_array_equal(oracle.prune_activations_f16(x, 0.0)[:5], x[:5])
+
+
+def test_spmspv_threshold_matches_library_on_masked_x():
+    W = synth.weights_f16(128, 512, 0.5, "uniform", 81)
+    x = synth.activations_f16(1, 512, 82)[0]
+    for t in (0.0, 0.3, 1.0, 1e9):
+        y, s = oracle.spmspv_threshold_f16(W, x, t)
+        xv = x.view(np.float16).astype(np.float64)
+        xm = np.where(np.abs(xv) <= np.float64(np.float32(t)), 0.0, xv)
+        np.testing.assert_allclose(y, _f64(W) @ xm, rtol=1e-12, atol=1e-15)
+    assert np.all(oracle.spmspv_threshold_f16(W, x, 1e9)[0] == 0)
+
+
+def test_prune_activations_i8():
+    x = np.array([-127, -60, -59, 0, 59, 60, 61, 127], dtype=np.int8)
+    np.testing.assert_array_equal(oracle.prune_activations_i8(x, 60),
+                                  np.array([-127, 0, 0, 0, 0, 0, 61, 127], dtype=np.int8))
