@@ -217,12 +217,18 @@ struct Accum<NT, true, false> { int v[2][NT]; };
 // value (the masked popcount gives the row-byte's first slot, then a
 // running index), a clear bit contributes nothing.  All 32 lanes run the
 // same instruction stream, and X sits in registers.
+#ifndef BSP_DEC_OCT_UNROLL
+#define BSP_DEC_OCT_UNROLL 2
+#endif
+
 template <int NT, bool I8, bool SKIP, typename A>
 __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t* base_s,
                                           const uint8_t* vals, const uint8_t* xraw, const float* x_s,
                                           int N, uint32_t act8, int lane, int bc0, A& acc)
 {
     using C = DecCfg<NT, I8>;
+    // octet loop unroll: the spMspV loop runs over active octets only
+    constexpr int OCT_UNROLL = SKIP ? 1 : (C::WIDE_X ? 4 : BSP_DEC_OCT_UNROLL);
     const int rr = lane & 7;
     const int gb0 = bt_local(lane >> 3, 0), gb1 = bt_local((lane >> 3) + 4, 0);
     const uint32_t rsh = 8u * (uint32_t)(rr & 3);
@@ -232,7 +238,7 @@ __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t*
     // branch, so skipped octets cost no instructions); otherwise all four,
     // unrolled
     uint32_t todo = SKIP ? ((act8 >> bc0) & 0xFu) : 0xFu;
-#pragma unroll(SKIP ? 1 : 4)
+#pragma unroll(OCT_UNROLL)
     for (int it = 0; it < 4; ++it) {
         if (SKIP && todo == 0u) break;
         const int k = SKIP ? __ffs(todo) - 1 : it;
