@@ -66,6 +66,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// One poll that may suspend the thread for up to `hint_ns` nanoseconds; the
+// thread resumes as soon as the phase completes, so a waiting warp takes
+// no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_bounded with suspending polls: at most `cap` polls of at most
+// `hint_ns` each.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t cap,
+                                                uint32_t hint_ns = 1000)
+{
+    for (uint32_t i = 0; i < cap; ++i)
+        if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+    return false;
+}
+
 // Bulk copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completing `bytes` transactions on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)

@@ -22,17 +22,24 @@
 //                       2-3 stages, producer -> MMA
 // each with a "full" and an "empty" mbarrier per stage, so decoding step
 // k+1 overlaps the MMAs of step k and the compressed data runs ahead.
-// Warp roles (10 warps):
+// Warp roles (2 + 2 + 16 warps):
 //   warp 0     producer: bulk copies of C (up to 3 steps ahead) and TMA
 //              tensor loads of B.
 //   warp 1     allocates 256 * NSUB TMEM columns; lane 0 issues NSUB x 4
 //              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) per
 //              step and commits them to the A and B "empty" barriers.
-//   warps 2-9  decoders: each takes one GT and a quarter of its rows, scans
-//              the BT popcounts (shfl) for the value bases and writes the
-//              dense row-bytes into A; then arrive on "a_full" / "c_empty".
-//   warps 4-7  after the K loop: epilogue, tcgen05.ld of their TMEM lane
-//              quadrant, fp32 -> fp16, stores to Y[n][m].
+//   warps 2-3  scanners, one per GT: exclusive scan of the BT popcounts
+//              (shfl) and per-byte popcounts give the first value index of
+//              every BT row; the 512 row starts go into the C stage, then
+//              "c_scan".
+//   warps 4-19 decoders: eight per GT, each on 16 of its rows and half of
+//              its columns; per row-byte one byte of bitmap, one row start
+//              and eight predicated shared-memory loads (no branch per
+//              position) give the 16-byte chunk of A; then "a_full" /
+//              "c_empty".
+//   warps 4-19 after the K loop: epilogue, tcgen05.ld of their TMEM lane
+//              quadrant (warp % 4) and a quarter of the columns, fp32 ->
+//              fp16, stores to Y[n][m].
 // Every wait is bounded; a wait that gives up stores BSP_ERR_TIMEOUT in the
 // error word, and the CTA still drains its copies, waits for its MMAs and
 // frees its tensor memory before it exits.
@@ -52,8 +59,19 @@ constexpr int A_BYTES = BM * BK * 2;          // 16384
 constexpr int B_BYTES = BN * BK * 2;          // 32768 per 256-column sub-tile
 constexpr int VAL_BYTES = 513 * 16;           // dense GT value span + misalignment
 constexpr int SLOT = 512 + VAL_BYTES;         // bitmaps + values of one GT
-constexpr int DEC_WARPS = 8;
-constexpr int WARPS = 2 + DEC_WARPS;
+// Decoder warps: 8 (four per GroupTile, four row-bytes per lane and step)
+// or 16 (eight per GroupTile, two row-bytes per lane and step).
+#ifndef BSP_PF_DEC_WARPS
+#define BSP_PF_DEC_WARPS 16
+#endif
+constexpr int DEC_WARPS = BSP_PF_DEC_WARPS;
+static_assert(DEC_WARPS == 8 || DEC_WARPS == 16, "decoder warps");
+constexpr int WPG = DEC_WARPS / 2;   // decoder warps per GroupTile
+constexpr int RBL = 16 / WPG;        // row-bytes per lane and step
+constexpr int DEC0 = 4;              // first decoder warp (after producer, MMA, 2 scanners)
+constexpr int WARPS = DEC0 + DEC_WARPS;
+constexpr int RS_BYTES = 64 * 8 * 2; // row starts of one GT: [BT][row] u16
+constexpr uint32_t kSleepNs = 1000;  // suspend hint of the waiting polls
 constexpr int THREADS = WARPS * 32;
 
 // NSUB 256-column sub-tiles of N per CTA, each with its own TMEM
@@ -66,14 +84,16 @@ struct PCfg {
     static constexpr int SA = 2;                      // decoded A tiles        -> MMA
     static constexpr int SC = 3;                      // compressed GroupTiles  -> decoders
     static constexpr int B_STAGE = NSUB * B_BYTES;
-    static constexpr int C_STAGE = ((2 * SLOT + 16) + 127) & ~127;  // two GTs + header (shifts)
+    // two GTs, header (value shifts, 16 B), row starts of the two GTs
+    static constexpr int C_HDR = 2 * SLOT;
+    static constexpr int C_RS = C_HDR + 16;
+    static constexpr int C_STAGE = ((C_RS + 2 * RS_BYTES) + 127) & ~127;
     static constexpr int OFF_B = 0;                   // 1024-B aligned regions first
     static constexpr int OFF_A = OFF_B + SB * B_STAGE;
     static constexpr int OFF_C = OFF_A + SA * A_BYTES;
-    static constexpr int OFF_BASE = OFF_C + SC * C_STAGE;  // decoder warps' BT bases, 64 u32 each
-    static constexpr int OFF_BAR = OFF_BASE + DEC_WARPS * 256;
-    // barriers: c_full[SC] c_empty[SC] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc
-    static constexpr int NBAR = 2 * SC + 2 * SB + 2 * SA + 1;
+    static constexpr int OFF_BAR = OFF_C + SC * C_STAGE;
+    // barriers: c_full[SC] c_empty[SC] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc c_scan[SC]
+    static constexpr int NBAR = 3 * SC + 2 * SB + 2 * SA + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_TMEM + 16;
     static constexpr int SMEM = SMEM_USED + 1024;    // slack to align the base to 1024 B
@@ -103,6 +123,47 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
 __device__ __forceinline__ int bt_local(int br, int bc)
 {
     return (((br >> 1) * 4 + (bc >> 1)) << 2) + (br & 1) + ((bc & 1) << 1);
+}
+
+// One position of a row-byte, without a branch: if rbyte & bit, the next
+// packed fp16 value (shared-memory byte address `addr`) zero-extended, and
+// addr advances by one value; else 0.
+__device__ __forceinline__ uint32_t take_f16(uint32_t& addr, uint32_t rbyte, uint32_t bit)
+{
+    uint32_t v;
+    asm(
+        "{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
+        "and.b32 t, %2, %3;\n\t"
+        "setp.ne.b32 p, t, 0;\n\t"
+        "mov.b32 %0, 0;\n\t"
+        "@p ld.shared.u16 %0, [%1];\n\t"
+        "@p add.u32 %1, %1, 2;\n\t}"
+        : "=r"(v), "+r"(addr)
+        : "r"(rbyte), "r"(bit));
+    return v;
+}
+
+// First value index of each of the 8 rows of a BT whose first value is
+// `base`: row r starts after the set bits of rows 0..r-1.  Per-byte
+// popcounts by the usual bit-slicing sums, their running sum by one
+// multiply (bytes <= 32, no carry between them), then spread to u16 pairs
+// (r0 | r1 << 16, ..., r6 | r7 << 16).
+__device__ __forceinline__ uint4 row_starts(uint64_t bits, uint32_t base)
+{
+    uint32_t pre[2];
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+        uint32_t x = (uint32_t)(bits >> (32 * hw));
+        x = x - ((x >> 1) & 0x55555555u);
+        x = (x & 0x33333333u) + ((x >> 2) & 0x33333333u);
+        x = (x + (x >> 4)) & 0x0F0F0F0Fu;          // popcount of each byte (row)
+        const uint32_t incl = x * 0x01010101u;       // byte k: rows 0..k
+        pre[hw] = incl << 8;                         // byte k: rows 0..k-1
+    }
+    const uint32_t lo_total = (uint32_t)__popc((uint32_t)bits);
+    const uint32_t b0 = base * 0x10001u, b1 = (base + lo_total) * 0x10001u;
+    return make_uint4(__byte_perm(pre[0], 0u, 0x5140) + b0, __byte_perm(pre[0], 0u, 0x5342) + b0,
+                      __byte_perm(pre[1], 0u, 0x5140) + b1, __byte_perm(pre[1], 0u, 0x5342) + b1);
 }
 
 struct PrefillArgs {
@@ -144,18 +205,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
-// 32 consecutive TMEM columns of this thread's lane (32x32b shape, x32).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+// 16 consecutive TMEM columns of this thread's lane (32x32b shape, x16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -181,6 +239,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     uint64_t* a_full = b_empty + SB;
     uint64_t* a_empty = a_full + SA;
     uint64_t* acc_bar = a_empty + SA;
+    uint64_t* c_scan = acc_bar + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::OFF_TMEM);
     auto b_stage = [&](int s) { return smem + P::OFF_B + s * P::B_STAGE; };
     auto a_stage = [&](int s) { return smem + P::OFF_A + s * A_BYTES; };
@@ -216,6 +275,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             bspx::mbar_init(a_empty + s, 1);
         }
         bspx::mbar_init(acc_bar, 1);
+        for (int s = 0; s < SC; ++s) bspx::mbar_init(c_scan + s, 2 * 32);  // every scanner lane
         bspx::fence_mbar_init();
     }
     tc_fence_before();
@@ -235,7 +295,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const int s = (int)(kc % SC);
                 if (kc >= SC) {
                     const uint32_t ph = (uint32_t)(((kc / SC) - 1) & 1);
-                    if (!__all_sync(FULL, bspx::mbar_wait_bounded(c_empty + s, ph, cap))) { failed = true; break; }
+                    if (!__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph, cap, kSleepNs))) { failed = true; break; }
                 }
                 if (kc - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
                     wbase = kc;
@@ -248,7 +308,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
                 if (lane == 0) {
                     uint8_t* st = c_stage(s);
-                    uint32_t* hdr = reinterpret_cast<uint32_t*>(st + 2 * SLOT);
+                    uint32_t* hdr = reinterpret_cast<uint32_t*>(st + P::C_HDR);
                     const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
                     const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
                     hdr[0] = oa0 - cha * 8;
@@ -269,7 +329,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const int s = (int)(kx % SB);
                 if (kx >= SB) {
                     const uint32_t ph = (uint32_t)(((kx / SB) - 1) & 1);
-                    if (!__all_sync(FULL, bspx::mbar_wait_bounded(b_empty + s, ph, cap))) { failed = true; break; }
+                    if (!__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph, cap, kSleepNs))) { failed = true; break; }
                 }
                 if (lane == 0) {
                     bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
@@ -288,8 +348,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         // ---------------- MMA issuer
         for (int64_t kb = 0; kb < KT; ++kb) {
             const int sa = (int)(kb % SA), sb = (int)(kb % SB);
-            const bool ok = bspx::mbar_wait_bounded(a_full + sa, (uint32_t)((kb / SA) & 1), cap) &&
-                            bspx::mbar_wait_bounded(b_full + sb, (uint32_t)((kb / SB) & 1), cap);
+            const bool ok = bspx::mbar_wait_sleep(a_full + sa, (uint32_t)((kb / SA) & 1), cap, kSleepNs) &&
+                            bspx::mbar_wait_sleep(b_full + sb, (uint32_t)((kb / SB) & 1), cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
@@ -310,37 +370,19 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
         __syncwarp();
         bspx::mbar_wait_bounded(acc_bar, 0, cap);
-    } else {
-        // ---------------- decoders
-        const int dw = warp - 2;
-        const int gsel = dw >> 2, q = dw & 3;
-        uint32_t* base_s = reinterpret_cast<uint32_t*>(smem + P::OFF_BASE + dw * 256);
-        // lane: row 16q + (lane & 15) of the GT, octets 2p + half (p = 0..3), so
-        // one step of a warp reads a single TCTile (rows 16q.., octets 2p, 2p+1)
-        const int row = 16 * q + (lane & 15);       // row inside the GT
-        const int trow = 64 * gsel + row;           // row inside the 128-row tile
-        const int br = row >> 3, rr = row & 7;
-        const int half = lane >> 4;
-        // The two half-warps read the two column halves of a TCTile, about
-        // 32 words apart: one bank cycle.  The upper half walks its
-        // positions rotated by 4 (4..7 then 0..3) so that the lanes of one
-        // step do not meet in the same bank.
-        const bool rot = half != 0;
-        const uint32_t rsh = 8u * (uint32_t)(rr & 3);
-        const bool hi = rr >= 4;
-        const uint32_t lowm = (1u << rsh) - 1u;
+    } else if (warp < DEC0) {
+        // ---------------- scanners: row starts of GT (warp - 2)
+        const int gsel = warp - 2;
         const bool active = gsel == 0 || has_b;
         for (int64_t kb = 0; kb < KT; ++kb) {
-            const int sc = (int)(kb % SC), sa = (int)(kb % SA);
-            bool ok = bspx::mbar_wait_bounded(c_full + sc, (uint32_t)((kb / SC) & 1), cap);
-            if (kb >= SA) ok = ok && bspx::mbar_wait_bounded(a_empty + sa, (uint32_t)(((kb / SA) - 1) & 1), cap);
+            const int sc = (int)(kb % SC);
+            const bool ok = bspx::mbar_wait_sleep(c_full + sc, (uint32_t)((kb / SC) & 1), cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
-            const uint8_t* st = c_stage(sc);
+            uint8_t* st = c_stage(sc);
             if (active) {
-                const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st + gsel * SLOT);
-                const uint16_t* vh = reinterpret_cast<const uint16_t*>(st + gsel * SLOT + 512);
-                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + 2 * SLOT)[gsel];
-                const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(bm_st)[lane];
+                // lane: BTs 2 lane and 2 lane + 1 (GT order = value order)
+                const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(st + gsel * SLOT)[lane];
+                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + P::C_HDR)[gsel];
                 const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
                 uint32_t incl = c0 + c1;
 #pragma unroll
@@ -348,38 +390,60 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                     const uint32_t o = __shfl_up_sync(FULL, incl, d);
                     if (lane >= d) incl += o;
                 }
-                const uint32_t ex = incl - (c0 + c1) + shift;
-                base_s[2 * lane] = ex;
-                base_s[2 * lane + 1] = ex + c0;
-                __syncwarp();
-                uint8_t* arow = a_stage(sa) + (trow >> 3) * 1024 + (trow & 7) * 128;
+                const uint32_t base0 = incl - (c0 + c1) + shift;
+                uint4* rs = reinterpret_cast<uint4*>(st + P::C_RS + gsel * RS_BYTES) + 2 * lane;
+                rs[0] = row_starts(bb.x, base0);
+                rs[1] = row_starts(bb.y, base0 + c0);
+            }
+            bspx::mbar_arrive(c_scan + sc);  // release: the row starts above
+        }
+    } else {
+        // ---------------- decoders
+        const int dw = warp - DEC0;
+        const int gsel = dw / WPG, wq = dw % WPG;
+        const int q = wq / (4 / RBL);             // TCTile row of the warp (16 GT rows)
+        const int p0 = (wq % (4 / RBL)) * RBL;    // first TCTile column (octet pair)
+        // lane: row 16q + (lane & 15) of the GT, octets 2p + half for the
+        // warp's RBL TCTile columns p, so one step of a warp reads a single
+        // TCTile (rows 16q.., octets 2p, 2p+1): the bitmap bytes and row
+        // starts of one step are 32 consecutive entries
+        const int row = 16 * q + (lane & 15);       // row inside the GT
+        const int trow = 64 * gsel + row;           // row inside the 128-row tile
+        const int half = lane >> 4;
+        int ent[RBL];       // BT row entry: 8 g + row % 8 (bitmap byte / row start)
+        uint32_t dst[RBL];  // byte offset of the row-byte's 16-B chunk in A (128-B swizzle)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int bc = 2 * j + half;
-                    const int g = bt_local(br, bc);
-                    const uint2 bm = *reinterpret_cast<const uint2*>(bm_st + g);
-                    const uint32_t w32 = hi ? bm.y : bm.x;
-                    const uint32_t byte = (w32 >> rsh) & 0xFFu;
-                    const uint32_t start = base_s[g] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
-                    const uint32_t rbyte = rot ? ((byte >> 4) | (byte << 4)) & 0xFFu : byte;
-                    uint32_t idx = rot ? start + (uint32_t)__popc(byte & 0xFu) : start;
+        for (int j = 0; j < RBL; ++j) {
+            const int bc = 2 * (p0 + j) + half;
+            ent[j] = 8 * bt_local(row >> 3, bc) + (row & 7);
+            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4));
+        }
+        const bool active = gsel == 0 || has_b;
+        for (int64_t kb = 0; kb < KT; ++kb) {
+            const int sc = (int)(kb % SC), sa = (int)(kb % SA);
+            const uint32_t pc = (uint32_t)((kb / SC) & 1);
+            bool ok = bspx::mbar_wait_sleep(c_scan + sc, pc, cap, kSleepNs) &&
+                      bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
+            if (kb >= SA)
+                ok = ok && bspx::mbar_wait_sleep(a_empty + sa, (uint32_t)(((kb / SA) - 1) & 1), cap, kSleepNs);
+            if (!__all_sync(FULL, ok)) { failed = true; break; }
+            const uint8_t* st = c_stage(sc);
+            if (active) {
+                const uint8_t* bmb = st + gsel * SLOT;  // bitmap bytes: byte 8 g + r = row r of BT g
+                const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + P::C_RS + gsel * RS_BYTES);
+                const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
+                uint8_t* at = a_stage(sa);
+#pragma unroll
+                for (int j = 0; j < RBL; ++j) {
+                    const uint32_t byte = bmb[ent[j]];
+                    uint32_t addr = vbase + 2u * (uint32_t)rst[ent[j]];
                     uint32_t h[8];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (c == 4 && rot) idx = start;
-                        const uint32_t bit = (rbyte >> c) & 1u;
-                        uint32_t v = 0;
-                        if (bit) v = vh[idx];
-                        idx += bit;
-                        h[c] = v;
-                    }
-                    const uint32_t w0 = h[0] | (h[1] << 16), w1 = h[2] | (h[3] << 16);
-                    const uint32_t w2 = h[4] | (h[5] << 16), w3 = h[6] | (h[7] << 16);
-                    const uint4 chunk = rot ? make_uint4(w2, w3, w0, w1) : make_uint4(w0, w1, w2, w3);
-                    // row-byte = one 16-B chunk; 128-B swizzle: chunk index ^ (row % 8)
-                    *reinterpret_cast<uint4*>(arow + ((bc ^ (trow & 7)) << 4)) = chunk;
+                    for (int c = 0; c < 8; ++c) h[c] = take_f16(addr, byte, 1u << c);
+                    const uint4 chunk = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                                   h[6] | (h[7] << 16));
+                    *reinterpret_cast<uint4*>(at + dst[j]) = chunk;
                 }
-                __syncwarp();
             }
             // make the generic-proxy writes of A visible to the tensor cores
             bspx::fence_proxy_async_smem();
@@ -389,23 +453,26 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 bspx::mbar_arrive(c_empty + sc);
             }
         }
-        // ---------------- epilogue (warps 4-7 own TMEM lane quadrants 0-3)
-        if (warp >= 4 && warp < 8) {
-            const bool ok = __all_sync(FULL, bspx::mbar_wait_bounded(acc_bar, 0, cap));
+        // ---------------- epilogue: every decoder warp; warp w reads TMEM lane
+        // quadrant w % 4 (the lanes a warp may access), and the DEC_WARPS / 4
+        // groups of four consecutive warps split the columns
+        {
+            const bool ok = __all_sync(FULL, bspx::mbar_wait_sleep(acc_bar, 0, cap, kSleepNs));
             if (!ok) {
                 failed = true;
             } else if (!failed) {
                 tc_fence_after();
-                const int quad = warp & 3;
+                constexpr int COLS = P::BN_CTA / (DEC_WARPS / 4);
+                const int quad = warp & 3, cg = dw >> 2;  // warps 4-7, 8-11, ...: quadrants 0-3
                 const int64_t m = mt * BM + 32 * quad + lane;
 #pragma unroll 1
-                for (int cb = 0; cb < P::BN_CTA / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem_base + ((uint32_t)(32 * quad) << 16) + (uint32_t)(cb * 32), r);
+                for (int cb = cg * COLS; cb < (cg + 1) * COLS; cb += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem_base + ((uint32_t)(32 * quad) << 16) + (uint32_t)cb, r);
                     if (m < M) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t n = n0 + cb * 32 + j;
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t n = n0 + cb + j;
                             if (n < N) a.Y[n * M + m] = __float2half_rn(__uint_as_float(r[j]));
                         }
                     }
