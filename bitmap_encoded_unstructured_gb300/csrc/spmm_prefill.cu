@@ -22,9 +22,12 @@
 //                       2-3 stages, producer -> MMA
 // each with a "full" and an "empty" mbarrier per stage, so decoding step
 // k+1 overlaps the MMAs of step k and the compressed data runs ahead.
-// Warp roles (2 + 2 + 16 warps):
-//   warp 0     producer: bulk copies of C (up to 3 steps ahead) and TMA
-//              tensor loads of B.
+// Warp roles (21 warps):
+//   warp 0     C producer: bulk copies of the compressed GTs, up to SC
+//              steps ahead of the decoders.
+//   warp 20    B producer: TMA tensor loads of the X tiles, up to SB steps
+//              ahead of the MMAs (its own warp, so that neither ring waits
+//              on the other).
 //   warp 1     allocates 256 * NSUB TMEM columns; lane 0 issues NSUB x 4
 //              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) per
 //              step and commits them to the A and B "empty" barriers.
@@ -69,7 +72,8 @@ static_assert(DEC_WARPS == 8 || DEC_WARPS == 16, "decoder warps");
 constexpr int WPG = DEC_WARPS / 2;   // decoder warps per GroupTile
 constexpr int RBL = 16 / WPG;        // row-bytes per lane and step
 constexpr int DEC0 = 4;              // first decoder warp (after producer, MMA, 2 scanners)
-constexpr int WARPS = DEC0 + DEC_WARPS;
+constexpr int BPROD = DEC0 + DEC_WARPS;  // B (X tile) producer, the last warp
+constexpr int WARPS = BPROD + 1;
 constexpr int RS_BYTES = 64 * 8 * 2; // row starts of one GT: [BT][row] u16
 constexpr uint32_t kSleepNs = 1000;  // suspend hint of the waiting polls
 constexpr int THREADS = WARPS * 32;
@@ -246,7 +250,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     auto c_stage = [&](int s) { return smem + P::OFF_C + s * P::C_STAGE; };
 
     const int64_t M = a.M, N = a.N, K = a.K;
-    const int64_t KT = K >> 6;
+    const uint32_t KT = (uint32_t)(K >> 6);
     const int64_t mt = blockIdx.y;
     const int64_t n0 = (int64_t)blockIdx.x * P::BN_CTA;
     const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
@@ -285,71 +289,74 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     bool failed = false;
 
     if (warp == 0) {
-        // ---------------- producer: compressed GTs up to SC steps ahead, X tiles up to SB
+        // ---------------- C producer: the two GTs of each step, up to SC steps ahead
         const int64_t ta = strip0 * KT, tb = strip1 * KT;
         uint32_t offa = 0, offb = 0;
-        int64_t wbase = -64;
-        int64_t kc = 0, kx = 0;  // next compressed step / next X step to issue
-        while ((kc < KT || kx < KT) && !failed) {
-            if (kc < KT && kc < kx + SC) {
-                const int s = (int)(kc % SC);
-                if (kc >= SC) {
-                    const uint32_t ph = (uint32_t)(((kc / SC) - 1) & 1);
-                    if (!__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph, cap, kSleepNs))) { failed = true; break; }
-                }
-                if (kc - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
-                    wbase = kc;
-                    const int64_t i = wbase + lane;
-                    offa = (i <= KT) ? __ldg(a.offsets + ta + i) : 0u;
-                    offb = (has_b && i <= KT) ? __ldg(a.offsets + tb + i) : 0u;
-                }
-                const int w = (int)(kc - wbase);
-                const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
-                const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
-                if (lane == 0) {
-                    uint8_t* st = c_stage(s);
-                    uint32_t* hdr = reinterpret_cast<uint32_t*>(st + P::C_HDR);
-                    const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
-                    const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
-                    hdr[0] = oa0 - cha * 8;
-                    hdr[1] = ob0 - chb * 8;
-                    uint32_t bytes = 512 + nca * 16;
-                    if (has_b) bytes += 512 + ncb * 16;
-                    bspx::mbar_arrive_expect_tx(c_full + s, bytes);
-                    bspx::bulk_g2s(st, a.bitmaps + (ta + kc) * 64, 512, c_full + s);
-                    if (nca) bspx::bulk_g2s(st + 512, a.values + (int64_t)cha * 16, nca * 16, c_full + s);
-                    if (has_b) {
-                        bspx::bulk_g2s(st + SLOT, a.bitmaps + (tb + kc) * 64, 512, c_full + s);
-                        if (ncb)
-                            bspx::bulk_g2s(st + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, c_full + s);
-                    }
-                }
-                ++kc;
-            } else {
-                const int s = (int)(kx % SB);
-                if (kx >= SB) {
-                    const uint32_t ph = (uint32_t)(((kx / SB) - 1) & 1);
-                    if (!__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph, cap, kSleepNs))) { failed = true; break; }
-                }
-                if (lane == 0) {
-                    bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
-                    for (int u = 0; u < NSUB; ++u)
-                        tma_load_2d(b_stage(s) + u * B_BYTES, &tmX, (int)(kx * BK), (int)(n0 + u * BN), b_full + s);
-                }
-                ++kx;
+        uint32_t wbase = 0;
+        uint32_t s = 0, ph = 0;  // stage and its phase parity
+        uint32_t kc = 0;         // steps issued
+        for (; kc < KT; ++kc) {
+            if (kc >= (uint32_t)SC &&
+                !__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph ^ 1u, cap, kSleepNs))) {
+                failed = true;
+                break;
             }
+            if (kc == 0 || kc - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
+                wbase = kc;
+                const uint32_t i = wbase + lane;
+                offa = (i <= KT) ? __ldg(a.offsets + ta + i) : 0u;
+                offb = (has_b && i <= KT) ? __ldg(a.offsets + tb + i) : 0u;
+            }
+            const int w = (int)(kc - wbase);
+            const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
+            const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
+            if (lane == 0) {
+                uint8_t* st = c_stage(s);
+                uint32_t* hdr = reinterpret_cast<uint32_t*>(st + P::C_HDR);
+                const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
+                const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                hdr[0] = oa0 - cha * 8;
+                hdr[1] = ob0 - chb * 8;
+                uint32_t bytes = 512 + nca * 16;
+                if (has_b) bytes += 512 + ncb * 16;
+                bspx::mbar_arrive_expect_tx(c_full + s, bytes);
+                bspx::bulk_g2s(st, a.bitmaps + (ta + kc) * 64, 512, c_full + s);
+                if (nca) bspx::bulk_g2s(st + 512, a.values + (int64_t)cha * 16, nca * 16, c_full + s);
+                if (has_b) {
+                    bspx::bulk_g2s(st + SLOT, a.bitmaps + (tb + kc) * 64, 512, c_full + s);
+                    if (ncb) bspx::bulk_g2s(st + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, c_full + s);
+                }
+            }
+            if (++s == (uint32_t)SC) { s = 0; ph ^= 1u; }
         }
         // let the last copies land before the CTA can exit (bounded)
-        for (int64_t k = (kc > SC ? kc - SC : 0); k < kc; ++k)
-            bspx::mbar_wait_bounded(c_full + (k % SC), (uint32_t)((k / SC) & 1), cap);
-        for (int64_t k = (kx > SB ? kx - SB : 0); k < kx; ++k)
-            bspx::mbar_wait_bounded(b_full + (k % SB), (uint32_t)((k / SB) & 1), cap);
+        for (uint32_t k = (kc > (uint32_t)SC ? kc - SC : 0); k < kc; ++k)
+            bspx::mbar_wait_bounded(c_full + (k % SC), (k / SC) & 1u, cap);
+    } else if (warp == BPROD) {
+        // ---------------- B producer: X tiles by TMA, up to SB steps ahead
+        uint32_t s = 0, ph = 0;
+        uint32_t kx = 0;  // steps issued
+        for (; kx < KT; ++kx) {
+            if (kx >= (uint32_t)SB &&
+                !__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph ^ 1u, cap, kSleepNs))) {
+                failed = true;
+                break;
+            }
+            if (lane == 0) {
+                bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
+                for (int u = 0; u < NSUB; ++u)
+                    tma_load_2d(b_stage(s) + u * B_BYTES, &tmX, (int)(kx * BK), (int)(n0 + u * BN), b_full + s);
+            }
+            if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
+        }
+        for (uint32_t k = (kx > (uint32_t)SB ? kx - SB : 0); k < kx; ++k)
+            bspx::mbar_wait_bounded(b_full + (k % SB), (k / SB) & 1u, cap);
     } else if (warp == 1) {
         // ---------------- MMA issuer
-        for (int64_t kb = 0; kb < KT; ++kb) {
-            const int sa = (int)(kb % SA), sb = (int)(kb % SB);
-            const bool ok = bspx::mbar_wait_sleep(a_full + sa, (uint32_t)((kb / SA) & 1), cap, kSleepNs) &&
-                            bspx::mbar_wait_sleep(b_full + sb, (uint32_t)((kb / SB) & 1), cap, kSleepNs);
+        uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
+        for (uint32_t kb = 0; kb < KT; ++kb) {
+            const bool ok = bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs) &&
+                            bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
@@ -366,6 +373,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 umma_commit(b_empty + sb);
             }
             __syncwarp();
+            if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
+            if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
         }
         if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
         __syncwarp();
@@ -374,9 +383,9 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         // ---------------- scanners: row starts of GT (warp - 2)
         const int gsel = warp - 2;
         const bool active = gsel == 0 || has_b;
-        for (int64_t kb = 0; kb < KT; ++kb) {
-            const int sc = (int)(kb % SC);
-            const bool ok = bspx::mbar_wait_sleep(c_full + sc, (uint32_t)((kb / SC) & 1), cap, kSleepNs);
+        uint32_t sc = 0, pc = 0;
+        for (uint32_t kb = 0; kb < KT; ++kb) {
+            const bool ok = bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             uint8_t* st = c_stage(sc);
             if (active) {
@@ -396,6 +405,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 rs[1] = row_starts(bb.y, base0 + c0);
             }
             bspx::mbar_arrive(c_scan + sc);  // release: the row starts above
+            if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
         }
     } else {
         // ---------------- decoders
@@ -419,13 +429,11 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4));
         }
         const bool active = gsel == 0 || has_b;
-        for (int64_t kb = 0; kb < KT; ++kb) {
-            const int sc = (int)(kb % SC), sa = (int)(kb % SA);
-            const uint32_t pc = (uint32_t)((kb / SC) & 1);
-            bool ok = bspx::mbar_wait_sleep(c_scan + sc, pc, cap, kSleepNs) &&
-                      bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
-            if (kb >= SA)
-                ok = ok && bspx::mbar_wait_sleep(a_empty + sa, (uint32_t)(((kb / SA) - 1) & 1), cap, kSleepNs);
+        uint32_t sc = 0, pc = 0, sa = 0, pa = 0;
+        for (uint32_t kb = 0; kb < KT; ++kb) {
+            // c_scan implies c_full: the scanners arrive only after they saw it
+            bool ok = bspx::mbar_wait_sleep(c_scan + sc, pc, cap, kSleepNs);
+            if (kb >= (uint32_t)SA) ok = ok && bspx::mbar_wait_sleep(a_empty + sa, pa ^ 1u, cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             const uint8_t* st = c_stage(sc);
             if (active) {
@@ -452,6 +460,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 bspx::mbar_arrive(a_full + sa);
                 bspx::mbar_arrive(c_empty + sc);
             }
+            if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
+            if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
         }
         // ---------------- epilogue: every decoder warp; warp w reads TMEM lane
         // quadrant w % 4 (the lanes a warp may access), and the DEC_WARPS / 4
