@@ -18,14 +18,14 @@
 //                       3 stages, producer -> decoders
 //   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB),
 //                       2 stages, decoders -> MMA
-//   B  X tile(s)        NSUB x 256 x 64 fp16, K-major, SWIZZLE_128B (TMA),
-//                       2-3 stages, producer -> MMA
+//   B  X sub-tiles      256 x 64 fp16 each, K-major, SWIZZLE_128B (TMA),
+//                       4 stages (NSUB per step), producer -> MMA
 // each with a "full" and an "empty" mbarrier per stage, so decoding step
 // k+1 overlaps the MMAs of step k and the compressed data runs ahead.
 // Warp roles (21 warps):
 //   warp 0     C producer: bulk copies of the compressed GTs, up to SC
 //              steps ahead of the decoders.
-//   warp 20    B producer: TMA tensor loads of the X tiles, up to SB steps
+//   warp 20    B producer: TMA tensor loads of the X sub-tiles, up to 4
 //              ahead of the MMAs (its own warp, so that neither ring waits
 //              on the other).
 //   warp 1     allocates 256 * NSUB TMEM columns; lane 0 issues NSUB x 4
@@ -84,10 +84,10 @@ template <int NSUB>
 struct PCfg {
     static constexpr int BN_CTA = BN * NSUB;
     // three rings with their own depths
-    static constexpr int SB = NSUB == 1 ? 3 : 2;     // X tiles (TMA)          -> MMA
+    static constexpr int SB = 4;                      // X sub-tiles (TMA)      -> MMA
     static constexpr int SA = 2;                      // decoded A tiles        -> MMA
     static constexpr int SC = 3;                      // compressed GroupTiles  -> decoders
-    static constexpr int B_STAGE = NSUB * B_BYTES;
+    static constexpr int B_STAGE = B_BYTES;          // one 256-column sub-tile per stage
     // two GTs, header (value shifts, 16 B), row starts of the two GTs
     static constexpr int C_HDR = 2 * SLOT;
     static constexpr int C_RS = C_HDR + 16;
@@ -333,48 +333,52 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         for (uint32_t k = (kc > (uint32_t)SC ? kc - SC : 0); k < kc; ++k)
             bspx::mbar_wait_bounded(c_full + (k % SC), (k / SC) & 1u, cap);
     } else if (warp == BPROD) {
-        // ---------------- B producer: X tiles by TMA, up to SB steps ahead
+        // ---------------- B producer: X sub-tiles by TMA, (step, sub-tile) order,
+        // up to SB sub-tiles ahead: a stage frees as soon as the MMAs of its
+        // own sub-tile are done, half a step before those of the next one
         uint32_t s = 0, ph = 0;
-        uint32_t kx = 0;  // steps issued
-        for (; kx < KT; ++kx) {
-            if (kx >= (uint32_t)SB &&
+        uint32_t i = 0;  // sub-tiles issued
+        const uint32_t nb = KT * NSUB;
+        for (; i < nb; ++i) {
+            if (i >= (uint32_t)SB &&
                 !__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph ^ 1u, cap, kSleepNs))) {
                 failed = true;
                 break;
             }
             if (lane == 0) {
-                bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
-                for (int u = 0; u < NSUB; ++u)
-                    tma_load_2d(b_stage(s) + u * B_BYTES, &tmX, (int)(kx * BK), (int)(n0 + u * BN), b_full + s);
+                const uint32_t kx = i / NSUB, u = i % NSUB;
+                bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)B_BYTES);
+                tma_load_2d(b_stage(s), &tmX, (int)(kx * BK), (int)(n0 + u * BN), b_full + s);
             }
             if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
         }
-        for (uint32_t k = (kx > (uint32_t)SB ? kx - SB : 0); k < kx; ++k)
+        for (uint32_t k = (i > (uint32_t)SB ? i - SB : 0); k < i; ++k)
             bspx::mbar_wait_bounded(b_full + (k % SB), (k / SB) & 1u, cap);
     } else if (warp == 1) {
         // ---------------- MMA issuer
         uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
-        for (uint32_t kb = 0; kb < KT; ++kb) {
-            const bool ok = bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs) &&
-                            bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
-            if (!__all_sync(FULL, ok)) { failed = true; break; }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t ad = smem_desc_sw128(bspx::smem_u32(a_stage(sa)));
+        for (uint32_t kb = 0; kb < KT && !failed; ++kb) {
+            if (!__all_sync(FULL, bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs))) { failed = true; break; }
+            const uint64_t ad = smem_desc_sw128(bspx::smem_u32(a_stage(sa)));
 #pragma unroll
-                for (int u = 0; u < NSUB; ++u) {
-                    const uint64_t bd = smem_desc_sw128(bspx::smem_u32(b_stage(sb) + u * B_BYTES));
+            for (int u = 0; u < NSUB; ++u) {
+                if (!__all_sync(FULL, bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs))) { failed = true; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t bd = smem_desc_sw128(bspx::smem_u32(b_stage(sb)));
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
                         umma_f16(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
                                  (kb | j) ? 1u : 0u);
+                    umma_commit(b_empty + sb);  // fires once the MMAs above are done
                 }
-                umma_commit(a_empty + sa);  // each fires once the MMAs above are done
-                umma_commit(b_empty + sb);
+                __syncwarp();
+                if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
             }
+            if (failed) break;
+            if (lane == 0) umma_commit(a_empty + sa);
             __syncwarp();
             if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
-            if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
         }
         if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
         __syncwarp();
