@@ -36,10 +36,9 @@
 //              every BT row; the 512 row starts go into the C stage, then
 //              "c_scan".
 //   warps 4-19 decoders: eight per GT, each on 16 of its rows and half of
-//              its columns; per row-byte one byte of bitmap, one row start
-//              and eight predicated shared-memory loads (no branch per
-//              position) give the 16-byte chunk of A; then "a_full" /
-//              "c_empty".
+//              its columns; per half row-byte one byte of bitmap, one row
+//              start and four predicated shared-memory loads (no branch per
+//              position) give 8 bytes of A; then "a_full" / "c_empty".
 //   warps 4-19 after the K loop: epilogue, tcgen05.ld of their TMEM lane
 //              quadrant (warp % 4) and a quarter of the columns, fp32 ->
 //              fp16, stores to Y[n][m].
@@ -62,15 +61,16 @@ constexpr int A_BYTES = BM * BK * 2;          // 16384
 constexpr int B_BYTES = BN * BK * 2;          // 32768 per 256-column sub-tile
 constexpr int VAL_BYTES = 513 * 16;           // dense GT value span + misalignment
 constexpr int SLOT = 512 + VAL_BYTES;         // bitmaps + values of one GT
-// Decoder warps: 8 (four per GroupTile, four row-bytes per lane and step)
-// or 16 (eight per GroupTile, two row-bytes per lane and step).
+// Decoder warps: 8 (four per GroupTile, eight half row-bytes per lane and
+// step) or 16 (eight per GroupTile, four half row-bytes per lane and step).
 #ifndef BSP_PF_DEC_WARPS
 #define BSP_PF_DEC_WARPS 16
 #endif
 constexpr int DEC_WARPS = BSP_PF_DEC_WARPS;
 static_assert(DEC_WARPS == 8 || DEC_WARPS == 16, "decoder warps");
 constexpr int WPG = DEC_WARPS / 2;   // decoder warps per GroupTile
-constexpr int RBL = 16 / WPG;        // row-bytes per lane and step
+constexpr int NU = 32 / WPG;         // units (half row-bytes) per lane and step
+constexpr int TCW = NU / 2;          // TCTile columns per warp
 constexpr int DEC0 = 4;              // first decoder warp (after producer, MMA, 2 scanners)
 constexpr int BPROD = DEC0 + DEC_WARPS;  // B (X tile) producer, the last warp
 constexpr int WARPS = BPROD + 1;
@@ -415,22 +415,28 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         // ---------------- decoders
         const int dw = warp - DEC0;
         const int gsel = dw / WPG, wq = dw % WPG;
-        const int q = wq / (4 / RBL);             // TCTile row of the warp (16 GT rows)
-        const int p0 = (wq % (4 / RBL)) * RBL;    // first TCTile column (octet pair)
-        // lane: row 16q + (lane & 15) of the GT, octets 2p + half for the
-        // warp's RBL TCTile columns p, so one step of a warp reads a single
-        // TCTile (rows 16q.., octets 2p, 2p+1): the bitmap bytes and row
-        // starts of one step are 32 consecutive entries
-        const int row = 16 * q + (lane & 15);       // row inside the GT
-        const int trow = 64 * gsel + row;           // row inside the 128-row tile
-        const int half = lane >> 4;
-        int ent[RBL];       // BT row entry: 8 g + row % 8 (bitmap byte / row start)
-        uint32_t dst[RBL];  // byte offset of the row-byte's 16-B chunk in A (128-B swizzle)
+        const int q = wq / (4 / TCW);             // TCTile row of the warp (16 GT rows)
+        const int p0 = (wq % (4 / TCW)) * TCW;    // first TCTile column (octet pair)
+        // Unit j of a lane: row 16q + 8 (lane / 16) + lane % 8 of the GT,
+        // octet bc = 2 (p0 + j / 2) + j % 2, and of its 8 positions the low
+        // (lane bit 3 clear) or the high half.  One unit of a warp thus reads
+        // the values of two BTs adjacent in value order (TL and BL, or TR
+        // and BR, of one TCTile): about 128 B at 50% density, where whole
+        // row-bytes per lane would span four BTs.  Each half-warp writes
+        // eight whole 16-B chunks of eight consecutive rows, which the
+        // swizzle puts in distinct banks.
+        const int row = 16 * q + 8 * (lane >> 4) + (lane & 7);  // row inside the GT
+        const int trow = 64 * gsel + row;                       // row inside the 128-row tile
+        const int half = (lane >> 3) & 1;
+        const uint32_t nsh = 4u * (uint32_t)half;            // the lane's half of the row-byte
+        const uint32_t lowm = half ? 0xFu : 0u;              // positions before it
+        int ent[NU];        // BT row entry: 8 g + row % 8 (bitmap byte / row start)
+        uint32_t dst[NU];   // byte offset of the unit's 8 bytes in A (128-B swizzle)
 #pragma unroll
-        for (int j = 0; j < RBL; ++j) {
-            const int bc = 2 * (p0 + j) + half;
+        for (int j = 0; j < NU; ++j) {
+            const int bc = 2 * (p0 + j / 2) + (j & 1);
             ent[j] = 8 * bt_local(row >> 3, bc) + (row & 7);
-            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4));
+            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4) + 8 * half);
         }
         const bool active = gsel == 0 || has_b;
         uint32_t sc = 0, pc = 0, sa = 0, pa = 0;
@@ -446,15 +452,15 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
                 uint8_t* at = a_stage(sa);
 #pragma unroll
-                for (int j = 0; j < RBL; ++j) {
+                for (int j = 0; j < NU; ++j) {
                     const uint32_t byte = bmb[ent[j]];
-                    uint32_t addr = vbase + 2u * (uint32_t)rst[ent[j]];
-                    uint32_t h[8];
+                    const uint32_t start = (uint32_t)rst[ent[j]] + (uint32_t)__popc(byte & lowm);
+                    const uint32_t nib = byte >> nsh;
+                    uint32_t addr = vbase + 2u * start;
+                    uint32_t h[4];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) h[c] = take_f16(addr, byte, 1u << c);
-                    const uint4 chunk = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                                                   h[6] | (h[7] << 16));
-                    *reinterpret_cast<uint4*>(at + dst[j]) = chunk;
+                    for (int c = 0; c < 4; ++c) h[c] = take_f16(addr, nib, 1u << c);
+                    *reinterpret_cast<uint2*>(at + dst[j]) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
                 }
             }
             // make the generic-proxy writes of A visible to the tensor cores
