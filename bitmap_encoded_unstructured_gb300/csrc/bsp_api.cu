@@ -79,6 +79,7 @@ bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
     h->K = K;
     h->NGT = (M / 64) * (K / 64);
     h->NBT = M * K / 64;
+    h->max_gt_nnz = 4096;  // set from the arrays by the encoder / the import check
     return h;
 }
 

@@ -17,6 +17,7 @@ struct bsp_handle {
     int64_t M, K;         // multiples of 64
     int64_t NGT, NBT;     // GroupTiles (64x64), BitmapTiles (8x8)
     uint64_t NNZ;
+    uint32_t max_gt_nnz;  // largest nonzero count of one GT (sizes the decode stages)
     uint64_t* bitmaps;    // [NBT]
     uint32_t* offsets;    // [NGT + 1]
     void* values;         // [NNZ] elements + >= 16 B zeroed tail slack
@@ -45,8 +46,9 @@ enum bsp_out_mode { BSP_OUT_F16 = 0, BSP_OUT_I32 = 1, BSP_OUT_F32_SCALED = 2 };
 // ---- encoder / decoder (encode.cu) ----
 bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s);
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s);
-// Check that offsets and bitmaps agree (imported arrays); synchronises s.
-bsp_status_t bsp_run_validate(const bsp_handle* h, cudaStream_t s);
+// Check that offsets and bitmaps agree (imported arrays) and set
+// h->max_gt_nnz; synchronises s.
+bsp_status_t bsp_run_validate(bsp_handle* h, cudaStream_t s);
 
 // ---- CUDA-core decode-path product (spmm_decode.cu) ----
 // Everything the decode kernel reads and writes besides X and Y: the
@@ -59,6 +61,7 @@ struct bsp_decode_problem {
     const void* values;
     bsp_dtype_t dtype;
     int64_t M, K;
+    uint32_t max_gt_nnz;  // bound on the nonzeros of one GT (4096: unknown)
     int device, num_sms;
     void* ws;
     uint32_t* counters;

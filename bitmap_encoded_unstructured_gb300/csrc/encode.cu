@@ -105,7 +105,7 @@ __global__ void enc_bitmap_kernel(const void* __restrict__ W, int64_t n_rowbytes
 // GT nonzero total.
 __global__ void enc_count_kernel(const uint64_t* __restrict__ bitmaps, int64_t NGT,
                                  uint32_t* __restrict__ bt_prefix,
-                                 uint32_t* __restrict__ gt_nnz)
+                                 uint32_t* __restrict__ gt_nnz, unsigned int* max_nnz)
 {
     const int lane = threadIdx.x & 31;
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -121,7 +121,10 @@ __global__ void enc_count_kernel(const uint64_t* __restrict__ bitmaps, int64_t N
     const uint32_t ex = incl - (c0 + c1);
     bt_prefix[t * 64 + 2 * lane] = ex;
     bt_prefix[t * 64 + 2 * lane + 1] = ex + c0;
-    if (lane == 31) gt_nnz[t] = incl;
+    if (lane == 31) {
+        gt_nnz[t] = incl;
+        atomicMax(max_nnz, incl);
+    }
 }
 
 // Pass 3: exclusive scan of the per-GT counts into offsets[NGT+1], one
@@ -253,7 +256,8 @@ inline unsigned grid_for(int64_t n, int block) { return (unsigned)((n + block - 
 
 // Validation of imported arrays: offsets[0] == 0 and, for every GT,
 // offsets[t+1] - offsets[t] == sum of the popcounts of its 64 bitmaps.
-// One warp per GT; any violation sets *bad.
+// One warp per GT; any violation sets bad[0]; bad[1] gets the largest
+// GT nonzero count.
 __global__ void validate_kernel(const uint64_t* __restrict__ bitmaps, const uint32_t* __restrict__ offsets,
                                 int64_t NGT, int* bad)
 {
@@ -267,6 +271,7 @@ __global__ void validate_kernel(const uint64_t* __restrict__ bitmaps, const uint
     if (lane == 0) {
         const uint32_t o0 = __ldg(offsets + t), o1 = __ldg(offsets + t + 1);
         if (o1 < o0 || o1 - o0 != c || (t == 0 && o0 != 0)) atomicExch(bad, 1);
+        atomicMax(bad + 1, (int)c);
     }
 }
 
@@ -283,33 +288,36 @@ bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s)
     int* overflow = nullptr;
     bsp_status_t st = BSP_OK;
     uint32_t total = 0;
-    int ovf = 0;
+    int ovf = 0, maxc = 0;
 
     if (cudaMalloc(&h->bitmaps, (size_t)h->NBT * 8) != cudaSuccess ||
         cudaMalloc(&h->offsets, (size_t)(h->NGT + 1) * 4) != cudaSuccess ||
         cudaMalloc(&bt_prefix, (size_t)h->NBT * 4) != cudaSuccess ||
         cudaMalloc(&gt_nnz, (size_t)h->NGT * 4) != cudaSuccess ||
-        cudaMalloc(&overflow, sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&overflow, 2 * sizeof(int)) != cudaSuccess) {  // overflow flag, largest GT count
         st = BSP_ERR_OOM;
         goto done;
     }
-    if (cudaMemsetAsync(overflow, 0, sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
+    if (cudaMemsetAsync(overflow, 0, 2 * sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
 
     if (eb == 2)
         enc_bitmap_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, (uint8_t*)h->bitmaps);
     else
         enc_bitmap_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, (uint8_t*)h->bitmaps);
-    enc_count_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->NGT, bt_prefix, gt_nnz);
+    enc_count_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->NGT, bt_prefix, gt_nnz,
+                                                                reinterpret_cast<unsigned int*>(overflow + 1));
     enc_scan_kernel<<<1, 1024, 0, s>>>(gt_nnz, h->NGT, h->offsets, overflow);
     if (cudaGetLastError() != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
     if (cudaMemcpyAsync(&total, h->offsets + h->NGT, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyAsync(&ovf, overflow, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&maxc, overflow + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         st = BSP_ERR_CUDA;
         goto done;
     }
     if (ovf) { st = BSP_ERR_SHAPE; goto done; }
     h->NNZ = total;
+    h->max_gt_nnz = (uint32_t)maxc;
     // values + at least 16 zeroed bytes of tail slack, so that 16-byte
     // vector loads of the last span never leave the allocation
     h->values_alloc = ((size_t)total * eb + 16 + 15) & ~(size_t)15;
@@ -343,23 +351,25 @@ bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
-bsp_status_t bsp_run_validate(const bsp_handle* h, cudaStream_t s)
+bsp_status_t bsp_run_validate(bsp_handle* h, cudaStream_t s)
 {
     int* bad = nullptr;
-    int hbad = 0;
+    int hbad = 0, maxc = 0;
     uint32_t last = 0;
     bsp_status_t st = BSP_OK;
-    if (cudaMalloc(&bad, sizeof(int)) != cudaSuccess) return BSP_ERR_OOM;
-    if (cudaMemsetAsync(bad, 0, sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
+    if (cudaMalloc(&bad, 2 * sizeof(int)) != cudaSuccess) return BSP_ERR_OOM;
+    if (cudaMemsetAsync(bad, 0, 2 * sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
     validate_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->offsets, h->NGT, bad);
     if (cudaGetLastError() != cudaSuccess ||
         cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&maxc, bad + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyAsync(&last, h->offsets + h->NGT, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         st = BSP_ERR_CUDA;
         goto done;
     }
     if (hbad || (uint64_t)last != h->NNZ) st = BSP_ERR_INVALID_ARG;
+    h->max_gt_nnz = (uint32_t)maxc;
 done:
     cudaFree(bad);
     return st;

@@ -221,14 +221,14 @@ struct Accum<NT, true, false> { int v[2][NT]; };
 #define BSP_DEC_OCT_UNROLL 2
 #endif
 
-template <int NT, bool I8, bool SKIP, typename A>
+template <int NT, bool I8, bool SKIP, int UNR = 0, typename A>
 __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t* base_s,
                                           const uint8_t* vals, const uint8_t* xraw, const float* x_s,
                                           int N, uint32_t act8, int lane, int bc0, A& acc)
 {
     using C = DecCfg<NT, I8>;
-    // octet loop unroll: the spMspV loop runs over active octets only
-    constexpr int OCT_UNROLL = SKIP ? 1 : (C::WIDE_X ? 4 : BSP_DEC_OCT_UNROLL);
+    // octet loop unroll (UNR if given): the spMspV loop runs over active octets only
+    constexpr int OCT_UNROLL = UNR ? UNR : (SKIP ? 1 : (C::WIDE_X ? 4 : BSP_DEC_OCT_UNROLL));
     const int rr = lane & 7;
     const int gb0 = bt_local(lane >> 3, 0), gb1 = bt_local((lane >> 3) + 4, 0);
     const uint32_t rsh = 8u * (uint32_t)(rr & 3);
@@ -698,6 +698,285 @@ spmm_decode_kernel(const Args a)
     if (threadIdx.x == 0) a.counters[gi] = 0u;
 }
 
+// ---------------------------------------------------------------------------
+// GT-per-warp kernel, fp16 N <= 2.
+//
+// One producer warp and CW consumer warps share one ring of S stages.
+// Consumer c decodes whole GroupTiles (i = c, c + CW, ...): lane l owns GT
+// rows l and l+32 over all eight K-octets, so the per-GT work that does not
+// scale with the positions (the wait, the BT popcount scan, the release)
+// is paid once per GT instead of once per GT and warp.  A stage holds the
+// bitmaps, a 16-byte header (the misalignment of the value span), the N
+// X rows of the GT column and the value span, sized for the largest GT of
+// the matrix (its nonzero count is recorded at encode / import time), so a
+// sparse matrix gets small stages and more of them fit on an SM.
+#ifndef BSP_GTW_CONSUMERS
+#define BSP_GTW_CONSUMERS 4
+#endif
+#ifndef BSP_GTW_STAGES
+#define BSP_GTW_STAGES 8
+#endif
+#ifndef BSP_GTW_MINB
+#define BSP_GTW_MINB 5
+#endif
+#ifndef BSP_GTW_OCT_UNROLL
+#define BSP_GTW_OCT_UNROLL 1
+#endif
+
+namespace gtw {
+constexpr int CW = BSP_GTW_CONSUMERS;  // consumer warps
+constexpr int S = BSP_GTW_STAGES;      // ring stages
+constexpr int THREADS = 32 * (1 + CW);
+constexpr int HDR = 16;                // stage header after the bitmaps
+constexpr uint32_t kSleepNs = 500;     // suspend hint of the waiting polls
+
+// bytes of one stage and offset of its value span, for N X rows and a GT
+// of at most max_nnz fp16 values
+inline void stage_geometry(int nt, uint32_t max_nnz, uint32_t& stage_bytes, uint32_t& val_off)
+{
+    val_off = 512 + HDR + (uint32_t)nt * 128;
+    const uint32_t chunks = (max_nnz * 2 + 15) / 16 + 1;  // + 1: misalignment of the span
+    stage_bytes = (val_off + chunks * 16 + 127) & ~127u;
+}
+inline size_t smem_bytes(uint32_t stage_bytes) { return (size_t)S * stage_bytes + CW * 256 + 2 * S * 8; }
+}  // namespace gtw
+
+struct GtwArgs {
+    const uint64_t* bitmaps;
+    const uint32_t* offsets;
+    const uint8_t* values;
+    const uint8_t* X;
+    int N;
+    int64_t M, K;
+    int splits, per_split;
+    float* ws;
+    uint32_t* counters;
+    int* err;
+    __half* Y;
+    uint32_t spin_cap;
+    uint32_t stage_bytes, val_off;
+    int stall_first;  // test only: skip the copies of the first GT
+};
+
+template <int NT>
+__global__ void __launch_bounds__(gtw::THREADS, BSP_GTW_MINB)
+spmm_decode_gtw_kernel(const GtwArgs a)
+{
+    using namespace gtw;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_last;
+    constexpr uint32_t FULL = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t SB = a.stage_bytes;
+    uint32_t* bases = reinterpret_cast<uint32_t*>(smem + S * SB);             // [CW][64]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + CW * 256);   // [S]
+    uint64_t* empty = full + S;                                                // [S]
+
+    const int64_t K = a.K, M = a.M, KT = K >> 6;
+    const int64_t gi = blockIdx.y;
+    const int64_t k_begin = (int64_t)blockIdx.x * a.per_split;
+    const int cnt = (int)max((int64_t)0, min((int64_t)a.per_split, KT - k_begin));
+    const int64_t t0 = gi * KT + k_begin;
+    const int N = a.N;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            bspx::mbar_init(full + s, 1);
+            bspx::mbar_init(empty + s, 1);
+        }
+        bspx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    bool failed = false;
+    Accum<NT, false, false> acc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int n = 0; n < 2 * NT; ++n) acc.v[h][n] = 0.f;
+
+    if (warp == 0) {
+        // ---- producer: GT i into stage i % S once its previous GT is released
+        uint32_t offv = 0;
+        int wbase = 0;
+        uint32_t s = 0, ph = 0;
+        int i = 0;  // GTs issued
+        for (; i < cnt; ++i) {
+            if (i >= S && !__all_sync(FULL, bspx::mbar_wait_sleep(empty + s, ph ^ 1u, a.spin_cap, kSleepNs))) {
+                failed = true;
+                break;
+            }
+            if (i == 0 || i - wbase >= 31) {  // window: lane j holds offsets[t0 + wbase + j]
+                wbase = i;
+                const int j = wbase + lane;
+                offv = (j <= cnt) ? __ldg(a.offsets + t0 + j) : 0u;
+            }
+            const uint32_t o0 = __shfl_sync(FULL, offv, i - wbase), o1 = __shfl_sync(FULL, offv, i - wbase + 1);
+            if (lane == 0 && !(a.stall_first && i == 0)) {
+                uint8_t* st = smem + s * SB;
+                const uint32_t ch0 = o0 / 8, nch = (o1 + 7) / 8 - ch0;
+                *reinterpret_cast<uint32_t*>(st + 512) = o0 - ch0 * 8;
+                bspx::mbar_arrive_expect_tx(full + s, 512u + (uint32_t)N * 128u + nch * 16u);
+                bspx::bulk_g2s(st, a.bitmaps + (t0 + i) * 64, 512, full + s);
+                for (int n = 0; n < N; ++n)
+                    bspx::bulk_g2s(st + 512 + HDR + n * 128, a.X + ((int64_t)n * K + (k_begin + i) * 64) * 2, 128,
+                                   full + s);
+                if (nch) bspx::bulk_g2s(st + a.val_off, a.values + (int64_t)ch0 * 16, nch * 16, full + s);
+            }
+            if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
+        }
+        // let the copies still in flight land before the stages are reused (bounded)
+        for (int k = (i > S ? i - S : 0); k < i; ++k)
+            bspx::mbar_wait_bounded(full + (k % S), (uint32_t)((k / S) & 1), a.spin_cap);
+    } else {
+        // ---- consumers
+        const int cw = warp - 1;
+        uint32_t* base_s = bases + cw * 64;
+        for (int i = cw; i < cnt; i += CW) {
+            const int s = i % S;
+            if (!__all_sync(FULL, bspx::mbar_wait_sleep(full + s, (uint32_t)((i / S) & 1), a.spin_cap, kSleepNs))) {
+                failed = true;
+                break;
+            }
+            const uint8_t* st = smem + s * SB;
+            const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st);
+            const uint32_t shift = *reinterpret_cast<const uint32_t*>(st + 512);
+            // BT value bases: popcounts and a warp exclusive scan
+            const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(bm_st)[lane];
+            const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
+            uint32_t incl = c0 + c1;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t o = __shfl_up_sync(FULL, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const uint32_t ex = incl - (c0 + c1) + shift;
+            base_s[2 * lane] = ex;
+            base_s[2 * lane + 1] = ex + c0;
+            __syncwarp();
+            const uint8_t* xraw = st + 512 + HDR;
+            decode_gt<NT, false, false, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, 0xFFu,
+                                                            lane, 0, acc);
+            decode_gt<NT, false, false, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, 0xFFu,
+                                                            lane, 4, acc);
+            __syncwarp();
+            if (lane == 0) bspx::mbar_arrive(empty + s);
+        }
+    }
+    if (failed && lane == 0) atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
+
+    // ---- CTA reduction over the consumers (the buffer aliases the ring)
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(smem);  // [CW][64][NT]
+    if (warp > 0) {
+        const int cw = warp - 1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                red[(cw * 64 + lane + 32 * h) * NT + n] = acc.v[h][n] + acc.v[h][n + NT];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * NT; i += THREADS) {
+        const int r = i / NT, n = i % NT;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < CW; ++c) sum += red[c * 64 * NT + i];
+        if (n < N) {
+            const int64_t m = gi * 64 + r;
+            if (a.splits == 1)
+                a.Y[(int64_t)n * M + m] = __float2half_rn(sum);
+            else
+                atomicAdd(a.ws + (int64_t)n * M + m, sum);
+        }
+    }
+    if (a.splits == 1) return;
+
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(a.counters + gi, 1u) == (uint32_t)(a.splits - 1));
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < 64 * N; i += THREADS) {
+        const int n = i >> 6, r = i & 63;
+        const int64_t m = gi * 64 + r;
+        a.Y[(int64_t)n * M + m] = __float2half_rn(ws_take(a.ws + (int64_t)n * M + m));
+    }
+    if (threadIdx.x == 0) a.counters[gi] = 0u;
+}
+
+// Split of the GT columns for the GT-per-warp kernel: the split whose
+// number of CTA waves times GTs per CTA is smallest (ties: fewer CTAs),
+// with at least 2 CW GTs per CTA when the row strip has that many.
+int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
+{
+    if (const char* e = std::getenv("BSP_SPLITK")) {
+        const int64_t v = std::atol(e);
+        if (v >= 1) return (int)std::min<int64_t>(v, KT);
+    }
+    int64_t best = 1, best_cost = INT64_MAX;
+    for (int64_t sp = 1; sp <= KT; ++sp) {
+        const int64_t per = (KT + sp - 1) / sp;
+        if (per < 2 * gtw::CW && sp > 1) break;
+        const int64_t real = (KT + per - 1) / per;
+        const int64_t ctas = strips * real;
+        const int64_t cost = ((ctas + slots - 1) / slots) * per;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = real;
+        }
+    }
+    return (int)best;
+}
+
+template <int NT>
+bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void* Y, cudaStream_t s)
+{
+    using namespace gtw;
+    static bool attr_done[64] = {};
+    if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
+    uint32_t stage_bytes = 0, val_off = 0;
+    stage_geometry(NT, 4096, stage_bytes, val_off);
+    const size_t smem_max = smem_bytes(stage_bytes);
+    if (!attr_done[p.device]) {
+        if (cudaFuncSetAttribute(spmm_decode_gtw_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_max) != cudaSuccess)
+            return BSP_ERR_CUDA;
+        attr_done[p.device] = true;
+    }
+    stage_geometry(NT, std::min<uint32_t>(p.max_gt_nnz, 4096u), stage_bytes, val_off);
+    const size_t smem = smem_bytes(stage_bytes);
+    const int64_t strips = p.M / 64, KT = p.K / 64;
+    int per_sm = (int)std::min<size_t>((size_t)BSP_GTW_MINB, (size_t)(227 * 1024) / (smem + 1024));
+    if (per_sm < 1) per_sm = 1;
+    const int splits0 = gtw_splits(strips, KT, (int64_t)p.num_sms * per_sm);
+    const int per_split = (int)((KT + splits0 - 1) / splits0);
+    const int splits = (int)((KT + per_split - 1) / per_split);
+    GtwArgs a;
+    a.bitmaps = p.bitmaps;
+    a.offsets = p.offsets;
+    a.values = (const uint8_t*)p.values;
+    a.X = (const uint8_t*)X;
+    a.N = N;
+    a.M = p.M;
+    a.K = p.K;
+    a.splits = splits;
+    a.per_split = per_split;
+    a.ws = (float*)p.ws;
+    a.counters = p.counters;
+    a.err = p.err;
+    a.Y = (__half*)Y;
+    a.spin_cap = bspx::kSpinCap;
+    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    a.stage_bytes = stage_bytes;
+    a.val_off = val_off;
+    a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    dim3 grid((unsigned)splits, (unsigned)strips);
+    spmm_decode_gtw_kernel<NT><<<grid, THREADS, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 template <int NT, bool I8, bool SKIP>
 bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, int mode,
                     const float* row_scale, float tau, cudaStream_t s)
@@ -786,6 +1065,11 @@ bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int
     if (skip_zero_octets && N != 1) return BSP_ERR_INVALID_ARG;
     if (!(tau >= 0.f)) return BSP_ERR_INVALID_ARG;  // also rejects NaN
     const bool i8 = p.dtype == BSP_INT8;
+#ifndef BSP_DEC_GTW
+#define BSP_DEC_GTW 1
+#endif
+    if (BSP_DEC_GTW && !i8 && !skip_zero_octets && mode == BSP_OUT_F16 && N <= 2)
+        return N == 1 ? launch_gtw<1>(p, X, N, Y, s) : launch_gtw<2>(p, X, N, Y, s);
     if (i8)
         return skip_zero_octets ? dispatch_nt<true, true>(p, X, N, Y, mode, row_scale, tau, s)
                                 : dispatch_nt<true, false>(p, X, N, Y, mode, row_scale, tau, s);
@@ -802,6 +1086,7 @@ bsp_decode_problem bsp_problem_of(const bsp_handle* h)
     p.dtype = h->dtype;
     p.M = h->M;
     p.K = h->K;
+    p.max_gt_nnz = h->max_gt_nnz;
     p.device = h->device;
     p.num_sms = h->num_sms;
     p.ws = h->ws;
