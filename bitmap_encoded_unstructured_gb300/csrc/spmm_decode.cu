@@ -726,6 +726,11 @@ spmm_decode_kernel(const Args a)
 namespace gtw {
 constexpr int CW = BSP_GTW_CONSUMERS;  // consumer warps
 constexpr int S = BSP_GTW_STAGES;      // ring stages
+// GT i goes to consumer i % CW and stage i % S.  With S a multiple of CW
+// every stage has one consumer, which has seen the previous GT of its
+// stage land before it waits for the next one: a parity wait can then
+// never be two phases behind (and mistake an old phase for the new one).
+static_assert(S % CW == 0 && S >= 2 * CW, "stages: a multiple of the consumers, two per consumer at least");
 constexpr int THREADS = 32 * (1 + CW);
 constexpr int HDR = 16;                // stage header after the bitmaps
 constexpr uint32_t kSleepNs = 500;     // suspend hint of the waiting polls
