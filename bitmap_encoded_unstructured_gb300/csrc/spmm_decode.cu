@@ -198,6 +198,27 @@ __device__ __forceinline__ void pos_f16x2(float& acc0, float& acc1, uint32_t& ad
         : "r"(byte), "r"(bit), "h"(x0), "h"(x1));
 }
 
+// One column c of a row-byte in the spMspV loop: if byte & bit (bit =
+// 1 << c), load the value at rank popcount(byte & below) (below = bit - 1)
+// after the row-byte's first value (byte address `base`) and accumulate
+// w * x with one rounding; no branch.
+__device__ __forceinline__ void col_f16(float& acc, uint32_t base, uint32_t byte, uint32_t bit, uint32_t below,
+                                        uint16_t x)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 t, r, a;\n\t.reg .b16 w;\n\t"
+        "and.b32 t, %2, %3;\n\t"
+        "setp.ne.b32 p, t, 0;\n\t"
+        "and.b32 r, %2, %4;\n\t"
+        "popc.b32 r, r;\n\t"
+        "shl.b32 r, r, 1;\n\t"
+        "add.u32 a, %1, r;\n\t"
+        "@p ld.shared.u16 w, [a];\n\t"
+        "@p fma.rn.f32.f16 %0, w, %5, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(base), "r"(byte), "r"(bit), "r"(below), "h"(x));
+}
+
 // Accumulator storage of one lane: rows l and l+32, NT columns of Y.
 template <int NT, bool I8, bool WIDE>
 struct Accum;
@@ -224,7 +245,8 @@ struct Accum<NT, true, false> { int v[2][NT]; };
 template <int NT, bool I8, bool SKIP, int UNR = 0, typename A>
 __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t* base_s,
                                           const uint8_t* vals, const uint8_t* xraw, const float* x_s,
-                                          int N, uint32_t act8, int lane, int bc0, A& acc)
+                                          int N, uint32_t act8, int lane, int bc0, A& acc,
+                                          uint64_t cols = ~0ull)
 {
     using C = DecCfg<NT, I8>;
     // octet loop unroll (UNR if given): the spMspV loop runs over active octets only
@@ -281,6 +303,25 @@ __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t*
                     acc.v[h][n] = __dp4a((int)wlo, (int)xlo[n], acc.v[h][n]);
                     acc.v[h][n] = __dp4a((int)whi, (int)xhi[n], acc.v[h][n]);
                 }
+            }
+        } else if constexpr (SKIP) {
+            // fp16 spMspV (N = 1): only the columns whose activation is not
+            // pruned (bit c of the octet's mask, the same for every lane: a
+            // warp-uniform loop).  The value of position c is found by the
+            // masked popcount of the row-byte below c, without walking the
+            // other positions.
+            const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(xraw);
+            uint32_t m = (uint32_t)(cols >> (8 * bc)) & 0xFFu;
+            uint32_t vb[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) vb[h] = bspx::smem_u32(vals) + 2u * idx[h];
+            while (m) {
+                const int c = __ffs(m) - 1;
+                m &= m - 1u;
+                const uint16_t xc = xs16[8 * bc + c];
+                const uint32_t bit = 1u << c;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) col_f16(acc.v[h][0], vb[h], byte[h], bit, bit - 1u, xc);
             }
         } else if constexpr (!C::WIDE_X) {
             // N <= 2: fp16 X octet in registers, mixed-precision FMA; two
@@ -743,7 +784,20 @@ inline void stage_geometry(int nt, uint32_t max_nnz, uint32_t& stage_bytes, uint
     const uint32_t chunks = (max_nnz * 2 + 15) / 16 + 1;  // + 1: misalignment of the span
     stage_bytes = (val_off + chunks * 16 + 127) & ~127u;
 }
-inline size_t smem_bytes(uint32_t stage_bytes) { return (size_t)S * stage_bytes + CW * 256 + 2 * S * 8; }
+inline size_t smem_bytes(uint32_t stage_bytes) { return (size_t)S * stage_bytes + CW * 256 + 3 * S * 8; }
+// spMspV: a GT beyond the first S (which start the ring at once) with at
+// most BSP_GTW_SELMAX active K-octets is fetched selectively (metadata
+// first, then only the value segments of its active octets).  The second
+// round trip costs more than it saves unless most of the values can be
+// left behind: with 85%-zero activations (3 in 4 octets active) fetching
+// whole GTs is faster, so the default asks for 6 of 8 octets inactive.
+#ifndef BSP_GTW_SELMAX
+#define BSP_GTW_SELMAX 2
+#endif
+__device__ __forceinline__ bool gtw_selective(int i, uint32_t act8)
+{
+    return i >= S && __popc(act8) <= BSP_GTW_SELMAX;
+}
 }  // namespace gtw
 
 struct GtwArgs {
@@ -761,9 +815,10 @@ struct GtwArgs {
     uint32_t spin_cap;
     uint32_t stage_bytes, val_off;
     int stall_first;  // test only: skip the copies of the first GT
+    float tau;        // spMspV pruning threshold: |x| <= tau counts as zero
 };
 
-template <int NT>
+template <int NT, bool SKIP>
 __global__ void __launch_bounds__(gtw::THREADS, BSP_GTW_MINB)
 spmm_decode_gtw_kernel(const GtwArgs a)
 {
@@ -776,6 +831,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
     uint32_t* bases = reinterpret_cast<uint32_t*>(smem + S * SB);             // [CW][64]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + CW * 256);   // [S]
     uint64_t* empty = full + S;                                                // [S]
+    uint64_t* full_v = full + 2 * S;                                           // [S] spMspV values
 
     const int64_t K = a.K, M = a.M, KT = K >> 6;
     const int64_t gi = blockIdx.y;
@@ -788,6 +844,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
         for (int s = 0; s < S; ++s) {
             bspx::mbar_init(full + s, 1);
             bspx::mbar_init(empty + s, 1);
+            bspx::mbar_init(full_v + s, 1);
         }
         bspx::fence_mbar_init();
     }
@@ -800,7 +857,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
 #pragma unroll
         for (int n = 0; n < 2 * NT; ++n) acc.v[h][n] = 0.f;
 
-    if (warp == 0) {
+    if (warp == 0 && !SKIP) {
         // ---- producer: GT i into stage i % S once its previous GT is released
         uint32_t offv = 0;
         int wbase = 0;
@@ -833,10 +890,150 @@ spmm_decode_gtw_kernel(const GtwArgs a)
         // let the copies still in flight land before the stages are reused (bounded)
         for (int k = (i > S ? i - S : 0); k < i; ++k)
             bspx::mbar_wait_bounded(full + (k % S), (uint32_t)((k / S) & 1), a.spin_cap);
+    } else if (warp == 0) {
+        // ---- spMspV producer ("metadata first"): a GT with an inactive K-octet
+        // (beyond the first S, which start the ring) is fetched in two steps:
+        // bitmaps + x, then, once those are in, only the value segments of
+        // its active octets.  The producer never blocks on one GT: each pass
+        // issues the values of the oldest selective GT whose metadata has
+        // landed and the metadata of the next GT whose stage is free, and
+        // naps when neither is ready.
+        uint32_t offv = 0, actv = 0;
+        int wbase = -64, awbase = -64;  // offsets / activity windows: lane j holds GT base + j
+        uint32_t selmask = 0;           // bit k % 32: GT k is selective
+        uint32_t vpend = 0, vpar = 0;   // stages with value copies in flight, their parities
+        int next = 0, vnext = 0;        // next GT to issue, oldest GT whose values may be pending
+        uint32_t idle = 0;
+        // value segments of selective GT p (its metadata has landed).  In
+        // GT order the BT pair (2l, 2l+1) is the segment (TCTile row l/8,
+        // octet l%8); runs of adjacent active segments go as one copy,
+        // issued by the run's first lane.
+        auto issue_values = [&](int p) {
+            const int sp = p % S;
+            uint8_t* st = smem + sp * SB;
+            const uint32_t* hdr = reinterpret_cast<const uint32_t*>(st + 512);
+            const uint32_t shift = hdr[0], ch0 = hdr[1], a8 = hdr[2];
+            const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(st)[lane];
+            const uint32_t seg = __popcll(bb.x) + __popcll(bb.y);
+            uint32_t incl = seg;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t o = __shfl_up_sync(FULL, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const uint32_t ex = incl - seg;
+            const bool act = (a8 >> (lane & 7)) & 1u;
+            const uint32_t q0 = (ex + shift) / 8, q1 = (ex + seg + shift + 7) / 8;
+            const uint32_t A = __ballot_sync(FULL, act);
+            const bool first = act && !(lane > 0 && ((A >> (lane - 1)) & 1u));
+            const uint32_t above = lane == 31 ? 0u : (~A & (~0u << (lane + 1)));  // inactive lanes above
+            const int e = above ? __ffs(above) - 2 : 31;                          // last lane of the run
+            const uint32_t q1e = __shfl_sync(FULL, q1, e);
+            uint32_t bytes = (first && q1e > q0) ? (q1e - q0) * 16 : 0u;
+            const uint32_t mine = bytes;
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) bytes += __shfl_xor_sync(FULL, bytes, d);
+            if (lane == 0) bspx::mbar_arrive_expect_tx(full_v + sp, bytes);
+            __syncwarp();
+            if (mine)
+                bspx::bulk_g2s(st + a.val_off + q0 * 16, a.values + ((int64_t)ch0 + q0) * 16, mine, full_v + sp);
+            vpend |= 1u << sp;
+        };
+        while (next < cnt || vnext < next) {
+            bool prog = false;
+            while (vnext < next && !((selmask >> (vnext & 31)) & 1u)) ++vnext;
+            if (vnext < next) {
+                const uint32_t landed =
+                    lane == 0 ? (uint32_t)bspx::mbar_try_wait(full + vnext % S, (uint32_t)((vnext / S) & 1)) : 0u;
+                if (__shfl_sync(FULL, landed, 0)) {
+                    issue_values(vnext);
+                    ++vnext;
+                    prog = true;
+                }
+            }
+            if (next < cnt) {
+                const int sn = next % S;
+                uint32_t free = next < S ? 1u : 0u;
+                if (!free && lane == 0)
+                    free = (uint32_t)bspx::mbar_try_wait(empty + sn, (uint32_t)(((next / S) & 1) ^ 1));
+                if (__shfl_sync(FULL, free, 0)) {
+                    if (vpend & (1u << sn)) {  // the stage's previous selective GT was consumed
+                        vpend &= ~(1u << sn);
+                        vpar ^= 1u << sn;
+                    }
+                    if (next - wbase >= 31) {
+                        wbase = next;
+                        const int j = wbase + lane;
+                        offv = (j <= cnt) ? __ldg(a.offsets + t0 + j) : 0u;
+                    }
+                    const uint32_t o0 = __shfl_sync(FULL, offv, next - wbase);
+                    const uint32_t o1 = __shfl_sync(FULL, offv, next - wbase + 1);
+                    uint32_t a8 = 0xFFu;
+                    if (next >= S) {
+                        if (next - awbase >= 32) {
+                            // lane j: K-octet activity of GT awbase + j, from x (one octet per 16-B load)
+                            awbase = next;
+                            const int j = awbase + lane;
+                            uint32_t act = 0xFFu;
+                            if (j < cnt) {
+                                act = 0;
+                                const uint4* xp = reinterpret_cast<const uint4*>(a.X + (k_begin + j) * 64 * 2);
+#pragma unroll
+                                for (int o = 0; o < 8; ++o) {
+                                    const uint4 q = __ldg(xp + o);
+                                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                                    bool nz = false;
+#pragma unroll
+                                    for (int e2 = 0; e2 < 4; ++e2) {
+                                        const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e2]);
+                                        nz |= active(__low2float(h2), a.tau) || active(__high2float(h2), a.tau);
+                                    }
+                                    act |= (nz ? 1u : 0u) << o;
+                                }
+                            }
+                            actv = act;
+                        }
+                        a8 = __shfl_sync(FULL, actv, next - awbase);
+                    }
+                    const bool sel = gtw_selective(next, a8);
+                    if (sel) selmask |= 1u << (next & 31);
+                    else selmask &= ~(1u << (next & 31));
+                    if (lane == 0 && !(a.stall_first && next == 0)) {
+                        uint8_t* st = smem + sn * SB;
+                        const uint32_t ch0 = o0 / 8, nch = sel ? 0u : (o1 + 7) / 8 - ch0;
+                        uint32_t* hdr = reinterpret_cast<uint32_t*>(st + 512);
+                        hdr[0] = o0 - ch0 * 8;
+                        hdr[1] = ch0;
+                        hdr[2] = a8;
+                        bspx::mbar_arrive_expect_tx(full + sn, 512u + 128u + nch * 16u);
+                        bspx::bulk_g2s(st, a.bitmaps + (t0 + next) * 64, 512, full + sn);
+                        bspx::bulk_g2s(st + 512 + HDR, a.X + (k_begin + next) * 64 * 2, 128, full + sn);
+                        if (nch) bspx::bulk_g2s(st + a.val_off, a.values + (int64_t)ch0 * 16, nch * 16, full + sn);
+                    }
+                    ++next;
+                    prog = true;
+                }
+            }
+            if (prog) {
+                idle = 0;
+            } else {
+                if (++idle > a.spin_cap) {
+                    failed = true;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        // let the copies still in flight land before the stages are reused (bounded)
+        for (int k = (next > S ? next - S : 0); k < next; ++k)
+            bspx::mbar_wait_bounded(full + (k % S), (uint32_t)((k / S) & 1), a.spin_cap);
+        for (int t = 0; t < S; ++t)
+            if ((vpend >> t) & 1u) bspx::mbar_wait_bounded(full_v + t, (vpar >> t) & 1u, a.spin_cap);
     } else {
         // ---- consumers
         const int cw = warp - 1;
         uint32_t* base_s = bases + cw * 64;
+        uint32_t vpar = 0;  // spMspV: parity of the next full_v wait, bit per stage
         for (int i = cw; i < cnt; i += CW) {
             const int s = i % S;
             if (!__all_sync(FULL, bspx::mbar_wait_sleep(full + s, (uint32_t)((i / S) & 1), a.spin_cap, kSleepNs))) {
@@ -846,6 +1043,27 @@ spmm_decode_gtw_kernel(const GtwArgs a)
             const uint8_t* st = smem + s * SB;
             const uint64_t* bm_st = reinterpret_cast<const uint64_t*>(st);
             const uint32_t shift = *reinterpret_cast<const uint32_t*>(st + 512);
+            const uint8_t* xraw = st + 512 + HDR;
+            uint32_t act8 = 0xFFu;
+            uint64_t cols = ~0ull;
+            if constexpr (SKIP) {
+                // column c is active iff x[c] is not pruned; K-octet j iff
+                // one of its columns is
+                const __half* xh = reinterpret_cast<const __half*>(xraw);
+                const uint32_t m_lo = __ballot_sync(FULL, active(__half2float(xh[lane]), a.tau));
+                const uint32_t m_hi = __ballot_sync(FULL, active(__half2float(xh[lane + 32]), a.tau));
+                cols = (uint64_t)m_lo | ((uint64_t)m_hi << 32);
+                act8 = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) act8 |= (((cols >> (8 * j)) & 0xFFull) ? 1u : 0u) << j;
+                if (gtw_selective(i, act8)) {  // selective GT: its values come on full_v[s]
+                    if (!__all_sync(FULL, bspx::mbar_wait_sleep(full_v + s, (vpar >> s) & 1u, a.spin_cap, kSleepNs))) {
+                        failed = true;
+                        break;
+                    }
+                    vpar ^= 1u << s;
+                }
+            }
             // BT value bases: popcounts and a warp exclusive scan
             const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(bm_st)[lane];
             const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
@@ -859,11 +1077,10 @@ spmm_decode_gtw_kernel(const GtwArgs a)
             base_s[2 * lane] = ex;
             base_s[2 * lane + 1] = ex + c0;
             __syncwarp();
-            const uint8_t* xraw = st + 512 + HDR;
-            decode_gt<NT, false, false, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, 0xFFu,
-                                                            lane, 0, acc);
-            decode_gt<NT, false, false, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, 0xFFu,
-                                                            lane, 4, acc);
+            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
+                                                           lane, 0, acc, cols);
+            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
+                                                           lane, 4, acc, cols);
             __syncwarp();
             if (lane == 0) bspx::mbar_arrive(empty + s);
         }
@@ -912,7 +1129,8 @@ spmm_decode_gtw_kernel(const GtwArgs a)
 }
 
 // Split of the GT columns for the GT-per-warp kernel: the split whose
-// number of CTA waves times GTs per CTA is smallest (ties: fewer CTAs),
+// number of CTA waves times (GTs per CTA + a fixed 4) is smallest (ties:
+// fewer CTAs),
 // with at least 2 CW GTs per CTA when the row strip has that many.
 int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
 {
@@ -926,7 +1144,8 @@ int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
         if (per < 2 * gtw::CW && sp > 1) break;
         const int64_t real = (KT + per - 1) / per;
         const int64_t ctas = strips * real;
-        const int64_t cost = ((ctas + slots - 1) / slots) * per;
+        // a CTA's start (first copies) and end (reduction) cost about 4 GTs
+        const int64_t cost = ((ctas + slots - 1) / slots) * (per + 4);
         if (cost < best_cost) {
             best_cost = cost;
             best = real;
@@ -935,8 +1154,8 @@ int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
     return (int)best;
 }
 
-template <int NT>
-bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void* Y, cudaStream_t s)
+template <int NT, bool SKIP>
+bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void* Y, float tau, cudaStream_t s)
 {
     using namespace gtw;
     static bool attr_done[64] = {};
@@ -945,7 +1164,7 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     stage_geometry(NT, 4096, stage_bytes, val_off);
     const size_t smem_max = smem_bytes(stage_bytes);
     if (!attr_done[p.device]) {
-        if (cudaFuncSetAttribute(spmm_decode_gtw_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(spmm_decode_gtw_kernel<NT, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_max) != cudaSuccess)
             return BSP_ERR_CUDA;
         attr_done[p.device] = true;
@@ -977,8 +1196,9 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     a.stage_bytes = stage_bytes;
     a.val_off = val_off;
     a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    a.tau = tau;
     dim3 grid((unsigned)splits, (unsigned)strips);
-    spmm_decode_gtw_kernel<NT><<<grid, THREADS, smem, s>>>(a);
+    spmm_decode_gtw_kernel<NT, SKIP><<<grid, THREADS, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
@@ -1073,8 +1293,10 @@ bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int
 #ifndef BSP_DEC_GTW
 #define BSP_DEC_GTW 1
 #endif
-    if (BSP_DEC_GTW && !i8 && !skip_zero_octets && mode == BSP_OUT_F16 && N <= 2)
-        return N == 1 ? launch_gtw<1>(p, X, N, Y, s) : launch_gtw<2>(p, X, N, Y, s);
+    if (BSP_DEC_GTW && !i8 && mode == BSP_OUT_F16 && N <= 2) {
+        if (skip_zero_octets) return launch_gtw<1, true>(p, X, N, Y, tau, s);
+        return N == 1 ? launch_gtw<1, false>(p, X, N, Y, tau, s) : launch_gtw<2, false>(p, X, N, Y, tau, s);
+    }
     if (i8)
         return skip_zero_octets ? dispatch_nt<true, true>(p, X, N, Y, mode, row_scale, tau, s)
                                 : dispatch_nt<true, false>(p, X, N, Y, mode, row_scale, tau, s);
