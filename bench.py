@@ -434,7 +434,8 @@ def run_gpu(args):
                 "data": "synthetic (seeded numpy: N(0,0.02) weights, magnitude 50% mask, N(0,1) X)",
                 "config": _config(), "frac_hbm": round(value / ws / peak, 4),
                 "breakdown": breakdown, "prefill": prefill,
-                "roofline": {"bound": "hbm", "kernel": "spmm_decode_kernel",
+                "roofline": {"bound": "hbm",
+                             "kernel": "spmm_decode_gtw_kernel (fp16 N<=2, spMspV) + spmm_decode_kernel (N>=4)",
                              "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                              "unit": "GB/s", "frac": round(achieved / peak, 4),
                              "algorithmic_bytes_per_launch": round(step_bytes / n_calls),
