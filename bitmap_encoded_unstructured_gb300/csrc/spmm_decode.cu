@@ -47,6 +47,7 @@
 // and returns.
 #include "bsp_internal.cuh"
 #include "bsp_ptx.cuh"
+#include "bsp_bits.cuh"
 
 #include <cstdlib>
 #include <type_traits>
@@ -169,10 +170,20 @@ __device__ __forceinline__ uint16_t half_of(const uint4& q, int c)
 // byte & bit, load the next packed fp16 value from shared memory (byte
 // address `addr`), advance `addr` and accumulate w * x into `acc` with one
 // rounding (fma.rn.f32.f16: the fp16 product is exact in fp32).
+#ifndef BSP_POS_ASM_VOLATILE
+#define BSP_POS_ASM_VOLATILE 1
+#endif
+#if BSP_POS_ASM_VOLATILE
+#define BSP_POS_ASM asm volatile
+#else
+// not volatile: the inputs of a step (address, bitmap byte) come from shared-memory loads made after the
+// stage's barrier wait, so the compiler cannot move a step above it, and may interleave independent steps
+#define BSP_POS_ASM asm
+#endif
 __device__ __forceinline__ void pos_f16(float& acc, uint32_t& addr, uint32_t byte, uint32_t bit,
                                         uint16_t x)
 {
-    asm volatile(
+    BSP_POS_ASM(
         "{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t.reg .b16 w;\n\t"
         "and.b32 t, %2, %3;\n\t"
         "setp.ne.b32 p, t, 0;\n\t"
@@ -186,7 +197,7 @@ __device__ __forceinline__ void pos_f16(float& acc, uint32_t& addr, uint32_t byt
 __device__ __forceinline__ void pos_f16x2(float& acc0, float& acc1, uint32_t& addr, uint32_t byte,
                                           uint32_t bit, uint16_t x0, uint16_t x1)
 {
-    asm volatile(
+    BSP_POS_ASM(
         "{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t.reg .b16 w;\n\t"
         "and.b32 t, %3, %4;\n\t"
         "setp.ne.b32 p, t, 0;\n\t"
@@ -242,7 +253,9 @@ struct Accum<NT, true, false> { int v[2][NT]; };
 #define BSP_DEC_OCT_UNROLL 2
 #endif
 
-template <int NT, bool I8, bool SKIP, int UNR = 0, typename A>
+// RS: base_s is a table of row starts, u16 [64 BT][8 rows] (absolute value
+// indices in the stage), instead of the 64 BT bases.
+template <int NT, bool I8, bool SKIP, int UNR = 0, bool RS = false, typename A>
 __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t* base_s,
                                           const uint8_t* vals, const uint8_t* xraw, const float* x_s,
                                           int N, uint32_t act8, int lane, int bc0, A& acc,
@@ -270,11 +283,16 @@ __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t*
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int gl = (h ? gb1 : gb0) + bt_local(0, bc);
-            const uint2 bm = *reinterpret_cast<const uint2*>(bm_st + gl);
-            const uint32_t w32 = hi ? bm.y : bm.x;
-            byte[h] = (w32 >> rsh) & 0xFFu;
-            // nonzeros of the earlier rows of the BT: masked popcount
-            idx[h] = base_s[gl] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
+            if constexpr (RS) {
+                byte[h] = reinterpret_cast<const uint8_t*>(bm_st)[8 * gl + rr];
+                idx[h] = reinterpret_cast<const uint16_t*>(base_s)[8 * gl + rr];
+            } else {
+                const uint2 bm = *reinterpret_cast<const uint2*>(bm_st + gl);
+                const uint32_t w32 = hi ? bm.y : bm.x;
+                byte[h] = (w32 >> rsh) & 0xFFu;
+                // nonzeros of the earlier rows of the BT: masked popcount
+                idx[h] = base_s[gl] + (uint32_t)__popc(w32 & lowm) + (hi ? (uint32_t)__popc(bm.x) : 0u);
+            }
         }
         if constexpr (I8) {
             // dense int8 row-byte packed into two words, then dp4a per column of Y
@@ -752,16 +770,25 @@ spmm_decode_kernel(const Args a)
 // the matrix (its nonzero count is recorded at encode / import time), so a
 // sparse matrix gets small stages and more of them fit on an SM.
 #ifndef BSP_GTW_CONSUMERS
-#define BSP_GTW_CONSUMERS 4
+#define BSP_GTW_CONSUMERS 2
 #endif
 #ifndef BSP_GTW_STAGES
-#define BSP_GTW_STAGES 8
+#define BSP_GTW_STAGES 4
 #endif
 #ifndef BSP_GTW_MINB
-#define BSP_GTW_MINB 5
+#define BSP_GTW_MINB 8
 #endif
 #ifndef BSP_GTW_OCT_UNROLL
 #define BSP_GTW_OCT_UNROLL 1
+#endif
+// consumers: a row-start table per GT (1) or BT bases + masked popcounts per
+// row-byte (0).  The table pays where few positions are decoded (spMspV);
+// for the plain product its cost exceeds the saving (measured).
+#ifndef BSP_GTW_RS_SPMM
+#define BSP_GTW_RS_SPMM 0
+#endif
+#ifndef BSP_GTW_RS_SKIP
+#define BSP_GTW_RS_SKIP 1
 #endif
 
 namespace gtw {
@@ -784,7 +811,8 @@ inline void stage_geometry(int nt, uint32_t max_nnz, uint32_t& stage_bytes, uint
     const uint32_t chunks = (max_nnz * 2 + 15) / 16 + 1;  // + 1: misalignment of the span
     stage_bytes = (val_off + chunks * 16 + 127) & ~127u;
 }
-inline size_t smem_bytes(uint32_t stage_bytes) { return (size_t)S * stage_bytes + CW * 256 + 3 * S * 8; }
+constexpr int AREA = 1024;  // per consumer: row starts u16 [64][8], or BT bases u32 [64]
+inline size_t smem_bytes(uint32_t stage_bytes) { return (size_t)S * stage_bytes + CW * AREA + 3 * S * 8; }
 // spMspV: a GT beyond the first S (which start the ring at once) with at
 // most BSP_GTW_SELMAX active K-octets is fetched selectively (metadata
 // first, then only the value segments of its active octets).  The second
@@ -823,13 +851,14 @@ __global__ void __launch_bounds__(gtw::THREADS, BSP_GTW_MINB)
 spmm_decode_gtw_kernel(const GtwArgs a)
 {
     using namespace gtw;
+    constexpr bool RS = SKIP ? (BSP_GTW_RS_SKIP != 0) : (BSP_GTW_RS_SPMM != 0);
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
     constexpr uint32_t FULL = 0xFFFFFFFFu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t SB = a.stage_bytes;
-    uint32_t* bases = reinterpret_cast<uint32_t*>(smem + S * SB);             // [CW][64]
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + CW * 256);   // [S]
+    uint32_t* bases = reinterpret_cast<uint32_t*>(smem + S * SB);             // [CW][AREA / 4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + CW * AREA);  // [S]
     uint64_t* empty = full + S;                                                // [S]
     uint64_t* full_v = full + 2 * S;                                           // [S] spMspV values
 
@@ -1032,7 +1061,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
     } else {
         // ---- consumers
         const int cw = warp - 1;
-        uint32_t* base_s = bases + cw * 64;
+        uint32_t* base_s = bases + cw * (AREA / 4);
         uint32_t vpar = 0;  // spMspV: parity of the next full_v wait, bit per stage
         for (int i = cw; i < cnt; i += CW) {
             const int s = i % S;
@@ -1074,13 +1103,20 @@ spmm_decode_gtw_kernel(const GtwArgs a)
                 if (lane >= d) incl += o;
             }
             const uint32_t ex = incl - (c0 + c1) + shift;
-            base_s[2 * lane] = ex;
-            base_s[2 * lane + 1] = ex + c0;
+            if constexpr (RS) {
+                // first value of every BT row of the GT: BTs 2 lane, 2 lane + 1
+                uint4* rs = reinterpret_cast<uint4*>(base_s) + 2 * lane;
+                rs[0] = bspx::row_starts(bb.x, ex);
+                rs[1] = bspx::row_starts(bb.y, ex + c0);
+            } else {
+                base_s[2 * lane] = ex;
+                base_s[2 * lane + 1] = ex + c0;
+            }
             __syncwarp();
-            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
-                                                           lane, 0, acc, cols);
-            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
-                                                           lane, 4, acc, cols);
+            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL, RS>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
+                                                               lane, 0, acc, cols);
+            decode_gt<NT, false, SKIP, BSP_GTW_OCT_UNROLL, RS>(bm_st, base_s, st + a.val_off, xraw, nullptr, N, act8,
+                                                               lane, 4, acc, cols);
             __syncwarp();
             if (lane == 0) bspx::mbar_arrive(empty + s);
         }
