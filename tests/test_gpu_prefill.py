@@ -32,13 +32,30 @@ def _run(W, X):
                                    (128, 320, 256),    # more k-blocks than stages
                                    (192, 256, 17),     # M % 128 == 64: half tile
                                    (384, 640, 300),    # two N tiles, the second ragged
-                                   (256, 1024, 513)])
+                                   (256, 1024, 513),
+                                   (512, 448, 300),    # four tiles, one ragged 512-column N tile
+                                   (768, 640, 256),    # six tiles, one 256-column sub-tile
+                                   (1024, 128, 40)])   # eight tiles, two k-blocks, narrow N
 def test_prefill_small_shapes(M, K, N):
     W = synth.weights_f16(M, K, 0.5, "uniform", 300 + M + K + N)
     X = synth.activations_f16(N, K, 301 + N)
     Y = _run(W, X)
     Yref, S = oracle.spmm_f16(W, X)
     assert_within_bound(Y, Yref, S, f"prefill {M}x{K} N={N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 1024, 513), (512, 448, 300), (768, 640, 256), (1024, 128, 40)])
+def test_prefill_cta_pairs(M, K, N, monkeypatch):
+    """The opt-in CTA-pair kernel (tcgen05.mma.cta_group::2: two 128-row
+    tiles share each MMA, each CTA holding half of the X sub-tile) matches
+    the oracle, then the default path again."""
+    W = synth.weights_f16(M, K, 0.5, "uniform", 350 + M + K + N)
+    X = synth.activations_f16(N, K, 351 + N)
+    Yref, S = oracle.spmm_f16(W, X)
+    monkeypatch.setenv("BSP_PF_PAIR", "1")
+    assert_within_bound(_run(W, X), Yref, S, f"pair prefill {M}x{K} N={N}")
+    monkeypatch.delenv("BSP_PF_PAIR")
+    assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
 
 
 def test_prefill_small_integers_exact():
