@@ -122,35 +122,51 @@ def position(K: int, g: int, p: int):
 
 # ---------------------------------------------------------------- format
 
+def _padded(n: int) -> int:
+    return (n + 63) // 64 * 64
+
+
 def encode(W: np.ndarray) -> dict:
-    """Encode dense ``W`` (uint16 fp16 bits or int8, [M][K]) into the format."""
+    """Encode dense ``W`` (uint16 fp16 bits or int8, [M][K]) into the format.
+
+    When M or K is not a multiple of 64 the grid of GroupTiles covers W
+    padded with zeros to multiples of 64 (the edge GroupTiles are zero-padded;
+    padding stores no values and its bits are 0).
+    """
     W = np.ascontiguousarray(W)
     M, K = W.shape
-    if M % 64 or K % 64:
-        raise ValueError("M and K must be multiples of 64")
+    if M < 1 or K < 1:
+        raise ValueError("M and K must be positive")
+    Mp, Kp = _padded(M), _padded(K)
+    if (Mp, Kp) != (M, K):
+        Wp = np.zeros((Mp, Kp), dtype=W.dtype)
+        Wp[:M, :K] = W
+    else:
+        Wp = W
     eb = _elem_bytes(W)
     lib = _load()
-    NBT = M * K // 64
-    NGT = (M // 64) * (K // 64)
+    NBT = Mp * Kp // 64
+    NGT = (Mp // 64) * (Kp // 64)
     bitmaps = np.zeros(NBT, dtype=np.uint64)
-    nnz = lib.oracle_encode_bitmaps(_ptr(W), eb, M, K, _ptr(bitmaps))
+    nnz = lib.oracle_encode_bitmaps(_ptr(Wp), eb, Mp, Kp, _ptr(bitmaps))
     offsets = np.zeros(NGT + 1, dtype=np.uint32)
     values = np.zeros(nnz, dtype=W.dtype)
-    lib.oracle_encode_values(_ptr(W), eb, M, K, _ptr(bitmaps), _ptr(offsets),
+    lib.oracle_encode_values(_ptr(Wp), eb, Mp, Kp, _ptr(bitmaps), _ptr(offsets),
                              _ptr(values) if nnz else None)
-    return {"M": M, "K": K, "dtype": W.dtype, "NGT": NGT, "NBT": NBT,
-            "NNZ": int(nnz), "bitmaps": bitmaps, "offsets": offsets,
+    return {"M": M, "K": K, "Mp": Mp, "Kp": Kp, "dtype": W.dtype, "NGT": NGT,
+            "NBT": NBT, "NNZ": int(nnz), "bitmaps": bitmaps, "offsets": offsets,
             "values": values}
 
 
 def decode(enc: dict) -> np.ndarray:
     M, K = enc["M"], enc["K"]
-    out = np.empty((M, K), dtype=enc["dtype"])
+    Mp, Kp = enc.get("Mp", M), enc.get("Kp", K)
+    out = np.empty((Mp, Kp), dtype=enc["dtype"])
     eb = 2 if enc["dtype"] == np.uint16 else 1
     vals = enc["values"]
     _load().oracle_decode(_ptr(enc["bitmaps"]), _ptr(enc["offsets"]),
-                          _ptr(vals) if vals.size else None, eb, M, K, _ptr(out))
-    return out
+                          _ptr(vals) if vals.size else None, eb, Mp, Kp, _ptr(out))
+    return np.ascontiguousarray(out[:M, :K])
 
 
 def storage_bytes(enc: dict) -> int:

@@ -207,6 +207,42 @@ def test_decode_by_brute_force_python():
     np.testing.assert_array_equal(out, W)
 
 
+# ----------------------------------------------------------- zero-padded edge GroupTiles
+
+@pytest.mark.parametrize("M,K", [(100, 72), (1, 8), (65, 64), (64, 136), (130, 200)])
+def test_padded_edges_by_brute_force(M, K):
+    """M or K not a multiple of 64: the grid covers W padded with zeros to
+    multiples of 64.  Checked position by position against W itself (the
+    oracle's own mapping from (row, col) to (BT, bit)), in a pure-Python
+    scan: a bit is set exactly for the nonzeros of W, never in the padding,
+    and the values come out in BT-then-bit order."""
+    W = synth.weights_f16(M, K, 0.5, "bernoulli", seed=M * 1000 + K)
+    enc = oracle.encode(W)
+    Mp, Kp = -(-M // 64) * 64, -(-K // 64) * 64
+    assert (enc["Mp"], enc["Kp"]) == (Mp, Kp)
+    assert enc["NGT"] == (Mp // 64) * (Kp // 64) and enc["NBT"] == Mp * Kp // 64
+    assert enc["NNZ"] == int(np.count_nonzero(W))
+    k = 0
+    for g in range(enc["NBT"]):
+        bm = int(enc["bitmaps"][g])
+        for p in range(64):
+            r, c = oracle.position(Kp, g, p)
+            inside = r < M and c < K
+            want = inside and W[r, c] != 0
+            assert ((bm >> p) & 1) == int(want), (g, p, r, c)
+            if want:
+                assert enc["values"][k] == W[r, c]
+                k += 1
+    assert k == enc["NNZ"]
+    np.testing.assert_array_equal(oracle.decode(enc), W)
+    # Stor counts the padded grid's tiles and the true nonzeros only
+    assert oracle.storage_bytes(enc) == 4 * (enc["NGT"] + 1) + 8 * enc["NBT"] + 2 * enc["NNZ"]
+    # the product ignores the padding: the dense one of the logical W
+    X = synth.activations_f16(3, K, seed=5)
+    y, _ = oracle.spmm_f16(W, X)
+    np.testing.assert_allclose(y, _f64(X) @ _f64(W).T, rtol=1e-12, atol=1e-15)  # [N][M]
+
+
 # ----------------------------------------------------------- storage accounting
 
 @pytest.mark.parametrize("M,K,s,dt", [(256, 256, 0.5, "f16"), (512, 384, 0.3, "f16"),
