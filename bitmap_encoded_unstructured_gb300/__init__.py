@@ -190,7 +190,9 @@ class BitmapMatrix:
     """An encoded weight W (M x K) living on one GPU.
 
     ``BitmapMatrix(W)`` encodes a CUDA tensor ``W`` (float16 or int8,
-    row-major [M][K], M and K multiples of 64).  ``spmm(X)`` takes
+    row-major [M][K]; K a multiple of 8 for float16, 16 for int8; edge
+    GroupTiles are zero-padded when M or K is not a multiple of 64).
+    ``spmm(X)`` takes
     X [N][K] and returns Y [N][M] (= (W @ X.T).T, the [tokens, features]
     layout).
     """
@@ -215,7 +217,8 @@ class BitmapMatrix:
     def from_arrays(cls, bitmaps, offsets, values, M: int, K: int, device=None, stream=None):
         """A handle from encoded arrays (tensors on the GPU or the CPU, or numpy
         arrays): bitmaps int64/uint64 [M*K/64], offsets int32/uint32 [NGT+1],
-        values fp16 (or uint16 bits) / int8 [NNZ].  Validated on the device."""
+        values fp16 (or uint16 bits) / int8 [NNZ]; M*K counted on the grid
+        padded to multiples of 64.  Validated on the device."""
         import numpy as np
         import torch
 

@@ -58,7 +58,7 @@ bsp_status_t grow(void** p, size_t* have, size_t need)
 bsp_status_t alloc_scratch(bsp_handle* h, cudaStream_t s)
 {
     const size_t ws_bytes = (size_t)BSP_DECODE_MAX_N * (size_t)h->M * 4;
-    const size_t cnt_bytes = (size_t)(h->M / 64) * 4;
+    const size_t cnt_bytes = (size_t)(h->Mp / 64) * 4;
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess || cudaMalloc(&h->counters, cnt_bytes) != cudaSuccess ||
         cudaMalloc(&h->err, sizeof(int)) != cudaSuccess)
         return BSP_ERR_OOM;
@@ -69,6 +69,17 @@ bsp_status_t alloc_scratch(bsp_handle* h, cudaStream_t s)
     return BSP_OK;
 }
 
+// Shapes the library takes: any M >= 1; K a multiple of 8 (fp16) or 16
+// (int8), so that every row of W and of X starts on a 16-byte boundary (the
+// bulk copies and vector loads need it).  M and K need not be multiples of
+// 64: the format covers the zero-padded grid (edge GroupTiles padded with
+// zeros, which are not stored).
+bool shape_ok(bsp_dtype_t dtype, int64_t M, int64_t K)
+{
+    if (M <= 0 || K <= 0) return false;
+    return (K % (dtype == BSP_INT8 ? 16 : 8)) == 0;
+}
+
 bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
 {
     bsp_handle* h = new (std::nothrow) bsp_handle{};
@@ -77,8 +88,10 @@ bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
     h->dtype = dtype;
     h->M = M;
     h->K = K;
-    h->NGT = (M / 64) * (K / 64);
-    h->NBT = M * K / 64;
+    h->Mp = (M + 63) / 64 * 64;
+    h->Kp = (K + 63) / 64 * 64;
+    h->NGT = (h->Mp / 64) * (h->Kp / 64);
+    h->NBT = h->Mp * h->Kp / 64;
     h->max_gt_nnz = 4096;  // set from the arrays by the encoder / the import check
     return h;
 }
@@ -92,7 +105,7 @@ const char* bsp_status_string(bsp_status_t s)
     switch (s) {
     case BSP_OK: return "ok";
     case BSP_ERR_INVALID_ARG: return "invalid argument";
-    case BSP_ERR_SHAPE: return "M and K must be positive multiples of 64 (and NNZ < 2^32)";
+    case BSP_ERR_SHAPE: return "bad shape: M, K >= 1, K a multiple of 8 (fp16) or 16 (int8), NNZ < 2^32";
     case BSP_ERR_DTYPE: return "dtype does not match the handle";
     case BSP_ERR_ALIGN: return "pointer not 16-byte aligned";
     case BSP_ERR_OOM: return "allocation failed";
@@ -110,7 +123,7 @@ bsp_status_t bsp_encode(const void* W, bsp_dtype_t dtype, int64_t M, int64_t K,
     *out = nullptr;
     if (!W) return BSP_ERR_INVALID_ARG;
     if (dtype != BSP_FP16 && dtype != BSP_INT8) return BSP_ERR_DTYPE;
-    if (M <= 0 || K <= 0 || (M % 64) || (K % 64)) return BSP_ERR_SHAPE;
+    if (!shape_ok(dtype, M, K)) return BSP_ERR_SHAPE;
     if (!aligned16(W)) return BSP_ERR_ALIGN;
     bsp_handle* h = new_handle(dtype, M, K);
     if (!h) return BSP_ERR_OOM;
@@ -276,8 +289,7 @@ bsp_status_t bsp_import(const uint64_t* bitmaps, const uint32_t* offsets, const 
     *out = nullptr;
     if (!bitmaps || !offsets || (nnz && !values)) return BSP_ERR_INVALID_ARG;
     if (dtype != BSP_FP16 && dtype != BSP_INT8) return BSP_ERR_DTYPE;
-    if (M <= 0 || K <= 0 || (M % 64) || (K % 64) || nnz > 0xFFFFFFFFull || nnz > (uint64_t)M * (uint64_t)K)
-        return BSP_ERR_SHAPE;
+    if (!shape_ok(dtype, M, K) || nnz > 0xFFFFFFFFull || nnz > (uint64_t)M * (uint64_t)K) return BSP_ERR_SHAPE;
     bsp_handle* h = new_handle(dtype, M, K);
     if (!h) return BSP_ERR_OOM;
     if (cudaGetDevice(&h->device) != cudaSuccess ||

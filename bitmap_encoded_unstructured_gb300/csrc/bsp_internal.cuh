@@ -14,8 +14,9 @@ struct bsp_handle {
     uint32_t magic;
     int device;
     bsp_dtype_t dtype;
-    int64_t M, K;         // multiples of 64
-    int64_t NGT, NBT;     // GroupTiles (64x64), BitmapTiles (8x8)
+    int64_t M, K;         // logical shape of W (K a multiple of 8, of 16 for int8)
+    int64_t Mp, Kp;       // M, K rounded up to multiples of 64: the zero-padded grid of the format
+    int64_t NGT, NBT;     // GroupTiles (64x64), BitmapTiles (8x8) of the padded grid
     uint64_t NNZ;
     uint32_t max_gt_nnz;  // largest nonzero count of one GT (sizes the decode stages)
     uint64_t* bitmaps;    // [NBT]
@@ -60,7 +61,8 @@ struct bsp_decode_problem {
     const uint32_t* offsets;
     const void* values;
     bsp_dtype_t dtype;
-    int64_t M, K;
+    int64_t M, K;         // logical shape: Y rows, X row length
+    int64_t Mp, Kp;       // padded grid: Mp / 64 row strips, Kp / 64 GT columns
     uint32_t max_gt_nnz;  // bound on the nonzeros of one GT (4096: unknown)
     int device, num_sms;
     void* ws;

@@ -21,6 +21,23 @@ __device__ __forceinline__ int bt_local(int br, int bc)
     return (((br >> 1) * 4 + (bc >> 1)) << 2) + (br & 1) + ((bc & 1) << 1);
 }
 
+// Logical shape of W inside its zero-padded grid: M rows, K8 row-bytes per
+// row (K / 8), padded width Kp (a multiple of 64).  Row-bytes outside
+// [0, M) x [0, K8) are padding: no nonzeros, nothing read or written.
+struct EncShape {
+    int64_t M, K8, Kp;
+};
+
+// Row-byte i of the padded grid -> its index in the logical W, or false.
+__device__ __forceinline__ bool logical_rowbyte(int64_t i, const EncShape& sh, int64_t* li)
+{
+    const int64_t Kp8 = sh.Kp >> 3;
+    const int64_t r = i / Kp8, c8 = i - r * Kp8;
+    if (r >= sh.M || c8 >= sh.K8) return false;
+    *li = r * sh.K8 + c8;
+    return true;
+}
+
 struct RowByte {
     int64_t g;   // global BT index
     int64_t t;   // GT index
@@ -87,16 +104,19 @@ __device__ __forceinline__ Row8<EB> load_row8(const void* W, int64_t i)
 
 // Pass 1: one byte of a bitmap per thread (the row-byte's occupancy).
 template <int EB>
-__global__ void enc_bitmap_kernel(const void* __restrict__ W, int64_t n_rowbytes,
-                                  int64_t K, uint8_t* __restrict__ bitmap_bytes)
+__global__ void enc_bitmap_kernel(const void* __restrict__ W, int64_t n_rowbytes, EncShape sh,
+                                  uint8_t* __restrict__ bitmap_bytes)
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_rowbytes) return;
-    const Row8<EB> e = load_row8<EB>(W, i);
+    int64_t li;
     uint32_t byte = 0;
+    if (logical_rowbyte(i, sh, &li)) {
+        const Row8<EB> e = load_row8<EB>(W, li);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) byte |= (e.elem(j) != 0u ? 1u : 0u) << j;
-    const RowByte rb = row_byte(i, K);
+        for (int j = 0; j < 8; ++j) byte |= (e.elem(j) != 0u ? 1u : 0u) << j;
+    }
+    const RowByte rb = row_byte(i, sh.Kp);
     // little-endian: byte rr of the uint64 holds bits 8*rr .. 8*rr+7
     bitmap_bytes[rb.g * 8 + rb.rr] = (uint8_t)byte;
 }
@@ -189,7 +209,7 @@ __device__ __forceinline__ uint64_t rowbyte_slot(const uint64_t* bitmaps, const 
 
 // Pass 4: write each row-byte's nonzeros to their packed slots.
 template <int EB>
-__global__ void enc_pack_kernel(const void* __restrict__ W, int64_t n_rowbytes, int64_t K,
+__global__ void enc_pack_kernel(const void* __restrict__ W, int64_t n_rowbytes, EncShape sh,
                                 const uint64_t* __restrict__ bitmaps,
                                 const uint32_t* __restrict__ offsets,
                                 const uint32_t* __restrict__ bt_prefix,
@@ -197,10 +217,12 @@ __global__ void enc_pack_kernel(const void* __restrict__ W, int64_t n_rowbytes, 
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_rowbytes) return;
-    const RowByte rb = row_byte(i, K);
+    int64_t li;
+    if (!logical_rowbyte(i, sh, &li)) return;  // padding: no nonzeros
+    const RowByte rb = row_byte(i, sh.Kp);
     uint32_t byte;
     uint64_t slot = rowbyte_slot(bitmaps, offsets, bt_prefix, rb, &byte);
-    const Row8<EB> e = load_row8<EB>(W, i);
+    const Row8<EB> e = load_row8<EB>(W, li);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if ((byte >> j) & 1u) {
@@ -220,11 +242,13 @@ template <int EB>
 __global__ void dec_kernel(const uint64_t* __restrict__ bitmaps,
                            const uint32_t* __restrict__ offsets,
                            const uint8_t* __restrict__ values, int64_t n_rowbytes,
-                           int64_t K, void* __restrict__ W_out)
+                           EncShape shape, void* __restrict__ W_out)
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_rowbytes) return;
-    const RowByte rb = row_byte(i, K);
+    int64_t li;
+    if (!logical_rowbyte(i, shape, &li)) return;  // padding is not part of W
+    const RowByte rb = row_byte(i, shape.Kp);
     const int64_t g0 = rb.t * 64;
     uint64_t pre = 0;
     for (int64_t g = g0; g < rb.g; ++g) pre += (uint64_t)__popcll(__ldg(bitmaps + g));
@@ -247,27 +271,42 @@ __global__ void dec_kernel(const uint64_t* __restrict__ bitmaps,
         }
     }
     if constexpr (EB == 2)
-        reinterpret_cast<uint4*>(W_out)[i] = out.v;
+        reinterpret_cast<uint4*>(W_out)[li] = out.v;
     else
-        reinterpret_cast<uint2*>(W_out)[i] = out.v;
+        reinterpret_cast<uint2*>(W_out)[li] = out.v;
 }
 
 inline unsigned grid_for(int64_t n, int block) { return (unsigned)((n + block - 1) / block); }
 
-// Validation of imported arrays: offsets[0] == 0 and, for every GT,
-// offsets[t+1] - offsets[t] == sum of the popcounts of its 64 bitmaps.
-// One warp per GT; any violation sets bad[0]; bad[1] gets the largest
-// GT nonzero count.
+// Validation of imported arrays: offsets[0] == 0, for every GT
+// offsets[t+1] - offsets[t] == sum of the popcounts of its 64 bitmaps, and
+// no bit set in the zero padding of the edge GTs (rows >= M, columns >= K).
+// One warp per GT; any violation sets bad[0]; bad[1] gets the largest GT
+// nonzero count.
 __global__ void validate_kernel(const uint64_t* __restrict__ bitmaps, const uint32_t* __restrict__ offsets,
-                                int64_t NGT, int* bad)
+                                int64_t NGT, int64_t M, int64_t K, int64_t KTp, int* bad)
 {
     const int lane = threadIdx.x & 31;
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= NGT) return;
     const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2*>(bitmaps + t * 64) + lane);
+    // rows / columns of this GT inside W
+    const int64_t vr = M - (t / KTp) * 64, vc = K - (t % KTp) * 64;
+    bool pad_ok = true;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int gl = 2 * lane + k;                    // BT inside the GT
+        const int tl = gl >> 2, bq = gl & 3;            // TCTile, BT inside it (TL, BL, TR, BR)
+        const int br = 2 * (tl >> 2) + (bq & 1), bc = 2 * (tl & 3) + (bq >> 1);
+        const int64_t rv = vr - 8 * br, cv = vc - 8 * bc;  // valid rows / columns of the BT (K % 8 == 0)
+        uint64_t valid = 0;
+        if (cv > 0 && rv > 0) valid = rv >= 8 ? ~0ull : ((1ull << (8 * rv)) - 1ull);
+        pad_ok = pad_ok && (((k ? b.y : b.x) & ~valid) == 0ull);
+    }
     uint32_t c = __popcll(b.x) + __popcll(b.y);
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
+    if (!__all_sync(0xFFFFFFFFu, pad_ok) && lane == 0) atomicExch(bad, 1);
     if (lane == 0) {
         const uint32_t o0 = __ldg(offsets + t), o1 = __ldg(offsets + t + 1);
         if (o1 < o0 || o1 - o0 != c || (t == 0 && o0 != 0)) atomicExch(bad, 1);
@@ -275,14 +314,13 @@ __global__ void validate_kernel(const uint64_t* __restrict__ bitmaps, const uint
     }
 }
 
-
-
 }  // namespace
 
 bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s)
 {
     const int eb = bsp_elem_bytes(h->dtype);
-    const int64_t n_rowbytes = h->M * h->K / 8;
+    const int64_t n_rowbytes = h->Mp * h->Kp / 8;  // the padded grid
+    const EncShape sh{h->M, h->K / 8, h->Kp};
     uint32_t* bt_prefix = nullptr;
     uint32_t* gt_nnz = nullptr;
     int* overflow = nullptr;
@@ -301,9 +339,9 @@ bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s)
     if (cudaMemsetAsync(overflow, 0, 2 * sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
 
     if (eb == 2)
-        enc_bitmap_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, (uint8_t*)h->bitmaps);
+        enc_bitmap_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, sh, (uint8_t*)h->bitmaps);
     else
-        enc_bitmap_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, (uint8_t*)h->bitmaps);
+        enc_bitmap_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, sh, (uint8_t*)h->bitmaps);
     enc_count_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->NGT, bt_prefix, gt_nnz,
                                                                 reinterpret_cast<unsigned int*>(overflow + 1));
     enc_scan_kernel<<<1, 1024, 0, s>>>(gt_nnz, h->NGT, h->offsets, overflow);
@@ -324,10 +362,10 @@ bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s)
     if (cudaMalloc(&h->values, h->values_alloc) != cudaSuccess) { st = BSP_ERR_OOM; goto done; }
     if (cudaMemsetAsync(h->values, 0, h->values_alloc, s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
     if (eb == 2)
-        enc_pack_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, h->bitmaps, h->offsets,
+        enc_pack_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, sh, h->bitmaps, h->offsets,
                                                                      bt_prefix, (uint8_t*)h->values);
     else
-        enc_pack_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, h->K, h->bitmaps, h->offsets,
+        enc_pack_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(W, n_rowbytes, sh, h->bitmaps, h->offsets,
                                                                      bt_prefix, (uint8_t*)h->values);
     if (cudaGetLastError() != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
     // the temporaries are freed below; make sure the pack has consumed them
@@ -341,13 +379,14 @@ done:
 
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s)
 {
-    const int64_t n_rowbytes = h->M * h->K / 8;
+    const int64_t n_rowbytes = h->Mp * h->Kp / 8;
+    const EncShape sh{h->M, h->K / 8, h->Kp};
     if (bsp_elem_bytes(h->dtype) == 2)
         dec_kernel<2><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(h->bitmaps, h->offsets, (const uint8_t*)h->values,
-                                                                n_rowbytes, h->K, W_out);
+                                                                n_rowbytes, sh, W_out);
     else
         dec_kernel<1><<<grid_for(n_rowbytes, 256), 256, 0, s>>>(h->bitmaps, h->offsets, (const uint8_t*)h->values,
-                                                                n_rowbytes, h->K, W_out);
+                                                                n_rowbytes, sh, W_out);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
@@ -359,7 +398,8 @@ bsp_status_t bsp_run_validate(bsp_handle* h, cudaStream_t s)
     bsp_status_t st = BSP_OK;
     if (cudaMalloc(&bad, 2 * sizeof(int)) != cudaSuccess) return BSP_ERR_OOM;
     if (cudaMemsetAsync(bad, 0, 2 * sizeof(int), s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
-    validate_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->offsets, h->NGT, bad);
+    validate_kernel<<<grid_for(h->NGT * 32, 256), 256, 0, s>>>(h->bitmaps, h->offsets, h->NGT, h->M, h->K,
+                                                               h->Kp / 64, bad);
     if (cudaGetLastError() != cudaSuccess ||
         cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyAsync(&maxc, bad + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||

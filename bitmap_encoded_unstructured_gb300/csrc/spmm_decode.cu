@@ -394,6 +394,34 @@ __device__ __forceinline__ void decode_gt(const uint64_t* bm_st, const uint32_t*
     }
 }
 
+// The last GT column of a K that is not a multiple of 64 holds fewer than
+// 64 activations: x_tail_zero clears the rest of the stage's X row (generic
+// stores by the producer lane, made before its arrive on the stage barrier
+// so that they are released with it; the proxy fence orders them before
+// later bulk copies into the same bytes), x_row_copy copies the part inside
+// K (a multiple of 16 bytes: K % (16 / eb) == 0).
+__device__ __forceinline__ uint32_t x_row_bytes(int64_t K, int64_t gj, int eb)
+{
+    const int64_t kv = K - gj * 64;
+    return (uint32_t)((kv >= 64 ? 64 : kv) * eb);
+}
+
+__device__ __forceinline__ void x_tail_zero(uint8_t* dst, int64_t K, int64_t gj, int eb)
+{
+    const uint32_t bytes = x_row_bytes(K, gj, eb);
+    if (bytes < (uint32_t)(64 * eb)) {
+        for (uint32_t b = bytes; b < (uint32_t)(64 * eb); b += 16)
+            *reinterpret_cast<uint4*>(dst + b) = make_uint4(0, 0, 0, 0);
+        bspx::fence_proxy_async_smem();
+    }
+}
+
+__device__ __forceinline__ void x_row_copy(uint8_t* dst, const uint8_t* row, int64_t K, int64_t gj, int eb,
+                                           uint64_t* bar)
+{
+    bspx::bulk_g2s(dst, row + gj * 64 * eb, x_row_bytes(K, gj, eb), bar);
+}
+
 __device__ __forceinline__ float ws_take(float* p) { return atomicExch(p, 0.0f); }
 __device__ __forceinline__ int ws_take(int* p) { return atomicExch(p, 0); }
 
@@ -403,7 +431,8 @@ struct Args {
     const uint8_t* values;
     const uint8_t* X;
     int N;
-    int64_t M, K;
+    int64_t M, K;     // logical: Y rows, X row length
+    int64_t KT;       // GT columns of the padded grid
     int splits, per_split;
     void* ws;
     uint32_t* counters;
@@ -438,7 +467,7 @@ spmm_decode_kernel(const Args a)
     uint64_t* empty = full + 2 * C::S;                               // [S] both warps done
 
     const int64_t K = a.K, M = a.M;
-    const int64_t KT = K >> 6;
+    const int64_t KT = a.KT;
     const int64_t gi = blockIdx.y;
     const int64_t k_begin = (int64_t)blockIdx.x * a.per_split;
     const int64_t k_cnt = min((int64_t)a.per_split, KT - k_begin);
@@ -470,18 +499,18 @@ spmm_decode_kernel(const Args a)
     auto issue_meta = [&](int i, int s, bool with_values, uint32_t o0, uint32_t o1) {
         uint8_t* st = stage_ptr(s);
         const int64_t t = t0 + i, gj = g0 + i;
-        uint32_t bytes = 512 + (uint32_t)(N * 64 * C::EB);
+        uint32_t bytes = 512 + (uint32_t)N * x_row_bytes(K, gj, C::EB);
         uint32_t ch0 = 0, nch = 0;
         if (with_values) {
             ch0 = o0 / C::E16;
             nch = (o1 + C::E16 - 1) / C::E16 - ch0;
             bytes += nch * 16;
         }
+        for (int n = 0; n < N; ++n) x_tail_zero(st + C::ST_X + n * 64 * C::EB, K, gj, C::EB);
         bspx::mbar_arrive_expect_tx(full + s, bytes);
         bspx::bulk_g2s(st + C::ST_BM, a.bitmaps + t * 64, 512, full + s);
         for (int n = 0; n < N; ++n)
-            bspx::bulk_g2s(st + C::ST_X + n * 64 * C::EB, a.X + ((int64_t)n * K + gj * 64) * C::EB,
-                           64 * C::EB, full + s);
+            x_row_copy(st + C::ST_X + n * 64 * C::EB, a.X + (int64_t)n * K * C::EB, K, gj, C::EB, full + s);
         if (with_values && nch)
             bspx::bulk_g2s(st + C::ST_VAL, a.values + (int64_t)ch0 * 16, nch * 16, full + s);
     };
@@ -567,10 +596,12 @@ spmm_decode_kernel(const Args a)
             // 8-B load) and keeps their K-octet activity mask
             if (lane >= C::S && lane < cnt) {
                 const uint8_t* xp = a.X + (g0 + lane) * 64 * C::EB;
+                const int64_t kv = K - (g0 + lane) * 64;  // activations of this GT column inside K
                 uint32_t act = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     bool nz = false;
+                    if (8 * j >= kv) break;
                     if constexpr (C::EB == 2) {
                         const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + j);
                         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -732,8 +763,8 @@ spmm_decode_kernel(const Args a)
 #pragma unroll
             for (int w = 0; w < 2; ++w)
                 sum += reinterpret_cast<const Acc*>(smem + t * C::TEAM_BYTES + w * C::RED_BYTES)[i];
-        if (n < N) {
-            const int64_t m = gi * 64 + r;
+        const int64_t m = gi * 64 + r;
+        if (n < N && m < M) {  // rows past M are padding
             if (a.splits == 1)
                 write_out(a.Y, a.mode, (int64_t)n * M + m, sum, a.row_scale ? a.row_scale[m] : 1.0f);
             else
@@ -751,6 +782,7 @@ spmm_decode_kernel(const Args a)
     for (int i = threadIdx.x; i < 64 * N; i += C::THREADS) {
         const int n = i >> 6, r = i & 63;
         const int64_t m = gi * 64 + r;
+        if (m >= M) continue;
         const Acc v = ws_take(ws + (int64_t)n * M + m);
         write_out(a.Y, a.mode, (int64_t)n * M + m, v, a.row_scale ? a.row_scale[m] : 1.0f);
     }
@@ -834,7 +866,8 @@ struct GtwArgs {
     const uint8_t* values;
     const uint8_t* X;
     int N;
-    int64_t M, K;
+    int64_t M, K;     // logical: Y rows, X row length
+    int64_t KT;       // GT columns of the padded grid
     int splits, per_split;
     float* ws;
     uint32_t* counters;
@@ -862,7 +895,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
     uint64_t* empty = full + S;                                                // [S]
     uint64_t* full_v = full + 2 * S;                                           // [S] spMspV values
 
-    const int64_t K = a.K, M = a.M, KT = K >> 6;
+    const int64_t K = a.K, M = a.M, KT = a.KT;
     const int64_t gi = blockIdx.y;
     const int64_t k_begin = (int64_t)blockIdx.x * a.per_split;
     const int cnt = (int)max((int64_t)0, min((int64_t)a.per_split, KT - k_begin));
@@ -907,11 +940,11 @@ spmm_decode_gtw_kernel(const GtwArgs a)
                 uint8_t* st = smem + s * SB;
                 const uint32_t ch0 = o0 / 8, nch = (o1 + 7) / 8 - ch0;
                 *reinterpret_cast<uint32_t*>(st + 512) = o0 - ch0 * 8;
-                bspx::mbar_arrive_expect_tx(full + s, 512u + (uint32_t)N * 128u + nch * 16u);
+                for (int n = 0; n < N; ++n) x_tail_zero(st + 512 + HDR + n * 128, K, k_begin + i, 2);
+                bspx::mbar_arrive_expect_tx(full + s, 512u + (uint32_t)N * x_row_bytes(K, k_begin + i, 2) + nch * 16u);
                 bspx::bulk_g2s(st, a.bitmaps + (t0 + i) * 64, 512, full + s);
                 for (int n = 0; n < N; ++n)
-                    bspx::bulk_g2s(st + 512 + HDR + n * 128, a.X + ((int64_t)n * K + (k_begin + i) * 64) * 2, 128,
-                                   full + s);
+                    x_row_copy(st + 512 + HDR + n * 128, a.X + (int64_t)n * K * 2, K, k_begin + i, 2, full + s);
                 if (nch) bspx::bulk_g2s(st + a.val_off, a.values + (int64_t)ch0 * 16, nch * 16, full + s);
             }
             if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
@@ -1007,8 +1040,10 @@ spmm_decode_gtw_kernel(const GtwArgs a)
                             if (j < cnt) {
                                 act = 0;
                                 const uint4* xp = reinterpret_cast<const uint4*>(a.X + (k_begin + j) * 64 * 2);
+                                const int64_t kv = K - (k_begin + j) * 64;  // activations inside K
 #pragma unroll
                                 for (int o = 0; o < 8; ++o) {
+                                    if (8 * o >= kv) break;
                                     const uint4 q = __ldg(xp + o);
                                     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
                                     bool nz = false;
@@ -1034,9 +1069,10 @@ spmm_decode_gtw_kernel(const GtwArgs a)
                         hdr[0] = o0 - ch0 * 8;
                         hdr[1] = ch0;
                         hdr[2] = a8;
-                        bspx::mbar_arrive_expect_tx(full + sn, 512u + 128u + nch * 16u);
+                        x_tail_zero(st + 512 + HDR, K, k_begin + next, 2);
+                        bspx::mbar_arrive_expect_tx(full + sn, 512u + x_row_bytes(K, k_begin + next, 2) + nch * 16u);
                         bspx::bulk_g2s(st, a.bitmaps + (t0 + next) * 64, 512, full + sn);
-                        bspx::bulk_g2s(st + 512 + HDR, a.X + (k_begin + next) * 64 * 2, 128, full + sn);
+                        x_row_copy(st + 512 + HDR, a.X, K, k_begin + next, 2, full + sn);
                         if (nch) bspx::bulk_g2s(st + a.val_off, a.values + (int64_t)ch0 * 16, nch * 16, full + sn);
                     }
                     ++next;
@@ -1140,8 +1176,8 @@ spmm_decode_gtw_kernel(const GtwArgs a)
         float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < CW; ++c) sum += red[c * 64 * NT + i];
-        if (n < N) {
-            const int64_t m = gi * 64 + r;
+        const int64_t m = gi * 64 + r;
+        if (n < N && m < M) {  // rows past M are padding
             if (a.splits == 1)
                 a.Y[(int64_t)n * M + m] = __float2half_rn(sum);
             else
@@ -1159,6 +1195,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
     for (int i = threadIdx.x; i < 64 * N; i += THREADS) {
         const int n = i >> 6, r = i & 63;
         const int64_t m = gi * 64 + r;
+        if (m >= M) continue;
         a.Y[(int64_t)n * M + m] = __float2half_rn(ws_take(a.ws + (int64_t)n * M + m));
     }
     if (threadIdx.x == 0) a.counters[gi] = 0u;
@@ -1207,7 +1244,7 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     }
     stage_geometry(NT, std::min<uint32_t>(p.max_gt_nnz, 4096u), stage_bytes, val_off);
     const size_t smem = smem_bytes(stage_bytes);
-    const int64_t strips = p.M / 64, KT = p.K / 64;
+    const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
     int per_sm = (int)std::min<size_t>((size_t)BSP_GTW_MINB, (size_t)(227 * 1024) / (smem + 1024));
     if (per_sm < 1) per_sm = 1;
     const int splits0 = gtw_splits(strips, KT, (int64_t)p.num_sms * per_sm);
@@ -1221,6 +1258,7 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     a.N = N;
     a.M = p.M;
     a.K = p.K;
+    a.KT = p.Kp / 64;
     a.splits = splits;
     a.per_split = per_split;
     a.ws = (float*)p.ws;
@@ -1252,7 +1290,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
             return BSP_ERR_CUDA;
         attr_done[p.device] = true;
     }
-    const int64_t KT = p.K / 64;
+    const int64_t KT = p.Kp / 64;
     int splits = bsp_decode_splits(p, N);
     const int per_split = (int)((KT + splits - 1) / splits);
     splits = (int)((KT + per_split - 1) / per_split);  // drop empty splits
@@ -1264,6 +1302,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
     a.N = N;
     a.M = p.M;
     a.K = p.K;
+    a.KT = p.Kp / 64;
     a.splits = splits;
     a.per_split = per_split;
     a.ws = p.ws;
@@ -1276,7 +1315,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
     a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
     a.tau = tau;
-    dim3 grid((unsigned)splits, (unsigned)(p.M / 64));
+    dim3 grid((unsigned)splits, (unsigned)(p.Mp / 64));
     spmm_decode_kernel<NT, I8, SKIP><<<grid, C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
@@ -1300,7 +1339,7 @@ bsp_status_t dispatch_nt(const bsp_decode_problem& p, const void* X, int N, void
 int bsp_decode_splits(const bsp_decode_problem& p, int N)
 {
     (void)N;
-    const int64_t strips = p.M / 64, KT = p.K / 64;
+    const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
     // each team run must fit kMaxRun GTs
     const int64_t min_splits = (KT + (int64_t)kMaxRun * kTeams - 1) / ((int64_t)kMaxRun * kTeams);
     int64_t splits;
@@ -1349,6 +1388,8 @@ bsp_decode_problem bsp_problem_of(const bsp_handle* h)
     p.dtype = h->dtype;
     p.M = h->M;
     p.K = h->K;
+    p.Mp = h->Mp;
+    p.Kp = h->Kp;
     p.max_gt_nnz = h->max_gt_nnz;
     p.device = h->device;
     p.num_sms = h->num_sms;

@@ -100,6 +100,8 @@ extern "C" bsp_status_t bsp_spmm_noalloc(const uint64_t* bitmaps, const uint32_t
     p.dtype = dtype;
     p.M = M;
     p.K = K;
+    p.Mp = M;  // this entry takes multiples of 64 only
+    p.Kp = K;
     p.max_gt_nnz = 4096;  // the arrays are not inspected: any GT may be dense
     p.device = dev;
     p.num_sms = d->num_sms;

@@ -174,8 +174,9 @@ struct PrefillArgs {
     const uint32_t* offsets;
     const uint8_t* values;
     __half* Y;
-    int64_t M, N, K;
-    int64_t ntiles;  // N tiles of BN * NSUB columns
+    int64_t M, N, K;  // logical: Y rows, columns, X row length
+    int64_t Mp, KT;   // padded grid: rows (a multiple of 64), GT columns
+    int64_t ntiles;   // N tiles of BN * NSUB columns
     int* err;
     uint32_t spin_cap;
 };
@@ -275,8 +276,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     auto a_stage = [&](int s) { return smem + P::OFF_A + s * A_BYTES; };
     auto c_stage = [&](int s) { return smem + P::OFF_C + s * P::C_STAGE; };
 
-    const int64_t M = a.M, N = a.N, K = a.K;
-    const uint32_t KT = (uint32_t)(K >> 6);
+    const int64_t M = a.M, N = a.N;
+    const uint32_t KT = (uint32_t)a.KT;
     // linear grid of clusters (one CTA, or a pair: two consecutive M tiles),
     // N tiles fastest, so that the CTAs streaming one W row strip run at
     // about the same time and share it in L2
@@ -284,7 +285,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     const int64_t mt = (cl / a.ntiles) * (PAIR ? 2 : 1) + (PAIR ? (int64_t)(blockIdx.x & 1) : 0);
     const int64_t n0 = (cl % a.ntiles) * P::BN_CTA;
     const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
-    const bool has_b = strip1 * 64 < M;  // second GT row strip of the tile exists
+    const bool has_b = strip1 * 64 < a.Mp;  // second GT row strip of the tile exists
     const uint32_t cap = a.spin_cap;
     const uint32_t rank = PAIR ? bspx::cluster_ctarank() : 0u;  // pair: 0 = leader (issues the MMAs)
     const bool leader = rank == 0;
@@ -681,7 +682,7 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     // cross-CTA handshakes and the co-scheduling of cluster pairs cost more
     // than the halved X-tile traffic saves.
     const char* pe = std::getenv("BSP_PF_PAIR");
-    const bool pair = pe && pe[0] == '1' && (p.M % 256) == 0;
+    const bool pair = pe && pe[0] == '1' && (p.Mp % 256) == 0;
     // X: [N][K] fp16, K contiguous; box = 64 (K) x 256 (N) rows, or 128 for a
     // CTA of a pair, with the 128-B swizzle
     CUtensorMap map;
@@ -701,13 +702,15 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     a.M = p.M;
     a.N = N;
     a.K = p.K;
+    a.Mp = p.Mp;
+    a.KT = p.Kp / 64;
     a.err = p.err;
     a.spin_cap = bspx::kSpinCap;
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
     // one 256-column sub-tile per CTA for N <= 256, two (512 columns) above
     if (N > BN)
-        return pair ? launch_prefill<2, true>(map, a, p.M, N, p.device, s)
-                    : launch_prefill<2, false>(map, a, p.M, N, p.device, s);
-    return pair ? launch_prefill<1, true>(map, a, p.M, N, p.device, s)
-                : launch_prefill<1, false>(map, a, p.M, N, p.device, s);
+        return pair ? launch_prefill<2, true>(map, a, p.Mp, N, p.device, s)
+                    : launch_prefill<2, false>(map, a, p.Mp, N, p.device, s);
+    return pair ? launch_prefill<1, true>(map, a, p.Mp, N, p.device, s)
+                : launch_prefill<1, false>(map, a, p.Mp, N, p.device, s);
 }

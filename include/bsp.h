@@ -14,7 +14,9 @@
  *     (rows 0-7/cols 0-7, rows 8-15/cols 0-7, rows 0-7/cols 8-15,
  *      rows 8-15/cols 8-15).
  *   - GroupTile (GT): 64x64 = 4x4 TCTiles, row-major; GTs row-major over the
- *     (M/64) x (K/64) grid.  BT g = (t*16 + tc)*4 + b for GT t, TCTile tc.
+ *     ceil(M/64) x ceil(K/64) grid.  BT g = (t*16 + tc)*4 + b for GT t,
+ *     TCTile tc.  When M or K is not a multiple of 64 the edge GTs are
+ *     padded with zeros (their bits are 0 and nothing is stored for them).
  *   - values: the nonzeros only, packed in GT -> TCTile -> BT -> bit order.
  *   - offsets: uint32 [NGT+1], offsets[t] = nonzeros stored before GT t.
  *   A value's index is offsets[t] + (nonzeros of the earlier BTs of its GT)
@@ -58,7 +60,7 @@ typedef struct bsp_handle *bsp_handle_t;
 typedef enum {
     BSP_OK = 0,
     BSP_ERR_INVALID_ARG = 1, /* null pointer, N out of range, bad handle   */
-    BSP_ERR_SHAPE = 2,       /* M or K not a positive multiple of 64       */
+    BSP_ERR_SHAPE = 2,       /* M, K < 1, or K not a multiple of 8 (fp16) / 16 (int8) */
     BSP_ERR_DTYPE = 3,       /* call does not match the handle's dtype     */
     BSP_ERR_ALIGN = 4,       /* X / Y / W not 16-byte aligned              */
     BSP_ERR_OOM = 5,         /* device or host allocation failed           */
@@ -80,7 +82,7 @@ typedef struct {
     int32_t dtype;        /* bsp_dtype_t                                   */
     int32_t gt_m, gt_k;   /* GroupTile shape: 64, 64                        */
     int32_t device;       /* CUDA device the arrays live on                */
-    int64_t NGT, NBT;     /* GroupTiles, BitmapTiles                        */
+    int64_t NGT, NBT;     /* GroupTiles, BitmapTiles of the padded grid     */
     uint64_t NNZ;         /* stored nonzeros                                */
     const uint64_t *bitmaps; /* device, [NBT]                              */
     const uint32_t *offsets; /* device, [NGT + 1]                          */
@@ -95,8 +97,11 @@ const char *bsp_status_string(bsp_status_t s);
  *   W      device, row-major [M][K] fp16 or int8 (raw bits are examined:
  *          an element is stored iff its bits are nonzero, so -0.0 / NaN /
  *          Inf are kept as payload); 16-byte aligned.  Not retained.
- *   M, K   positive multiples of 64 (BSP_ERR_SHAPE otherwise); the total
- *          nonzero count must fit in uint32.
+ *   M, K   M >= 1; K a multiple of 8 for fp16 or of 16 for int8, so that
+ *          every row of W and of X starts on a 16-byte boundary
+ *          (BSP_ERR_SHAPE otherwise); the total nonzero count must fit in
+ *          uint32.  M and K need not be multiples of 64 (zero-padded edge
+ *          GTs; NGT and NBT count the padded grid).
  *   stream work is ordered on it; the call synchronises `stream` once (to
  *          learn NNZ and size the values array), so W may be freed when it
  *          returns.
@@ -200,12 +205,14 @@ bsp_status_t bsp_export(bsp_handle_t h, uint64_t *bitmaps, uint32_t *offsets,
 
 /*
  * Build a handle from an existing encoding (for instance one cached on disk
- * after bsp_export): copies bitmaps u64 [M*K/64], offsets u32
- * [M/64 * K/64 + 1] and values [nnz] elements from device or host memory
- * (anything cudaMemcpyAsync with cudaMemcpyDefault accepts) into arrays the
- * new handle owns.  The copy is validated on the device (offsets[0] == 0,
- * each GroupTile's offset step == the popcount of its bitmaps, last offset
- * == nnz) before any kernel can read it; an inconsistent encoding returns
+ * after bsp_export): copies bitmaps u64 [Mp*Kp/64], offsets u32
+ * [Mp/64 * Kp/64 + 1] and values [nnz] elements (Mp, Kp: M, K rounded up
+ * to multiples of 64) from device or host memory (anything cudaMemcpyAsync
+ * with cudaMemcpyDefault accepts) into arrays the new handle owns.  The
+ * copy is validated on the device (offsets[0] == 0, each GroupTile's
+ * offset step == the popcount of its bitmaps, no bit set in the zero
+ * padding, last offset == nnz) before any kernel can read it; an
+ * inconsistent encoding returns
  * BSP_ERR_INVALID_ARG and no handle.  Synchronises `stream`; the caller's
  * arrays may be freed when it returns.
  */

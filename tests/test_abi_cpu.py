@@ -52,7 +52,9 @@ def test_argument_errors_without_gpu():
     L = bsp.lib()
     h = ctypes.c_void_p()
     assert L.bsp_encode(None, 0, 64, 64, None, ctypes.byref(h)) == 1   # null W
-    assert L.bsp_encode(16, 0, 65, 64, None, ctypes.byref(h)) == 2     # M % 64
+    assert L.bsp_encode(16, 0, 0, 64, None, ctypes.byref(h)) == 2      # M < 1
+    assert L.bsp_encode(16, 0, 64, 60, None, ctypes.byref(h)) == 2     # fp16: K % 8
+    assert L.bsp_encode(16, 1, 64, 72, None, ctypes.byref(h)) == 2     # int8: K % 16
     assert L.bsp_encode(16, 7, 64, 64, None, ctypes.byref(h)) == 3     # dtype
     assert L.bsp_encode(8, 0, 64, 64, None, ctypes.byref(h)) == 4      # alignment
     assert L.bsp_spmm(None, 16, 1, 16, None) == 1

@@ -294,7 +294,7 @@ def test_abi_error_paths():
     Wd = to_dev_f16(W, DEV)
     L = bsp.lib()
     h = ctypes.c_void_p()
-    assert L.bsp_encode(Wd.data_ptr(), 0, 100, 128, None, ctypes.byref(h)) == 2
+    assert L.bsp_encode(Wd.data_ptr(), 0, 128, 100, None, ctypes.byref(h)) == 2  # fp16: K % 8
     assert L.bsp_encode(Wd.data_ptr() + 2, 0, 64, 64, None, ctypes.byref(h)) == 4
     A = bsp.BitmapMatrix(Wd)
     X = torch.zeros((4, 128), dtype=torch.float16, device=DEV)
