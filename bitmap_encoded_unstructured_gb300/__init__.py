@@ -52,6 +52,7 @@ SIGNATURES = {
     "bsp_check": (C.c_int, [_P, _P]),
     "bsp_import": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, C.c_uint64, _P, C.POINTER(_P)]),
     "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
+    "bsp_set_deterministic": (C.c_int, [_P, C.c_int]),
 }
 
 
@@ -145,6 +146,10 @@ def bsp_info(h: int) -> bsp_info_t:
     o = bsp_info_t()
     _check("bsp_info", lib().bsp_info(h, C.byref(o)))
     return o
+
+
+def bsp_set_deterministic(h: int, on: bool) -> None:
+    _check("bsp_set_deterministic", lib().bsp_set_deterministic(h, 1 if on else 0))
 
 
 def bsp_decode(h: int, W_out_ptr: int, stream: int = 0) -> None:
@@ -283,6 +288,11 @@ class BitmapMatrix:
     def check(self, stream=None):
         """Synchronise and raise if a kernel on this handle gave up a wait."""
         bsp_check(self.h, _stream(stream))
+
+    def set_deterministic(self, on: bool = True):
+        """Split-K partial sums added in a fixed order (bit-identical fp16
+        outputs from call to call) instead of by atomic adds."""
+        bsp_set_deterministic(self.h, on)
 
     # -- compute
     def _out(self, N, out, dtype):

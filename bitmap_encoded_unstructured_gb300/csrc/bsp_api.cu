@@ -35,6 +35,7 @@ void free_handle(bsp_handle* h)
     cudaFree(h->offsets);
     cudaFree(h->values);
     cudaFree(h->ws);
+    cudaFree(h->ws_det);
     cudaFree(h->counters);
     cudaFree(h->err);
     cudaFree(h->stage_x);
@@ -262,6 +263,24 @@ bsp_status_t bsp_info(bsp_handle_t h, bsp_info_t* o)
     o->bitmaps = h->bitmaps;
     o->offsets = h->offsets;
     o->values = h->values;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on)
+{
+    if (!valid(h) || (on != 0 && on != 1)) return BSP_ERR_INVALID_ARG;
+    if (on && !h->ws_det) {
+        DeviceGuard g(h->device);
+        if (!g.ok) return BSP_ERR_CUDA;
+        const int slots = bsp_decode_split_cap(bsp_problem_of(h));
+        const size_t bytes = (size_t)slots * BSP_DECODE_MAX_N * (size_t)h->M * 4;
+        if (cudaMalloc(&h->ws_det, bytes) != cudaSuccess) {
+            h->ws_det = nullptr;
+            return BSP_ERR_OOM;
+        }
+        h->det_slots = slots;
+    }
+    h->deterministic = on;
     return BSP_OK;
 }
 

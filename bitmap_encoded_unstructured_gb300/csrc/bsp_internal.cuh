@@ -28,6 +28,12 @@ struct bsp_handle {
     // reads and clears its slice); one arrival counter per 64-row strip.
     void* ws;
     uint32_t* counters;
+    // deterministic split-K (bsp_set_deterministic): fp16 partial sums per
+    // split, [det_slots][BSP_DECODE_MAX_N][M] fp32, allocated when first
+    // switched on; det_slots bounds the split count in that mode
+    int deterministic;
+    float* ws_det;
+    int det_slots;
     // device error word: a kernel whose bounded wait gave up stores
     // BSP_ERR_TIMEOUT here; bsp_check reads and clears it
     int* err;
@@ -68,6 +74,10 @@ struct bsp_decode_problem {
     void* ws;
     uint32_t* counters;
     int* err;
+    // deterministic split-K: [det_slots][N][M] fp32 slots, or null (atomic
+    // accumulation into ws)
+    float* ws_det = nullptr;
+    int det_slots = 0;
 };
 
 bsp_decode_problem bsp_problem_of(const bsp_handle* h);
@@ -83,6 +93,9 @@ bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int
 
 // Split-K factor chosen for a problem (exposed for tests and tuning).
 int bsp_decode_splits(const bsp_decode_problem& p, int N);
+// Largest split count the decode kernels choose for a problem at any N
+// (ignoring BSP_SPLITK): the slot count of the deterministic workspace.
+int bsp_decode_split_cap(const bsp_decode_problem& p);
 
 // ---- tcgen05 prefill-path product (spmm_prefill.cu), fp16 only ----
 // X: [N][K] fp16, Y: [N][M] fp16, any N >= 1 (used for N > BSP_DECODE_MAX_N).

@@ -435,6 +435,7 @@ struct Args {
     int64_t KT;       // GT columns of the padded grid
     int splits, per_split;
     void* ws;
+    float* ws_det;      // fp16 deterministic split-K: [splits][N][M] partial sums, else null
     uint32_t* counters;
     int* err;
     void* Y;
@@ -755,6 +756,11 @@ spmm_decode_kernel(const Args a)
     __syncthreads();
 
     Acc* ws = reinterpret_cast<Acc*>(a.ws);
+    // deterministic split-K (fp16): each split stores its partial sums to a
+    // slot of its own and the last CTA adds the slots in split order
+    float* det = nullptr;
+    if constexpr (!I8)
+        if (a.ws_det) det = a.ws_det + (int64_t)blockIdx.x * N * M;
     for (int i = threadIdx.x; i < 64 * NT; i += C::THREADS) {
         const int r = i / NT, n = i % NT;
         Acc sum = Acc(0);
@@ -767,6 +773,8 @@ spmm_decode_kernel(const Args a)
         if (n < N && m < M) {  // rows past M are padding
             if (a.splits == 1)
                 write_out(a.Y, a.mode, (int64_t)n * M + m, sum, a.row_scale ? a.row_scale[m] : 1.0f);
+            else if (det)
+                det[(int64_t)n * M + m] = (float)sum;
             else
                 atomicAdd(ws + (int64_t)n * M + m, sum);
         }
@@ -783,7 +791,17 @@ spmm_decode_kernel(const Args a)
         const int n = i >> 6, r = i & 63;
         const int64_t m = gi * 64 + r;
         if (m >= M) continue;
-        const Acc v = ws_take(ws + (int64_t)n * M + m);
+        Acc v;
+        if constexpr (!I8) {
+            if (det) {
+                v = 0.f;
+                for (int sp = 0; sp < a.splits; ++sp) v += __ldcg(a.ws_det + ((int64_t)sp * N + n) * M + m);
+            } else {
+                v = ws_take(ws + (int64_t)n * M + m);
+            }
+        } else {
+            v = ws_take(ws + (int64_t)n * M + m);
+        }
         write_out(a.Y, a.mode, (int64_t)n * M + m, v, a.row_scale ? a.row_scale[m] : 1.0f);
     }
     if (threadIdx.x == 0) a.counters[gi] = 0u;
@@ -870,6 +888,7 @@ struct GtwArgs {
     int64_t KT;       // GT columns of the padded grid
     int splits, per_split;
     float* ws;
+    float* ws_det;    // deterministic split-K: [splits][N][M] partial sums, else null
     uint32_t* counters;
     int* err;
     __half* Y;
@@ -1171,6 +1190,7 @@ spmm_decode_gtw_kernel(const GtwArgs a)
                 red[(cw * 64 + lane + 32 * h) * NT + n] = acc.v[h][n] + acc.v[h][n + NT];
     }
     __syncthreads();
+    float* det = a.ws_det ? a.ws_det + (int64_t)blockIdx.x * N * M : nullptr;  // deterministic split-K slot
     for (int i = threadIdx.x; i < 64 * NT; i += THREADS) {
         const int r = i / NT, n = i % NT;
         float sum = 0.f;
@@ -1180,6 +1200,8 @@ spmm_decode_gtw_kernel(const GtwArgs a)
         if (n < N && m < M) {  // rows past M are padding
             if (a.splits == 1)
                 a.Y[(int64_t)n * M + m] = __float2half_rn(sum);
+            else if (det)
+                det[(int64_t)n * M + m] = sum;
             else
                 atomicAdd(a.ws + (int64_t)n * M + m, sum);
         }
@@ -1196,7 +1218,13 @@ spmm_decode_gtw_kernel(const GtwArgs a)
         const int n = i >> 6, r = i & 63;
         const int64_t m = gi * 64 + r;
         if (m >= M) continue;
-        a.Y[(int64_t)n * M + m] = __float2half_rn(ws_take(a.ws + (int64_t)n * M + m));
+        float v = 0.f;
+        if (det) {
+            for (int sp = 0; sp < a.splits; ++sp) v += __ldcg(a.ws_det + ((int64_t)sp * N + n) * M + m);
+        } else {
+            v = ws_take(a.ws + (int64_t)n * M + m);
+        }
+        a.Y[(int64_t)n * M + m] = __float2half_rn(v);
     }
     if (threadIdx.x == 0) a.counters[gi] = 0u;
 }
@@ -1205,12 +1233,8 @@ spmm_decode_gtw_kernel(const GtwArgs a)
 // number of CTA waves times (GTs per CTA + a fixed 4) is smallest (ties:
 // fewer CTAs),
 // with at least 2 CW GTs per CTA when the row strip has that many.
-int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
+int gtw_splits_auto(int64_t strips, int64_t KT, int64_t slots)
 {
-    if (const char* e = std::getenv("BSP_SPLITK")) {
-        const int64_t v = std::atol(e);
-        if (v >= 1) return (int)std::min<int64_t>(v, KT);
-    }
     int64_t best = 1, best_cost = INT64_MAX;
     for (int64_t sp = 1; sp <= KT; ++sp) {
         const int64_t per = (KT + sp - 1) / sp;
@@ -1225,6 +1249,34 @@ int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
         }
     }
     return (int)best;
+}
+
+// BSP_SPLITK overrides the choice (tests and tuning)
+int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
+{
+    if (const char* e = std::getenv("BSP_SPLITK")) {
+        const int64_t v = std::atol(e);
+        if (v >= 1) return (int)std::min<int64_t>(v, KT);
+    }
+    return gtw_splits_auto(strips, KT, slots);
+}
+
+// CTAs of the GT-per-warp kernel resident at once on the whole GPU
+int64_t gtw_slots(const bsp_decode_problem& p, int NT)
+{
+    uint32_t stage_bytes = 0, val_off = 0;
+    gtw::stage_geometry(NT, std::min<uint32_t>(p.max_gt_nnz, 4096u), stage_bytes, val_off);
+    const size_t smem = gtw::smem_bytes(stage_bytes);
+    int per_sm = (int)std::min<size_t>((size_t)BSP_GTW_MINB, (size_t)(227 * 1024) / (smem + 1024));
+    if (per_sm < 1) per_sm = 1;
+    return (int64_t)p.num_sms * per_sm;
+}
+
+// In deterministic mode the split count is bounded by the handle's slots.
+int clamp_det(const bsp_decode_problem& p, int splits)
+{
+    if (p.ws_det && splits > p.det_slots) return p.det_slots;
+    return splits;
 }
 
 template <int NT, bool SKIP>
@@ -1245,9 +1297,7 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     stage_geometry(NT, std::min<uint32_t>(p.max_gt_nnz, 4096u), stage_bytes, val_off);
     const size_t smem = smem_bytes(stage_bytes);
     const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
-    int per_sm = (int)std::min<size_t>((size_t)BSP_GTW_MINB, (size_t)(227 * 1024) / (smem + 1024));
-    if (per_sm < 1) per_sm = 1;
-    const int splits0 = gtw_splits(strips, KT, (int64_t)p.num_sms * per_sm);
+    const int splits0 = clamp_det(p, gtw_splits(strips, KT, gtw_slots(p, NT)));
     const int per_split = (int)((KT + splits0 - 1) / splits0);
     const int splits = (int)((KT + per_split - 1) / per_split);
     GtwArgs a;
@@ -1262,6 +1312,7 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     a.splits = splits;
     a.per_split = per_split;
     a.ws = (float*)p.ws;
+    a.ws_det = splits > 1 ? p.ws_det : nullptr;
     a.counters = p.counters;
     a.err = p.err;
     a.Y = (__half*)Y;
@@ -1291,7 +1342,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
         attr_done[p.device] = true;
     }
     const int64_t KT = p.Kp / 64;
-    int splits = bsp_decode_splits(p, N);
+    int splits = clamp_det(p, bsp_decode_splits(p, N));
     const int per_split = (int)((KT + splits - 1) / splits);
     splits = (int)((KT + per_split - 1) / per_split);  // drop empty splits
     Args a;
@@ -1306,6 +1357,7 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
     a.splits = splits;
     a.per_split = per_split;
     a.ws = p.ws;
+    a.ws_det = (!I8 && splits > 1) ? p.ws_det : nullptr;
     a.counters = p.counters;
     a.err = p.err;
     a.Y = Y;
@@ -1336,14 +1388,16 @@ bsp_status_t dispatch_nt(const bsp_decode_problem& p, const void* X, int N, void
 
 }  // namespace
 
-int bsp_decode_splits(const bsp_decode_problem& p, int N)
+namespace {
+
+int team_splits(const bsp_decode_problem& p, bool env)
 {
-    (void)N;
     const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
     // each team run must fit kMaxRun GTs
     const int64_t min_splits = (KT + (int64_t)kMaxRun * kTeams - 1) / ((int64_t)kMaxRun * kTeams);
     int64_t splits;
-    if (const char* e = std::getenv("BSP_SPLITK")) {
+    const char* e = env ? std::getenv("BSP_SPLITK") : nullptr;
+    if (e) {
         splits = std::atol(e);
     } else {
         // about 8 GTs per team run, and at least ~2 CTAs per SM
@@ -1355,6 +1409,24 @@ int bsp_decode_splits(const bsp_decode_problem& p, int N)
     if (splits < min_splits) splits = min_splits;
     if (splits < 1) splits = 1;
     return (int)splits;
+}
+
+}  // namespace
+
+int bsp_decode_splits(const bsp_decode_problem& p, int N)
+{
+    (void)N;
+    return team_splits(p, true);
+}
+
+int bsp_decode_split_cap(const bsp_decode_problem& p)
+{
+    const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
+    int cap = team_splits(p, false);
+    for (int nt = 1; nt <= 2; ++nt) cap = std::max(cap, gtw_splits_auto(strips, KT, gtw_slots(p, nt)));
+    // cap >= the team kernel's floor (runs of at most kMaxRun GTs), so a
+    // count clamped to it still satisfies that floor
+    return cap;
 }
 
 bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int N, void* Y,
@@ -1394,6 +1466,8 @@ bsp_decode_problem bsp_problem_of(const bsp_handle* h)
     p.device = h->device;
     p.num_sms = h->num_sms;
     p.ws = h->ws;
+    p.ws_det = h->deterministic ? h->ws_det : nullptr;
+    p.det_slots = h->det_slots;
     p.counters = h->counters;
     p.err = h->err;
     return p;

@@ -132,6 +132,25 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void *X, int64_t N, void *Y,
                       bsp_stream_t stream);
 
 /*
+ * Deterministic split-K (on = 1) or the default atomic one (on = 0).
+ * The decode kernels split the K range of a row strip over several CTAs.
+ * By default the fp16 partial sums meet through fp32 atomic adds, so the
+ * rounding order, and with it the last bit of an fp16 output, may change
+ * from call to call.  With on = 1 each split stores its partial sums to a
+ * slot of its own and the last CTA of the strip adds the slots in split
+ * order: the same inputs give bit-identical outputs on every call on the
+ * same GPU model (the split count depends on the SM count).  int8 is
+ * exact either way; the prefill kernel (fp16, N > BSP_DECODE_MAX_N) does
+ * not split K and is deterministic either way.  The first switch-on
+ * allocates the slots (splits x BSP_DECODE_MAX_N x M fp32) on the handle's
+ * device; later calls do not allocate.  Not safe to call while another
+ * thread uses the handle.  BSP_ERR_INVALID_ARG for a bad handle or an `on`
+ * other than 0 or 1; BSP_ERR_OOM if the slots cannot be allocated (the
+ * mode is then unchanged).
+ */
+bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
+
+/*
  * INT8 with per-row dequantisation: Y[n][m] = fp32(acc[n][m]) * row_scale[m],
  * one round-to-nearest int->float conversion and one fp32 multiply.
  *   X device int8 [N][K]; row_scale device fp32 [M]; Y device fp32 [N][M].

@@ -60,5 +60,6 @@ def test_argument_errors_without_gpu():
     assert L.bsp_spmm(None, 16, 1, 16, None) == 1
     assert L.bsp_spmspv(None, 16, 16, None) == 1
     assert L.bsp_destroy(None) == 1
+    assert L.bsp_set_deterministic(None, 1) == 1
     v = ctypes.c_uint64()
     assert L.bsp_storage_bytes(None, ctypes.byref(v)) == 1

@@ -1,0 +1,121 @@
+"""Deterministic split-K: with the handle switched to deterministic mode,
+repeated fp16 products give bit-identical outputs and stay within the fp16
+bound of the oracle; switching back restores the atomic mode."""
+import numpy as np
+import pytest
+import torch
+
+import bitmap_encoded_unstructured_gb300 as bsp
+import oracle
+from bitmap_encoded_unstructured_gb300 import synth
+from helpers import assert_within_bound, to_dev_f16
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+REPEATS = 25
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture
+def splitk(monkeypatch):
+    def set_(s):
+        if s is None:
+            monkeypatch.delenv("BSP_SPLITK", raising=False)
+        else:
+            monkeypatch.setenv("BSP_SPLITK", str(s))
+    yield set_
+    monkeypatch.delenv("BSP_SPLITK", raising=False)
+
+
+def _repeat(fn):
+    outs = [fn().clone() for _ in range(REPEATS)]
+    torch.cuda.synchronize()
+    return outs
+
+
+def _n_distinct(outs):
+    return sum(not torch.equal(outs[0], o) for o in outs[1:])
+
+
+@pytest.mark.parametrize("N", [1, 2, 5, 8, 16])
+@pytest.mark.parametrize("M,K", [(1024, 4096), (330, 1480)])
+@pytest.mark.parametrize("s", [None, 7])
+def test_spmm_deterministic_bitwise(M, K, N, s, splitk):
+    W = synth.weights_f16(M, K, 0.5, "uniform", 3 * M + K + N)
+    X = synth.activations_f16(N, K, 17 * N + K)
+    Yref, S = oracle.spmm_f16(W, X)
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    Xd = to_dev_f16(X, DEV)
+    splitk(s)
+    A.set_deterministic(True)
+    outs = _repeat(lambda: A.spmm(Xd))
+    A.check()
+    assert _n_distinct(outs) == 0, f"{M}x{K} N={N} splitk={s}: outputs differ between calls"
+    assert_within_bound(outs[0].cpu().numpy(), Yref, S, f"deterministic {M}x{K} N={N} splitk={s}")
+    # back to atomic accumulation: still within the bound (the atomic
+    # workspace was not disturbed by the deterministic calls)
+    A.set_deterministic(False)
+    assert_within_bound(A.spmm(Xd).cpu().numpy(), Yref, S, f"atomic {M}x{K} N={N} splitk={s}")
+    A.check()
+
+
+def test_split_count_above_the_slots_is_clamped(splitk):
+    M, K, N = 256, 8192, 4
+    W = synth.weights_f16(M, K, 0.6, "uniform", 91)
+    X = synth.activations_f16(N, K, 92)
+    Yref, S = oracle.spmm_f16(W, X)
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    A.set_deterministic(True)
+    splitk(128)  # one GT column per split, more than the slots hold
+    outs = _repeat(lambda: A.spmm(to_dev_f16(X, DEV)))
+    A.check()
+    assert _n_distinct(outs) == 0
+    assert_within_bound(outs[0].cpu().numpy(), Yref, S, "clamped split count")
+
+
+@pytest.mark.parametrize("t", [0.0, 0.5])
+def test_spmspv_deterministic_bitwise(t, splitk):
+    M, K = 2048, 4096
+    W = synth.weights_f16(M, K, 0.5, "uniform", 41)
+    x = synth.activations_relu_f16(K, 42)
+    Yref, S = oracle.spmspv_threshold_f16(W, x, t)
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    xd = to_dev_f16(x, DEV)
+    A.set_deterministic(True)
+    for s in (None, 9):
+        splitk(s)
+        outs = _repeat(lambda: A.spmspv_threshold(xd, t))
+        A.check()
+        assert _n_distinct(outs) == 0, f"spMspV t={t} splitk={s}"
+        assert_within_bound(outs[0].cpu().numpy().reshape(1, -1), Yref.reshape(1, -1), S.reshape(1, -1),
+                            f"spMspV t={t} splitk={s}")
+
+
+def test_atomic_mode_variation_is_reported():
+    """Not a requirement: how often the default atomic mode changed an fp16
+    output bit over the repeats (printed for the record)."""
+    M, K, N = 1024, 4096, 8
+    W = synth.weights_f16(M, K, 0.5, "uniform", 5)
+    X = to_dev_f16(synth.activations_f16(N, K, 6), DEV)
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    outs = _repeat(lambda: A.spmm(X))
+    A.set_deterministic(True)
+    det = _repeat(lambda: A.spmm(X))
+    print(f"atomic mode: {_n_distinct(outs)} of {REPEATS - 1} repeats differ; "
+          f"deterministic: {_n_distinct(det)}")
+    assert _n_distinct(det) == 0
+
+
+def test_int8_unaffected():
+    W = synth.weights_i8(512, 1024, 0.5, 7)
+    X = synth.activations_i8(8, 1024, 8)
+    Yref = oracle.spmm_i8(W, X)
+    A = bsp.BitmapMatrix(torch.from_numpy(W).to(DEV))
+    A.set_deterministic(True)
+    np.testing.assert_array_equal(A.spmm(torch.from_numpy(X).to(DEV)).cpu().numpy(), Yref)
+    A.check()
