@@ -107,6 +107,22 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Shared-window address, in the CTA of cluster rank `rank`, of this CTA's
+// shared-memory address `saddr` (the same offset).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// 16-byte store to a cluster shared-window address (another CTA's memory).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // Arrive on the mbarrier at the same shared-memory offset as `bar` in the
 // CTA of cluster rank `rank`.  CLUSTER_SCOPE: release at cluster scope (a
 // fence the arriving thread waits for); else the default release

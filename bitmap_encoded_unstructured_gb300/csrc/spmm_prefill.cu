@@ -15,7 +15,8 @@
 // CTA tile: 128 rows of W (two GT row strips) x 256 * NSUB columns of Y
 // (tokens); one GT column (K = 64) per pipeline step, three rings:
 //   C  compressed data  bitmaps + value spans of the two GTs (bulk copies),
-//                       3 stages, producer -> decoders
+//                       the rest of shared memory in stages sized for the
+//                       densest GT (up to SC_MAX), producer -> decoders
 //   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB),
 //                       2 stages, decoders -> MMA
 //   B  X sub-tiles      256 x 64 fp16 each, K-major, SWIZZLE_128B (TMA),
@@ -52,6 +53,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -60,8 +62,6 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;    // BN: columns of one MMA / one TMEM accumulator
 constexpr int A_BYTES = BM * BK * 2;          // 16384
-constexpr int VAL_BYTES = 513 * 16;           // dense GT value span + misalignment
-constexpr int SLOT = 512 + VAL_BYTES;         // bitmaps + values of one GT
 // Decoder warps: 8 (four per GroupTile, eight half row-bytes per lane and
 // step) or 16 (eight per GroupTile, four half row-bytes per lane and step).
 #ifndef BSP_PF_DEC_WARPS
@@ -91,39 +91,53 @@ constexpr int THREADS = WARPS * 32;
 // (cluster rank 0) issues the MMAs, and each CTA's TMEM receives its own
 // 128 rows.  A CTA thus holds and the tensor cores read half of the X
 // tile, which frees shared memory for deeper rings.
+// ring depths (X sub-tiles) of the single-CTA kernel with one 256-column
+// sub-tile, and of the pair kernel
+#ifndef BSP_PF1_SB
+#define BSP_PF1_SB 3
+#endif
 #ifndef BSP_PF2_SB
 #define BSP_PF2_SB 6
 #endif
 #ifndef BSP_PF2_SA
 #define BSP_PF2_SA 3
 #endif
-#ifndef BSP_PF2_SC
-#define BSP_PF2_SC 4
-#endif
+constexpr int SC_MAX = 12;        // barrier slots of the C ring
+constexpr int SMEM_MAX = 227 * 1024;
+
+// One C stage: two GT slots (512 B of bitmaps, then the 16-B chunks that
+// hold the GT's value span), a 16-B header (the value shifts) and the row
+// starts of the two GTs.  The slot is sized for the densest GT of the
+// matrix, so the number of stages that fit follows the density.
+__host__ __device__ constexpr uint32_t c_slot_bytes(uint32_t max_gt_nnz)
+{
+    return (512u + 16u * ((max_gt_nnz + 7u) / 8u + 1u) + 127u) & ~127u;
+}
+__host__ __device__ constexpr uint32_t c_stage_bytes(uint32_t slot)
+{
+    return (2u * slot + 16u + 2u * (uint32_t)RS_BYTES + 127u) & ~127u;
+}
+
 template <int NSUB, bool PAIR>
 struct PCfg {
     static constexpr int BN_CTA = BN * NSUB;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // X rows of a sub-tile held by this CTA
-    // three rings with their own depths
-    static constexpr int SB = PAIR ? BSP_PF2_SB : 4;  // X sub-tiles (TMA)      -> MMA
-    static constexpr int SA = PAIR ? BSP_PF2_SA : 2;  // decoded A tiles        -> MMA
-    static constexpr int SC = PAIR ? BSP_PF2_SC : 3;  // compressed GroupTiles  -> decoders
+    // three rings with their own depths; the C ring takes the rest of the
+    // shared memory, in stages sized at launch
+    static constexpr int SB = PAIR ? BSP_PF2_SB : (NSUB == 1 ? BSP_PF1_SB : 4);  // X sub-tiles (TMA) -> MMA
+    static constexpr int SA = PAIR ? BSP_PF2_SA : 2;                             // decoded A tiles   -> MMA
     static constexpr int B_STAGE = B_ROWS * BK * 2;   // one sub-tile (this CTA's rows) per stage
-    // two GTs, header (value shifts, 16 B), row starts of the two GTs
-    static constexpr int C_HDR = 2 * SLOT;
-    static constexpr int C_RS = C_HDR + 16;
-    static constexpr int C_STAGE = ((C_RS + 2 * RS_BYTES) + 127) & ~127;
     static constexpr int OFF_B = 0;                   // 1024-B aligned regions first
     static constexpr int OFF_A = OFF_B + SB * B_STAGE;
-    static constexpr int OFF_C = OFF_A + SA * A_BYTES;
-    static constexpr int OFF_BAR = OFF_C + SC * C_STAGE;
-    // barriers: c_full[SC] c_empty[SC] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc c_scan[SC] b_peer[SB]
-    static constexpr int NBAR = 3 * SC + 3 * SB + 2 * SA + 1;
+    static constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
+    // barriers: c_full[SC_MAX] c_empty[SC_MAX] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc
+    // c_scan[SC_MAX] b_peer[SB]
+    static constexpr int NBAR = 3 * SC_MAX + 3 * SB + 2 * SA + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_USED = OFF_TMEM + 16;
-    static constexpr int SMEM = SMEM_USED + 1024;    // slack to align the base to 1024 B
+    static constexpr int OFF_C = (OFF_TMEM + 16 + 127) & ~127;
+    static constexpr int C_BYTES = SMEM_MAX - 1024 - OFF_C;  // 1024: slack to align the base to 1024 B
     static constexpr uint32_t TMEM_COLS = 256 * NSUB;
-    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(C_BYTES >= 2 * (int)c_stage_bytes(c_slot_bytes(4096)), "two dense C stages");
     static_assert((B_STAGE % 1024) == 0 && (A_BYTES % 1024) == 0, "swizzle atoms need 1024-B alignment");
 };
 
@@ -177,6 +191,8 @@ struct PrefillArgs {
     int64_t M, N, K;  // logical: Y rows, columns, X row length
     int64_t Mp, KT;   // padded grid: rows (a multiple of 64), GT columns
     int64_t ntiles;   // N tiles of BN * NSUB columns
+    uint32_t c_slot, c_stage;  // C ring geometry (bytes): GT slot, stage
+    int sc;                    // C stages in use, 2..SC_MAX
     int* err;
     uint32_t spin_cap;
 };
@@ -248,12 +264,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int NSUB, bool PAIR>
+// KS: split-K over a cluster of two CTAs on one output tile.  Rank 0 takes
+// the first ceil(KT / 2) GT columns, rank 1 the rest (at least one: the host
+// launches KS only for KT >= 2); each accumulates in its own TMEM, then rank
+// 1 stores its fp32 partial tile into rank 0's rings (idle by then) and
+// rank 0 writes Y = RN(own + partner).
+template <int NSUB, bool PAIR, bool KS>
 __global__ void __launch_bounds__(THREADS, 1)
 spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a)
 {
     using P = PCfg<NSUB, PAIR>;
-    constexpr int SA = P::SA, SB = P::SB, SC = P::SC;
+    static_assert(!KS || (!PAIR && NSUB == 1), "split-K: single-CTA MMAs, one 256-column sub-tile");
+    static_assert(!KS || P::OFF_BAR >= BM * BN * 4, "split-K exchange buffer: the rings, below the barriers");
+    constexpr int SA = P::SA, SB = P::SB;
+    const int SC = a.sc;
+    const uint32_t SLOT = a.c_slot, C_HDR = 2 * SLOT, C_RS = C_HDR + 16;
+    const uint32_t vchunks = (SLOT - 512) / 16;  // value chunks a slot holds
     constexpr uint32_t TMEM_COLS = P::TMEM_COLS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-B alignment of the shared-window offset (the 128-B swizzle atoms)
@@ -263,25 +289,29 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     uint64_t* c_full = reinterpret_cast<uint64_t*>(smem + P::OFF_BAR);
-    uint64_t* c_empty = c_full + SC;
-    uint64_t* b_full = c_empty + SC;
+    uint64_t* c_empty = c_full + SC_MAX;
+    uint64_t* b_full = c_empty + SC_MAX;
     uint64_t* b_empty = b_full + SB;
     uint64_t* a_full = b_empty + SB;
     uint64_t* a_empty = a_full + SA;
     uint64_t* acc_bar = a_empty + SA;
     uint64_t* c_scan = acc_bar + 1;
-    uint64_t* b_peer = c_scan + SC;  // pair leader: the peer's X sub-tile has landed
+    uint64_t* b_peer = c_scan + SC_MAX;  // pair leader: the peer's X sub-tile has landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::OFF_TMEM);
     auto b_stage = [&](int s) { return smem + P::OFF_B + s * P::B_STAGE; };
     auto a_stage = [&](int s) { return smem + P::OFF_A + s * A_BYTES; };
-    auto c_stage = [&](int s) { return smem + P::OFF_C + s * P::C_STAGE; };
+    auto c_stage = [&](int s) { return smem + P::OFF_C + s * a.c_stage; };
 
     const int64_t M = a.M, N = a.N;
-    const uint32_t KT = (uint32_t)a.KT;
-    // linear grid of clusters (one CTA, or a pair: two consecutive M tiles),
-    // N tiles fastest, so that the CTAs streaming one W row strip run at
-    // about the same time and share it in L2
-    const int64_t cl = (int64_t)blockIdx.x / (PAIR ? 2 : 1);
+    const uint32_t KTA = (uint32_t)a.KT;                 // GT columns of the grid (row pitch)
+    const uint32_t krank = KS ? bspx::cluster_ctarank() : 0u;
+    const uint32_t KT0 = KS ? (KTA + 1) / 2 : KTA;
+    const uint32_t k0 = krank ? KT0 : 0u;                // first GT column of this CTA
+    const uint32_t KT = krank ? KTA - KT0 : KT0;         // GT columns of this CTA
+    // linear grid of clusters (one CTA, a pair of consecutive M tiles, or
+    // the two K halves of one tile), N tiles fastest, so that the CTAs
+    // streaming one W row strip run at about the same time and share it in L2
+    const int64_t cl = (int64_t)blockIdx.x / ((PAIR || KS) ? 2 : 1);
     const int64_t mt = (cl / a.ntiles) * (PAIR ? 2 : 1) + (PAIR ? (int64_t)(blockIdx.x & 1) : 0);
     const int64_t n0 = (cl % a.ntiles) * P::BN_CTA;
     const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
@@ -335,7 +365,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
 
     if (warp == 0) {
         // ---------------- C producer: the two GTs of each step, up to SC steps ahead
-        const int64_t ta = strip0 * KT, tb = strip1 * KT;
+        const int64_t ta = strip0 * KTA + k0, tb = strip1 * KTA + k0;
         uint32_t offa = 0, offb = 0;
         uint32_t wbase = 0;
         uint32_t s = 0, ph = 0;  // stage and its phase parity
@@ -357,9 +387,14 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
             if (lane == 0) {
                 uint8_t* st = c_stage(s);
-                uint32_t* hdr = reinterpret_cast<uint32_t*>(st + P::C_HDR);
-                const uint32_t cha = oa0 / 8, nca = (oa1 + 7) / 8 - cha;
-                const uint32_t chb = ob0 / 8, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                uint32_t* hdr = reinterpret_cast<uint32_t*>(st + C_HDR);
+                const uint32_t cha = oa0 / 8, chb = ob0 / 8;
+                uint32_t nca = (oa1 + 7) / 8 - cha, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                if (nca > vchunks || ncb > vchunks) {  // a GT denser than the handle recorded
+                    atomicExch(a.err, (int)BSP_ERR_INTERNAL);
+                    nca = min(nca, vchunks);
+                    ncb = min(ncb, vchunks);
+                }
                 hdr[0] = oa0 - cha * 8;
                 hdr[1] = ob0 - chb * 8;
                 uint32_t bytes = 512 + nca * 16;
@@ -393,7 +428,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             if (lane == 0) {
                 const uint32_t kx = i / NSUB, u = i % NSUB;
                 bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
-                tma_load_2d(b_stage(s), &tmX, (int)(kx * BK), (int)(n0 + u * BN + rank * P::B_ROWS), b_full + s);
+                tma_load_2d(b_stage(s), &tmX, (int)((k0 + kx) * BK), (int)(n0 + u * BN + rank * P::B_ROWS),
+                            b_full + s);
             }
             if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
         }
@@ -474,7 +510,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             if (active) {
                 // lane: BTs 2 lane and 2 lane + 1 (GT order = value order)
                 const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(st + gsel * SLOT)[lane];
-                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + P::C_HDR)[gsel];
+                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + C_HDR)[gsel];
                 const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
                 uint32_t incl = c0 + c1;
 #pragma unroll
@@ -483,7 +519,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                     if (lane >= d) incl += o;
                 }
                 const uint32_t base0 = incl - (c0 + c1) + shift;
-                uint4* rs = reinterpret_cast<uint4*>(st + P::C_RS + gsel * RS_BYTES) + 2 * lane;
+                uint4* rs = reinterpret_cast<uint4*>(st + C_RS + gsel * RS_BYTES) + 2 * lane;
                 rs[0] = bspx::row_starts(bb.x, base0);
                 rs[1] = bspx::row_starts(bb.y, base0 + c0);
             }
@@ -527,7 +563,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             const uint8_t* st = c_stage(sc);
             if (active) {
                 const uint8_t* bmb = st + gsel * SLOT;  // bitmap bytes: byte 8 g + r = row r of BT g
-                const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + P::C_RS + gsel * RS_BYTES);
+                const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + C_RS + gsel * RS_BYTES);
                 const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
                 uint8_t* at = a_stage(sa);
 #pragma unroll
@@ -554,8 +590,8 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         }
         // ---------------- epilogue: every decoder warp; warp w reads TMEM lane
         // quadrant w % 4 (the lanes a warp may access), and the DEC_WARPS / 4
-        // groups of four consecutive warps split the columns
-        {
+        // groups of four consecutive warps split the columns (split-K: below)
+        if constexpr (!KS) {
             const bool ok = __all_sync(FULL, bspx::mbar_wait_sleep(acc_bar, 0, cap, kSleepNs));
             if (!ok) {
                 failed = true;
@@ -573,6 +609,63 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                         for (int j = 0; j < 16; ++j) {
                             const int64_t n = n0 + cb + j;
                             if (n < N) a.Y[n * M + m] = __float2half_rn(__uint_as_float(r[j]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    if constexpr (KS) {
+        // ---------------- split-K exchange.  First barrier: every role of
+        // both CTAs is past its rings, so rank 0's rings are free; the
+        // decoder warps (the epilogue threads) have seen their MMAs complete.
+        const bool dec = warp >= DEC0 && warp < BPROD;
+        bool acc_ok = true;
+        if (dec) {
+            acc_ok = __all_sync(FULL, bspx::mbar_wait_sleep(acc_bar, 0, cap, kSleepNs));
+            if (!acc_ok) failed = true;
+        }
+        tc_fence_before();
+        bspx::cluster_sync();
+        // exchange buffer [BN / 4][BM][4] fp32 over the idle rings (X first):
+        // lane-consecutive 16-B chunks
+        float* xbuf = reinterpret_cast<float*>(smem + P::OFF_B);
+        constexpr int COLS = BN / (DEC_WARPS / 4);
+        const int quad = warp & 3, cg = (warp - DEC0) >> 2;
+        const int trow = 32 * quad + lane;
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * quad) << 16);
+        if (dec && krank == 1 && acc_ok) {
+            tc_fence_after();
+            const uint32_t remote = bspx::mapa_shared(bspx::smem_u32(xbuf), 0);
+#pragma unroll 1
+            for (int cb = cg * COLS; cb < (cg + 1) * COLS; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + (uint32_t)cb, r);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    bspx::st_cluster_v4(remote + (uint32_t)((((cb + j) >> 2) * BM + trow) * 16), r[j], r[j + 1],
+                                        r[j + 2], r[j + 3]);
+            }
+        }
+        // second barrier: the partner's partial tile is in rank 0's memory
+        bspx::cluster_sync();
+        if (dec && krank == 0 && acc_ok) {
+            tc_fence_after();
+            const int64_t m = mt * BM + trow;
+#pragma unroll 1
+            for (int cb = cg * COLS; cb < (cg + 1) * COLS; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + (uint32_t)cb, r);
+                if (m < M) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 q = *reinterpret_cast<const float4*>(xbuf + (((cb + j) >> 2) * BM + trow) * 4);
+                        const float pv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int64_t n = n0 + cb + j + e;
+                            if (n < N) a.Y[n * M + m] = __float2half_rn(__uint_as_float(r[j + e]) + pv[e]);
                         }
                     }
                 }
@@ -616,37 +709,44 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 
 namespace {
 
-template <int NSUB, bool PAIR>
-bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64_t M, int64_t N, int device,
-                            cudaStream_t s)
+template <int NSUB, bool PAIR, bool KS>
+bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64_t M, int64_t N,
+                            uint32_t max_gt_nnz, int device, cudaStream_t s)
 {
     using P = PCfg<NSUB, PAIR>;
     static bool attr_done[64] = {};
     if (!attr_done[device]) {
-        const cudaError_t e = cudaFuncSetAttribute(spmm_prefill_kernel<NSUB, PAIR>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+        const cudaError_t e = cudaFuncSetAttribute(spmm_prefill_kernel<NSUB, PAIR, KS>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
         if (e != cudaSuccess) {
             if (std::getenv("BSP_DEBUG"))
-                std::fprintf(stderr, "spmm_prefill_kernel<%d, %d> attribute: %s\n", NSUB, (int)PAIR,
+                std::fprintf(stderr, "spmm_prefill_kernel<%d, %d, %d> attribute: %s\n", NSUB, (int)PAIR, (int)KS,
                              cudaGetErrorString(e));
             return BSP_ERR_CUDA;
         }
         attr_done[device] = true;
     }
+    if (KS && a0.KT < 2) return BSP_ERR_INTERNAL;  // rank 1 would have no GT column
     const int64_t bn_cta = (int64_t)BN * NSUB;
     const int64_t ntiles = (N + bn_cta - 1) / bn_cta;
-    const int64_t ctas = ntiles * ((M + BM - 1) / BM);
+    const int64_t ctas = ntiles * ((M + BM - 1) / BM) * (KS ? 2 : 1);
     if (ctas > 0x7FFFFFFF) return BSP_ERR_INVALID_ARG;
     PrefillArgs a = a0;
     a.ntiles = ntiles;
+    // C ring: as many stages as fit, each sized for the densest GT
+    a.c_slot = c_slot_bytes(std::min<uint32_t>(max_gt_nnz, 4096u));
+    a.c_stage = c_stage_bytes(a.c_slot);
+    a.sc = std::min<int>(SC_MAX, P::C_BYTES / (int)a.c_stage);
+    if (const char* e = std::getenv("BSP_PF_SC")) a.sc = std::max(2, std::min(a.sc, std::atoi(e)));  // tuning
+    const int smem = P::OFF_C + a.sc * (int)a.c_stage + 1024;
     dim3 grid((unsigned)ctas, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = P::SMEM;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    if (PAIR) {  // consecutive 128-row tiles form a cluster of two
+    if (PAIR || KS) {  // two consecutive CTAs form a cluster: two 128-row tiles, or two K halves
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -654,13 +754,14 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, spmm_prefill_kernel<NSUB, PAIR>, map, a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, spmm_prefill_kernel<NSUB, PAIR, KS>, map, a);
     if (e != cudaSuccess) {
         if (std::getenv("BSP_DEBUG")) {
             int nc = -1;
-            const cudaError_t oe = cudaOccupancyMaxActiveClusters(&nc, spmm_prefill_kernel<NSUB, PAIR>, &cfg);
-            std::fprintf(stderr, "spmm_prefill_kernel<%d, %d> launch grid (%u, %u) smem %d: %s; max active clusters %d (%s)\n",
-                         NSUB, (int)PAIR, grid.x, grid.y, P::SMEM, cudaGetErrorString(e), nc, cudaGetErrorString(oe));
+            const cudaError_t oe = cudaOccupancyMaxActiveClusters(&nc, spmm_prefill_kernel<NSUB, PAIR, KS>, &cfg);
+            std::fprintf(stderr, "spmm_prefill_kernel<%d, %d, %d> launch grid (%u, %u) smem %d: %s; max active clusters %d (%s)\n",
+                         NSUB, (int)PAIR, (int)KS, grid.x, grid.y, smem, cudaGetErrorString(e), nc,
+                         cudaGetErrorString(oe));
         }
         return BSP_ERR_CUDA;
     }
@@ -668,6 +769,20 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
 }
 
 }  // namespace
+
+// Split K over two CTAs (N <= 256: one tile column) when that shortens the
+// critical path: CTA waves times GT columns per CTA, plus a fixed cost per
+// CTA (start, epilogue; about 4 GT columns) and the exchange (about 2).
+// BSP_PF_KSPLIT=0/1 forces the choice (tests), for KT >= 2.
+static bool prefill_split_k(int64_t tiles, int64_t KT, int num_sms)
+{
+    if (KT < 2) return false;
+    if (const char* e = std::getenv("BSP_PF_KSPLIT")) return e[0] == '1';
+    const int64_t slots = num_sms > 0 ? num_sms : 1;  // one CTA per SM (shared memory)
+    const int64_t one = ((tiles + slots - 1) / slots) * (KT + 4);
+    const int64_t two = ((2 * tiles + slots - 1) / slots) * ((KT + 1) / 2 + 6);
+    return two < one;
+}
 
 bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
 {
@@ -709,8 +824,10 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
     // one 256-column sub-tile per CTA for N <= 256, two (512 columns) above
     if (N > BN)
-        return pair ? launch_prefill<2, true>(map, a, p.Mp, N, p.device, s)
-                    : launch_prefill<2, false>(map, a, p.Mp, N, p.device, s);
-    return pair ? launch_prefill<1, true>(map, a, p.Mp, N, p.device, s)
-                : launch_prefill<1, false>(map, a, p.Mp, N, p.device, s);
+        return pair ? launch_prefill<2, true, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s)
+                    : launch_prefill<2, false, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+    if (pair) return launch_prefill<1, true, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+    if (prefill_split_k(p.Mp / BM + (p.Mp % BM ? 1 : 0), a.KT, p.num_sms))
+        return launch_prefill<1, false, true>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+    return launch_prefill<1, false, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
 }

@@ -58,6 +58,32 @@ def test_prefill_cta_pairs(M, K, N, monkeypatch):
     assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(128, 128, 32),     # KT = 2: one GT column per CTA of the cluster
+                                   (192, 320, 17),     # KT = 5: 3 + 2; half tile
+                                   (130, 136, 256),    # ragged M and K (KT = 3 over the padded grid)
+                                   (768, 640, 256),
+                                   (1024, 1024, 100)])
+def test_prefill_split_k(M, K, N, monkeypatch):
+    """Split-K over a cluster of two CTAs (rank 1's partial tile added in
+    rank 0's shared memory) matches the oracle, forced on and forced off."""
+    W = synth.weights_f16(M, K, 0.5, "uniform", 370 + M + K + N)
+    X = synth.activations_f16(N, K, 371 + N)
+    Yref, S = oracle.spmm_f16(W, X)
+    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    assert_within_bound(_run(W, X), Yref, S, f"split-K prefill {M}x{K} N={N}")
+    monkeypatch.setenv("BSP_PF_KSPLIT", "0")
+    assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
+
+
+def test_prefill_split_k_small_integers_exact(monkeypatch):
+    """Both partial sums and their sum are small integers: exact."""
+    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    W = synth.small_int_f16((256, 256), -8, 8, seed=381, sparsity=0.5)
+    X = synth.small_int_f16((40, 256), -8, 8, seed=382)
+    Yref, _ = oracle.spmm_f16(W, X)
+    np.testing.assert_array_equal(_run(W, X).astype(np.float64), Yref)
+
+
 def test_prefill_small_integers_exact():
     """Every partial sum is a small integer: one correct fp16 result."""
     W = synth.small_int_f16((256, 256), -8, 8, seed=311, sparsity=0.5)
