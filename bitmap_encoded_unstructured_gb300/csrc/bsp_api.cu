@@ -81,6 +81,18 @@ bool shape_ok(bsp_dtype_t dtype, int64_t M, int64_t K)
     return (K % (dtype == BSP_INT8 ? 16 : 8)) == 0;
 }
 
+// Smallest fp16 N (up to BSP_DECODE_MAX_N) that runs the tcgen05 narrow
+// kernel instead of the CUDA-core decode kernels.  BSP_NARROW_MIN_N
+// overrides it (17 or more: never).
+#ifndef BSP_NARROW_MIN_N_DEFAULT
+#define BSP_NARROW_MIN_N_DEFAULT 4
+#endif
+int64_t narrow_min_n()
+{
+    if (const char* e = std::getenv("BSP_NARROW_MIN_N")) return std::atol(e);
+    return BSP_NARROW_MIN_N_DEFAULT;
+}
+
 bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
 {
     bsp_handle* h = new (std::nothrow) bsp_handle{};
@@ -158,8 +170,11 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_str
     if (!g.ok) return BSP_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
-    if (N <= BSP_DECODE_MAX_N)
+    if (N <= BSP_DECODE_MAX_N) {
+        if (h->dtype == BSP_FP16 && N >= narrow_min_n())
+            return bsp_run_spmm_narrow(bsp_problem_of(h), X, N, Y, s);
         return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, mode, nullptr, false, s);
+    }
     // Larger N, fp16: the tcgen05 prefill kernel.
     if (h->dtype == BSP_FP16) return bsp_run_spmm_prefill(bsp_problem_of(h), X, N, Y, s);
     // Larger N, int8 (no int8 tensor-core path): the decode kernel over column blocks of 16 tokens.

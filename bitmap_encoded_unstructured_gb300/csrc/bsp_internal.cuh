@@ -78,6 +78,7 @@ struct bsp_decode_problem {
     // accumulation into ws)
     float* ws_det = nullptr;
     int det_slots = 0;
+    uint64_t values_bytes = 0;  // bytes allocated for values (0: unknown)
 };
 
 bsp_decode_problem bsp_problem_of(const bsp_handle* h);
@@ -93,7 +94,7 @@ bsp_status_t bsp_run_spmm_decode(const bsp_decode_problem& p, const void* X, int
 
 // Split-K factor chosen for a problem (exposed for tests and tuning).
 int bsp_decode_splits(const bsp_decode_problem& p, int N);
-// Largest split count the decode kernels choose for a problem at any N
+// Largest split count the decode kernels (and the narrow kernel) choose for a problem at any N
 // (ignoring BSP_SPLITK): the slot count of the deterministic workspace.
 int bsp_decode_split_cap(const bsp_decode_problem& p);
 
@@ -101,3 +102,14 @@ int bsp_decode_split_cap(const bsp_decode_problem& p);
 // X: [N][K] fp16, Y: [N][M] fp16, any N >= 1 (used for N > BSP_DECODE_MAX_N).
 bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                   cudaStream_t s);
+
+// ---- tcgen05 narrow kernel (spmm_prefill.cu), fp16, 1 <= N <= 16 ----
+// One 16-column MMA tile per CTA, split-K over the workspace, counters and
+// deterministic slots of the decode problem (same invariants as the decode
+// kernels: the workspace and counters are zero between calls).
+bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
+                                 cudaStream_t s);
+// Its split count (BSP_NARROW_SPLITK overrides; clamped to the deterministic
+// slots when those are in use), and the automatic choice alone.
+int bsp_narrow_splits(const bsp_decode_problem& p);
+int bsp_narrow_splits_auto(const bsp_decode_problem& p);

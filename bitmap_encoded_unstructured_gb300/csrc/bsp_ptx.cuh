@@ -101,9 +101,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// Every thread of every CTA of the cluster arrives (release) and waits (acquire).
+// Every thread of every CTA of the cluster arrives (release) and waits
+// (acquire).  The .aligned forms need the whole warp to execute them
+// together, and the compiler does not reconverge a warp before inline asm:
+// a warp that comes from a per-lane polling loop (bounded mbarrier waits)
+// may still be split, and its parts would then arrive in different phases
+// of the barrier.  __syncwarp() reconverges it first.
 __device__ __forceinline__ void cluster_sync()
 {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 

@@ -1424,6 +1424,7 @@ int bsp_decode_split_cap(const bsp_decode_problem& p)
     const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
     int cap = team_splits(p, false);
     for (int nt = 1; nt <= 2; ++nt) cap = std::max(cap, gtw_splits_auto(strips, KT, gtw_slots(p, nt)));
+    cap = std::max(cap, bsp_narrow_splits_auto(p));
     // cap >= the team kernel's floor (runs of at most kMaxRun GTs), so a
     // count clamped to it still satisfies that floor
     return cap;
@@ -1468,6 +1469,7 @@ bsp_decode_problem bsp_problem_of(const bsp_handle* h)
     p.ws = h->ws;
     p.ws_det = h->deterministic ? h->ws_det : nullptr;
     p.det_slots = h->det_slots;
+    p.values_bytes = h->values_alloc;
     p.counters = h->counters;
     p.err = h->err;
     return p;

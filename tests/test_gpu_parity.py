@@ -30,14 +30,26 @@ def _need_gpu():
 
 @pytest.fixture
 def splitk(monkeypatch):
-    """Force the split-K factor of the decode kernel for one test."""
+    """Force the split-K factor of the decode and narrow kernels for one test."""
     def set_(v):
         if v is None:
             monkeypatch.delenv("BSP_SPLITK", raising=False)
+            monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
         else:
             monkeypatch.setenv("BSP_SPLITK", str(v))
+            monkeypatch.setenv("BSP_NARROW_SPLITK", str(v))
     yield set_
     monkeypatch.delenv("BSP_SPLITK", raising=False)
+    monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+
+
+@pytest.fixture(params=["cuda_cores", "tcgen05_narrow"])
+def path(request, monkeypatch):
+    """fp16 N <= 16 on the CUDA-core decode kernels, or on the tcgen05
+    narrow kernel (every N forced onto it)."""
+    monkeypatch.setenv("BSP_NARROW_MIN_N", "17" if request.param == "cuda_cores" else "1")
+    yield request.param
+    monkeypatch.delenv("BSP_NARROW_MIN_N", raising=False)
 
 
 def _encode(W):
@@ -116,7 +128,7 @@ def test_spmm_tiny_config(N):
 
 
 @pytest.mark.parametrize("N", list(range(1, 17)))
-def test_spmm_every_n_ragged(N, splitk):
+def test_spmm_every_n_ragged(N, splitk, path):
     """Every N in 1..16 (padded register tiles), several tiles, odd split."""
     W = synth.weights_f16(384, 1472, 0.5, "uniform", 77)   # K/64 = 23 GT columns
     X = synth.activations_f16(N, 1472, 78 + N)
@@ -125,11 +137,11 @@ def test_spmm_every_n_ragged(N, splitk):
     for s in (1, 3, None):
         splitk(s)
         Y = A.spmm(to_dev_f16(X, DEV)).cpu().numpy()
-        assert_within_bound(Y, Yref, S, f"N={N} splitk={s}")
+        assert_within_bound(Y, Yref, S, f"{path} N={N} splitk={s}")
 
 
 @pytest.mark.parametrize("s", [0.3, 0.4, 0.5, 0.6, 0.7])
-def test_spmm_sparsity_sweep_small(s):
+def test_spmm_sparsity_sweep_small(s, path):
     W = synth.weights_f16(512, 1024, s, "uniform", synth.seed_for(3, int(s * 10)))
     X = synth.activations_f16(16, 1024, 5)
     Yref, S = oracle.spmm_f16(W, X)
@@ -139,7 +151,7 @@ def test_spmm_sparsity_sweep_small(s):
 
 
 @pytest.mark.parametrize("N", [1, 3, 16])
-def test_spmm_small_integers_exact(N, splitk):
+def test_spmm_small_integers_exact(N, splitk, path):
     """|w|,|x| <= 8, K = 256: every partial sum is an exact integer, so the
     fp16 output has exactly one correct value, in any summation order."""
     W = synth.small_int_f16((320, 256), -8, 8, seed=41, sparsity=0.5)
@@ -163,7 +175,7 @@ def test_spmm_permutation_exact():
     np.testing.assert_array_equal(Y.view(np.uint16), X[:, perm])
 
 
-def test_spmm_all_zero_weight():
+def test_spmm_all_zero_weight(path):
     W = np.zeros((128, 256), dtype=np.uint16)
     X = synth.activations_f16(4, 256, 1)
     Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
@@ -184,12 +196,14 @@ def test_spmm_dense_weight_vs_library():
 def test_spmm_large_n_column_blocks():
     W = synth.weights_f16(256, 512, 0.5, "uniform", 19)
     X = synth.activations_f16(40, 512, 20)
-    Y = _encode(W).spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    A = _encode(W)
+    Y = A.spmm(to_dev_f16(X, DEV)).cpu().numpy()
+    A.check()
     Yref, S = oracle.spmm_f16(W, X)
     assert_within_bound(Y, Yref, S, "N=40")
 
 
-def test_spmm_guard_bands():
+def test_spmm_guard_bands(path):
     """Canaries around Y are untouched; only Y[N][M] is written."""
     W = synth.weights_f16(192, 256, 0.5, "uniform", 23)
     X = synth.activations_f16(5, 256, 24)

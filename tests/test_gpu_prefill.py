@@ -75,6 +75,23 @@ def test_prefill_split_k(M, K, N, monkeypatch):
     assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(256, 512, 40), (1024, 2048, 256)])
+def test_prefill_split_k_repeated(M, K, N, monkeypatch):
+    """Twenty calls in a row (the cluster barriers of the exchange run
+    every time): every result within the bound and all bitwise equal."""
+    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    W = synth.weights_f16(M, K, 0.5, "uniform", 390 + M)
+    X = synth.activations_f16(N, K, 391)
+    Yref, S = oracle.spmm_f16(W, X)
+    A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
+    Xd = to_dev_f16(X, DEV)
+    outs = [A.spmm(Xd).clone() for _ in range(20)]
+    A.check()
+    for i, Y in enumerate(outs):
+        assert torch.equal(Y, outs[0]), f"call {i} differs"
+    assert_within_bound(outs[0].cpu().numpy(), Yref, S, f"split-K repeated {M}x{K} N={N}")
+
+
 def test_prefill_split_k_small_integers_exact(monkeypatch):
     """Both partial sums and their sum are small integers: exact."""
     monkeypatch.setenv("BSP_PF_KSPLIT", "1")

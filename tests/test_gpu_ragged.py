@@ -25,10 +25,13 @@ def splitk(monkeypatch):
     def set_(s):
         if s is None:
             monkeypatch.delenv("BSP_SPLITK", raising=False)
+            monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
         else:
             monkeypatch.setenv("BSP_SPLITK", str(s))
+            monkeypatch.setenv("BSP_NARROW_SPLITK", str(s))
     yield set_
     monkeypatch.delenv("BSP_SPLITK", raising=False)
+    monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
 
 
 def _encode(W):
