@@ -53,6 +53,14 @@ SIGNATURES = {
     "bsp_import": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, C.c_uint64, _P, C.POINTER(_P)]),
     "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
     "bsp_set_deterministic": (C.c_int, [_P, C.c_int]),
+    "bsp_union_encode": (C.c_int, [_P, C.c_int, _I64, _I64, _P, C.POINTER(_P)]),
+    "bsp_union_destroy": (C.c_int, [_P]),
+    "bsp_union_spmm": (C.c_int, [_P, _P, _I64, _P, _P]),
+    "bsp_union_storage_bytes": (C.c_int, [_P, C.POINTER(C.c_uint64)]),
+    "bsp_union_info": (C.c_int, [_P, _P]),
+    "bsp_union_export": (C.c_int, [_P, _P, _P, _P, _P]),
+    "bsp_union_decode": (C.c_int, [_P, _P, _P]),
+    "bsp_union_check": (C.c_int, [_P, _P]),
 }
 
 
@@ -61,6 +69,14 @@ class bsp_info_t(C.Structure):
                 ("gt_m", C.c_int32), ("gt_k", C.c_int32), ("device", C.c_int32),
                 ("NGT", C.c_int64), ("NBT", C.c_int64), ("NNZ", C.c_uint64),
                 ("bitmaps", C.c_void_p), ("offsets", C.c_void_p), ("values", C.c_void_p)]
+
+
+class bsp_union_info_t(C.Structure):
+    _fields_ = [("M", C.c_int64), ("K", C.c_int64), ("bits", C.c_int32), ("lt", C.c_int32),
+                ("areas_r", C.c_int32), ("areas_c", C.c_int32), ("device", C.c_int32),
+                ("NLT", C.c_int64), ("nnz", C.c_uint64), ("total_values", C.c_uint64),
+                ("value_bytes", C.c_uint64), ("masks", C.c_void_p), ("offsets", C.c_void_p),
+                ("values", C.c_void_p)]
 
 
 class BspError(RuntimeError):
@@ -181,6 +197,44 @@ def bsp_spmm_noalloc(bitmaps_ptr: int, offsets_ptr: int, values_ptr: int, dtype:
 
 
 # ---------------------------------------------------------------- tensor layer
+
+def bsp_union_encode(W_ptr: int, bits: int, M: int, K: int, stream: int = 0) -> int:
+    h = C.c_void_p()
+    _check("bsp_union_encode", lib().bsp_union_encode(W_ptr, bits, M, K, stream, C.byref(h)))
+    return h.value
+
+
+def bsp_union_destroy(h: int) -> None:
+    _check("bsp_union_destroy", lib().bsp_union_destroy(h))
+
+
+def bsp_union_spmm(h: int, X_ptr: int, N: int, Y_ptr: int, stream: int = 0) -> None:
+    _check("bsp_union_spmm", lib().bsp_union_spmm(h, X_ptr, N, Y_ptr, stream))
+
+
+def bsp_union_storage_bytes(h: int) -> int:
+    v = C.c_uint64()
+    _check("bsp_union_storage_bytes", lib().bsp_union_storage_bytes(h, C.byref(v)))
+    return v.value
+
+
+def bsp_union_info(h: int) -> bsp_union_info_t:
+    o = bsp_union_info_t()
+    _check("bsp_union_info", lib().bsp_union_info(h, C.byref(o)))
+    return o
+
+
+def bsp_union_export(h: int, masks_ptr, offsets_ptr, values_ptr, stream: int = 0) -> None:
+    _check("bsp_union_export", lib().bsp_union_export(h, masks_ptr, offsets_ptr, values_ptr, stream))
+
+
+def bsp_union_decode(h: int, W_out_ptr: int, stream: int = 0) -> None:
+    _check("bsp_union_decode", lib().bsp_union_decode(h, W_out_ptr, stream))
+
+
+def bsp_union_check(h: int, stream: int = 0) -> None:
+    _check("bsp_union_check", lib().bsp_union_check(h, stream))
+
 
 def _stream(stream):
     import torch
@@ -340,3 +394,65 @@ class BitmapMatrix:
                                                     device=self.device)
         bsp_decode(self.h, W.data_ptr(), _stream(stream))
         return W
+
+
+class UnionMatrix:
+    """An integer weight W (M x K) in the IE-BME union-bitmap format on one
+    GPU: ``UnionMatrix(W, bits)`` encodes a CUDA int8 tensor whose values lie
+    in the signed ``bits``-bit range (4 or 8); ``spmm`` multiplies by an int8
+    activation block X [N][K] into int32 Y [N][M]."""
+
+    def __init__(self, W, bits: int, stream=None):
+        import torch
+        if W.dtype != torch.int8 or not W.is_cuda or W.dim() != 2:
+            raise TypeError("W must be a 2-D int8 CUDA tensor")
+        W = W.contiguous()
+        self.M, self.K = int(W.shape[0]), int(W.shape[1])
+        self.bits = int(bits)
+        self.device = W.device
+        self.h = bsp_union_encode(W.data_ptr(), self.bits, self.M, self.K, _stream(stream))
+
+    def close(self):
+        if getattr(self, "h", None):
+            bsp_union_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def storage_bytes(self) -> int:
+        return bsp_union_storage_bytes(self.h)
+
+    def info(self) -> dict:
+        o = bsp_union_info(self.h)
+        return {f: getattr(o, f) for f, _ in bsp_union_info_t._fields_}
+
+    def arrays(self, stream=None):
+        """Copies of (masks int64 [NLT * 16], offsets int32 [NLT + 1], values uint8 [value_bytes])."""
+        import torch
+        o = bsp_union_info(self.h)
+        masks = torch.empty(o.NLT * 16, dtype=torch.int64, device=self.device)
+        offsets = torch.empty(o.NLT + 1, dtype=torch.int32, device=self.device)
+        values = torch.empty(o.value_bytes, dtype=torch.uint8, device=self.device)
+        bsp_union_export(self.h, masks.data_ptr(), offsets.data_ptr(), values.data_ptr() if o.value_bytes else None,
+                         _stream(stream))
+        return masks, offsets, values
+
+    def decode(self, stream=None):
+        import torch
+        W = torch.empty((self.M, self.K), dtype=torch.int8, device=self.device)
+        bsp_union_decode(self.h, W.data_ptr(), _stream(stream))
+        return W
+
+    def check(self, stream=None):
+        bsp_union_check(self.h, _stream(stream))
+
+    def spmm(self, X, out=None, stream=None):
+        import torch
+        N = int(X.shape[0])
+        Y = out if out is not None else torch.empty((N, self.M), dtype=torch.int32, device=self.device)
+        bsp_union_spmm(self.h, X.data_ptr(), N, Y.data_ptr(), _stream(stream))
+        return Y

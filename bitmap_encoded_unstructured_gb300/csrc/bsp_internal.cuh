@@ -53,6 +53,10 @@ enum bsp_out_mode { BSP_OUT_F16 = 0, BSP_OUT_I32 = 1, BSP_OUT_F32_SCALED = 2 };
 // ---- encoder / decoder (encode.cu) ----
 bsp_status_t bsp_run_encode(bsp_handle* h, const void* W, cudaStream_t s);
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s);
+// offsets[0..n] = exclusive prefix sums of counts[0..n-1] (one block, on s);
+// *overflow (device) is set when a sum does not fit uint32.
+bsp_status_t bsp_exclusive_scan_u32(const uint32_t* counts, int64_t n, uint32_t* offsets, int* overflow,
+                                    cudaStream_t s);
 // Check that offsets and bitmaps agree (imported arrays) and set
 // h->max_gt_nnz; synchronises s.
 bsp_status_t bsp_run_validate(bsp_handle* h, cudaStream_t s);

@@ -377,6 +377,13 @@ done:
     return st;
 }
 
+bsp_status_t bsp_exclusive_scan_u32(const uint32_t* counts, int64_t n, uint32_t* offsets, int* overflow,
+                                    cudaStream_t s)
+{
+    enc_scan_kernel<<<1, 1024, 0, s>>>(counts, n, offsets, overflow);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 bsp_status_t bsp_run_decode(const bsp_handle* h, void* W_out, cudaStream_t s)
 {
     const int64_t n_rowbytes = h->Mp * h->Kp / 8;

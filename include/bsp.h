@@ -296,6 +296,89 @@ bsp_status_t bsp_spmm_noalloc(const uint64_t *bitmaps, const uint32_t *offsets,
                               int64_t K, const void *X, int64_t N, void *Y,
                               bsp_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * IE-BME: the low-bit union-bitmap format ("UnionSparse", sections
+ * "IE-BME", "Area Partitioning", "Shared Union Mask", "IE-BME Storage
+ * Layout") and its decode-path product with LSPD decoding (section
+ * "Low-Bit Shared-Memory Parallel Decoding").
+ *
+ * Local tiles (LTs) of 64 x 64 over M and K zero-padded to multiples of 64,
+ * row-major; each LT cut into 2 x 2 areas of 32 x 32 (area a = 2 ra + ca).
+ * Position (i, j) of the 32 x 32 logical grid groups the four values
+ * W[64 ti + 32 ra + i][64 tj + 32 ca + j]; its union-mask bit is 1 iff one
+ * of them is nonzero.  Arrays:
+ *   masks    u64 [NLT * 16]  each LT's mask row-major, leftmost position in
+ *                            the least significant bit (row i = bits
+ *                            32 i .. 32 i + 31)
+ *   offsets  u32 [NLT + 1]   value counts: offsets[t + 1] - offsets[t] = 4 P_t,
+ *                            P_t = active positions of LT t
+ *   values   the four area streams of each LT: value index
+ *            offsets[t] + a P_t + rank (rank = active positions before (i, j)
+ *            in row-major order), zeros kept inside active groups; int8, or
+ *            int4 two per byte (value e in byte e / 2, low nibble first, two's
+ *            complement).
+ * Storage = 4 (NLT + 1) + 128 NLT + ceil(bits * total values / 8) bytes.
+ * ------------------------------------------------------------------------ */
+typedef struct bsp_union *bsp_union_t;
+
+typedef struct {
+    int64_t M, K;
+    int32_t bits;          /* 4 or 8                                          */
+    int32_t lt;            /* local tile side: 64                             */
+    int32_t areas_r, areas_c; /* 2, 2                                         */
+    int32_t device;
+    int64_t NLT;           /* local tiles of the padded grid                  */
+    uint64_t nnz;          /* nonzero weights                                 */
+    uint64_t total_values; /* stored values (offsets[NLT])                    */
+    uint64_t value_bytes;  /* bytes of the packed values                      */
+    const uint64_t *masks;    /* device, [NLT * 16]                           */
+    const uint32_t *offsets;  /* device, [NLT + 1]                            */
+    const uint8_t *values;    /* device, [value_bytes] (+32 B slack)          */
+} bsp_union_info_t;
+
+/*
+ * Encode an integer weight into IE-BME on the device.
+ *   W      device int8 [M][K], values in the signed `bits`-bit range
+ *          (bits 4: -8..7, BSP_ERR_INVALID_ARG otherwise), 16-B aligned.
+ *   M, K   M >= 1, K a multiple of 16 (BSP_ERR_SHAPE otherwise).
+ *   stream ordered on it; synchronises it (sizes the values array), so W may
+ *          be freed on return.
+ *   out    a new handle owning its device arrays and an int32 split-K
+ *          workspace [16][M].
+ */
+bsp_status_t bsp_union_encode(const int8_t *W, int bits, int64_t M, int64_t K,
+                              bsp_stream_t stream, bsp_union_t *out);
+
+/* Free a union handle (synchronises the device first). */
+bsp_status_t bsp_union_destroy(bsp_union_t h);
+
+/*
+ * Y = W * X, exact int32 accumulation ("UnionSparse" W8A8 / W4A4: the int4
+ * activations are int8 values in -8..7).  X device int8 [N][K], Y device
+ * int32 [N][M], both 16-B aligned; N >= 1 (runs in blocks of 16 columns).
+ * The decode-path kernel on CUDA cores (dp4a); calls on one handle must be
+ * serialised on one stream.  A device-side wait that gives up leaves Y
+ * incomplete and is reported by bsp_union_check.
+ */
+bsp_status_t bsp_union_spmm(bsp_union_t h, const int8_t *X, int64_t N, int32_t *Y,
+                            bsp_stream_t stream);
+
+/* Bytes of the three arrays (the closed form above). */
+bsp_status_t bsp_union_storage_bytes(bsp_union_t h, uint64_t *bytes);
+
+/* Shape, counts and device pointers of the arrays. */
+bsp_status_t bsp_union_info(bsp_union_t h, bsp_union_info_t *out);
+
+/* Copies of the arrays (any of the pointers may be NULL), ordered on stream. */
+bsp_status_t bsp_union_export(bsp_union_t h, uint64_t *masks, uint32_t *offsets,
+                              uint8_t *values, bsp_stream_t stream);
+
+/* W back from the arrays into device int8 [M][K] (round trip). */
+bsp_status_t bsp_union_decode(bsp_union_t h, int8_t *W_out, bsp_stream_t stream);
+
+/* Synchronise stream and report (then clear) a device-side wait that gave up. */
+bsp_status_t bsp_union_check(bsp_union_t h, bsp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
