@@ -108,6 +108,28 @@ def weights_i8(M: int, K: int, sparsity: float, seed: int) -> np.ndarray:
     return w
 
 
+def weights_int(M: int, K: int, bits: int, sparsity: float, seed: int, exact: bool = True) -> np.ndarray:
+    """int8 containers of b-bit weights: nonzeros uniform over the signed
+    b-bit range without 0; an exact-count uniform mask, or (exact=False) an
+    i.i.d. Bernoulli(sparsity) one."""
+    g = rng(seed)
+    lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
+    w = g.integers(lo, hi, size=(M, K), dtype=np.int8)   # lo .. hi - 1
+    w[w >= 0] += 1                                       # skip 0: lo .. -1, 1 .. hi
+    if exact:
+        zero = _exact_count_mask(g, M * K, int(round(sparsity * M * K))).reshape(M, K)
+    else:
+        zero = g.random((M, K), dtype=np.float32) < sparsity
+    w[zero] = 0
+    return w
+
+
+def activations_int(N: int, K: int, bits: int, seed: int) -> np.ndarray:
+    """int8 containers of b-bit activations, uniform over the signed range."""
+    g = rng(seed)
+    return g.integers(-(1 << (bits - 1)), 1 << (bits - 1), size=(N, K), dtype=np.int16).astype(np.int8)
+
+
 def activations_f16(N: int, K: int, seed: int) -> np.ndarray:
     """fp16 bits ``uint16[N][K]``, N(0, 1)."""
     g = rng(seed)
