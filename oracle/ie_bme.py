@@ -51,10 +51,12 @@ def _check(W: np.ndarray, bits: int, lt, areas):
         raise ValueError(f"values outside the signed {bits}-bit range")
 
 
-def union_encode(W: np.ndarray, bits: int, lt=LT, areas=AREAS) -> dict:
+def union_encode(W: np.ndarray, bits: int, lt=LT, areas=AREAS, perms=None) -> dict:
     """IE-BME arrays of an integer matrix W [M][K] (values in the signed
     `bits`-bit range): masks u64 [NLT * words], offsets u32 [NLT + 1] (value
-    counts), values int8 [o_NLT] (one element per value, unpacked)."""
+    counts), values int8 [o_NLT] (one element per value, unpacked).
+    perms (optional, [NLT][H_L]): LT t is encoded with its rows reordered,
+    row k of the reordered tile being row perms[t][k] of the original."""
     W = np.asarray(W, dtype=np.int64)
     _check(W, bits, lt, areas)
     M, K = W.shape
@@ -70,6 +72,8 @@ def union_encode(W: np.ndarray, bits: int, lt=LT, areas=AREAS) -> dict:
     for ti in range(Mp // H):
         for tj in range(Kp // KL):
             tile = Wp[ti * H:(ti + 1) * H, tj * KL:(tj + 1) * KL]
+            if perms is not None:
+                tile = tile[np.asarray(perms[len(offsets) - 1], dtype=np.int64)]
             area = [tile[ra * h:(ra + 1) * h, ca * w:(ca + 1) * w] for ra in range(RA) for ca in range(CA)]
             B = np.zeros((h, w), dtype=bool)
             for A in area:
@@ -84,7 +88,8 @@ def union_encode(W: np.ndarray, bits: int, lt=LT, areas=AREAS) -> dict:
     masks = np.concatenate(masks).astype(np.uint64) if masks else np.zeros(0, dtype=np.uint64)
     return {"masks": masks, "offsets": np.array(offsets, dtype=np.uint64).astype(np.uint32),
             "values": vals, "bits": bits, "lt": tuple(lt), "areas": tuple(areas),
-            "M": M, "K": K, "Mp": Mp, "Kp": Kp, "nnz": int(np.count_nonzero(W))}
+            "M": M, "K": K, "Mp": Mp, "Kp": Kp, "nnz": int(np.count_nonzero(W)),
+            "perms": None if perms is None else np.asarray(perms, dtype=np.int64)}
 
 
 def union_decode(enc: dict) -> np.ndarray:
@@ -105,11 +110,17 @@ def union_decode(enc: dict) -> np.ndarray:
             P = int(flat.sum())
             o = int(enc["offsets"][t])
             assert int(enc["offsets"][t + 1]) - o == Q * P
+            tile = np.zeros((H, KL), dtype=np.int64)
             for a in range(Q):
                 ra, ca = divmod(a, CA)
                 A = np.zeros((h, w), dtype=np.int64)
                 A[B] = enc["values"][o + a * P:o + (a + 1) * P]
-                W[ti * H + ra * h:ti * H + (ra + 1) * h, tj * KL + ca * w:tj * KL + (ca + 1) * w] = A
+                tile[ra * h:(ra + 1) * h, ca * w:(ca + 1) * w] = A
+            if enc.get("perms") is not None:  # undo the LT's row reordering
+                orig = np.zeros_like(tile)
+                orig[enc["perms"][t]] = tile
+                tile = orig
+            W[ti * H:(ti + 1) * H, tj * KL:(tj + 1) * KL] = tile
             t += 1
     return W[:enc["M"], :enc["K"]].astype(np.int8)
 
@@ -156,3 +167,84 @@ def union_spmm(W: np.ndarray, X: np.ndarray) -> np.ndarray:
     """Y [N][M] = X [N][K] * W^T, exact in int64 (the definition; the format
     does not change the result)."""
     return np.asarray(X, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T
+
+
+# ---------------------------------------------------------------- row reordering
+#
+# UnionSparse, "Bitmap-aware row reordering" ("Grouped Cost Formulation",
+# "Grouped Subset Dynamic Programming"): the rows of an LT are partitioned
+# into groups of R_A rows; a group's cost is the number of logical
+# union-mask entries it activates, i.e. over the K_L / C_A grouped columns
+# j, whether any of its rows has a nonzero at one of the C_A columns that
+# group into j.  A subset DP finds the minimum total cost: F(S) for the set
+# S of rows not yet grouped, F(empty) = 0, F(S) = min over the groups g of
+# size R_A that contain the smallest row of S of cost(g) + F(S \ g).  The
+# result is made canonical (rows ascending inside each group, groups in
+# lexicographic order) and turned into a permutation partition-wise: the
+# p-th row of every group, group by group, for p = 0 .. R_A - 1.
+
+def group_costs_table(tile: np.ndarray, RA: int, CA: int) -> dict:
+    """cost(g) for every group g (a sorted tuple of R_A row indices)."""
+    from itertools import combinations
+    H, KL = tile.shape
+    w = KL // CA
+    # grouped activity of each row: column j is active if one of its C_A
+    # columns j, w + j, ... holds a nonzero
+    act = np.zeros((H, w), dtype=bool)
+    for ca in range(CA):
+        act |= tile[:, ca * w:(ca + 1) * w] != 0
+    return {g: int(np.logical_or.reduce(act[list(g)], axis=0).sum()) for g in combinations(range(H), RA)}
+
+
+def reorder_rows(tile: np.ndarray, RA: int, CA: int):
+    """Optimal grouping of the tile's rows by the subset DP; returns
+    (permutation, total cost).  perm[k] = original row placed at row k:
+    row i of area row p is the p-th row of group i."""
+    from itertools import combinations
+    H = tile.shape[0]
+    if H % RA:
+        raise ValueError("R_A must divide the tile's rows")
+    cost = group_costs_table(tile, RA, CA)
+    full = (1 << H) - 1
+    F = {0: (0, None)}   # state -> (min cost, chosen group)
+    # states in order of increasing size (only sizes divisible by R_A occur)
+    order = sorted((S for S in range(full + 1) if bin(S).count("1") % RA == 0), key=lambda S: bin(S).count("1"))
+    for S in order:
+        if S == 0:
+            continue
+        rows = [r for r in range(H) if (S >> r) & 1]
+        r0 = rows[0]
+        best = None
+        for rest in combinations(rows[1:], RA - 1):   # lexicographic: the first minimum is kept
+            g = (r0,) + rest
+            T = S
+            for r in g:
+                T &= ~(1 << r)
+            c = cost[g] + F[T][0]
+            if best is None or c < best[0]:
+                best = (c, g)
+        F[S] = best
+    groups, S = [], full
+    while S:
+        g = F[S][1]
+        groups.append(tuple(sorted(g)))
+        for r in g:
+            S &= ~(1 << r)
+    groups.sort()
+    perm = [g[p] for p in range(RA) for g in groups]
+    return np.array(perm, dtype=np.int64), F[full][0]
+
+
+def union_active(tile: np.ndarray, RA: int, CA: int) -> int:
+    """P_t of a tile as it stands (rows grouped i, h + i, 2h + i, ...)."""
+    H = tile.shape[0]
+    h = H // RA
+    cost = 0
+    w = tile.shape[1] // CA
+    for i in range(h):
+        act = np.zeros(w, dtype=bool)
+        for ra in range(RA):
+            for ca in range(CA):
+                act |= tile[ra * h + i, ca * w:(ca + 1) * w] != 0
+        cost += int(act.sum())
+    return cost

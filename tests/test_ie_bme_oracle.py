@@ -131,3 +131,80 @@ def test_out_of_range_values_rejected():
     u.union_encode(np.zeros((64, 64)), 4, lt=(64, 64), areas=(4, 4))      # 16 x 16 = 256 bits: whole words
     with pytest.raises(ValueError):
         u.union_encode(np.zeros((8, 8)), 4, lt=(8, 8), areas=(2, 2))        # 4 x 4 = 16 bits: not whole words
+
+
+# ---------------------------------------------------------------- row reordering
+
+def _all_groupings(rows, RA):
+    """Every partition of `rows` into groups of RA (brute force)."""
+    from itertools import combinations
+    if not rows:
+        yield []
+        return
+    r0, rest = rows[0], rows[1:]
+    for others in combinations(rest, RA - 1):
+        g = (r0,) + others
+        remaining = [r for r in rest if r not in others]
+        for tail in _all_groupings(remaining, RA):
+            yield [g] + tail
+
+
+@pytest.mark.parametrize("H,KL,RA,CA,seed", [(6, 8, 2, 2, 1), (8, 8, 2, 1, 2), (8, 16, 2, 2, 3),
+                                             (6, 6, 3, 1, 4), (9, 12, 3, 2, 5)])
+def test_reorder_dp_is_the_brute_force_optimum(H, KL, RA, CA, seed):
+    """The subset DP reaches the minimum of the grouped cost over every
+    partition of the rows, and its permutation realizes that cost."""
+    rng = np.random.default_rng(seed)
+    T = (rng.random((H, KL)) < 0.35).astype(np.int64)
+    cost = u.group_costs_table(T, RA, CA)
+    best = min(sum(cost[tuple(sorted(g))] for g in part) for part in _all_groupings(list(range(H)), RA))
+    perm, c = u.reorder_rows(T, RA, CA)
+    assert c == best
+    assert sorted(perm.tolist()) == list(range(H))
+    assert u.union_active(T[perm], RA, CA) == best
+    assert u.union_active(T, RA, CA) >= best
+
+
+def test_reorder_canonical_form():
+    """Rows ascending inside each group, groups in lexicographic order,
+    permutation taken partition-wise."""
+    rng = np.random.default_rng(11)
+    T = (rng.random((8, 8)) < 0.3).astype(np.int64)
+    perm, _ = u.reorder_rows(T, 2, 2)
+    h = 4
+    groups = [(int(perm[i]), int(perm[h + i])) for i in range(h)]
+    assert all(a < b for a, b in groups)
+    assert groups == sorted(groups)
+
+
+def test_reorder_pairs_identical_rows():
+    """Rows i and i + 4 of an 8-row tile are complementary, rows 2k and
+    2k + 1 identical: the identity grouping activates every column, the
+    optimum pairs the identical rows (cost = their own activity)."""
+    T = np.zeros((8, 8), dtype=np.int64)
+    pats = [0b00000011, 0b00001100, 0b00110000, 0b11000000]
+    for k in range(4):
+        for r in (2 * k, 2 * k + 1):
+            for c in range(8):
+                T[r, c] = (pats[k] >> c) & 1
+    perm, c = u.reorder_rows(T, 2, 1)
+    assert c == 4 * 2 and u.union_active(T, 2, 1) > c
+    assert perm.tolist() == [0, 2, 4, 6, 1, 3, 5, 7]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_permuted_encoding_round_trip(bits):
+    """An encoding with per-LT row permutations decodes to the original
+    matrix, and its union count equals the permuted tiles' activity."""
+    rng = np.random.default_rng(bits + 20)
+    lo, hi = -(1 << (bits - 1)), 1 << (bits - 1)
+    W = rng.integers(lo, hi, size=(128, 192)) * (rng.random((128, 192)) < 0.3)
+    perms = [rng.permutation(64) for _ in range(2 * 3)]
+    enc = u.union_encode(W, bits, perms=perms)
+    np.testing.assert_array_equal(u.union_decode(enc), W)
+    t = 0
+    for ti in range(2):
+        for tj in range(3):
+            tile = W[ti * 64:(ti + 1) * 64, tj * 64:(tj + 1) * 64][perms[t]]
+            assert int(enc["offsets"][t + 1] - enc["offsets"][t]) == 4 * u.union_active(tile, 2, 2)
+            t += 1
