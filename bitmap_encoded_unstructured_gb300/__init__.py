@@ -61,6 +61,9 @@ SIGNATURES = {
     "bsp_union_export": (C.c_int, [_P, _P, _P, _P, _P]),
     "bsp_union_decode": (C.c_int, [_P, _P, _P]),
     "bsp_union_check": (C.c_int, [_P, _P]),
+    "bsp_union_encode_reordered": (C.c_int, [_P, C.c_int, _I64, _I64, _P, C.POINTER(_P)]),
+    "bsp_union_export_perms": (C.c_int, [_P, _P, _P]),
+    "bsp_reorder_rows": (C.c_int, [_P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, C.POINTER(_I64)]),
 }
 
 
@@ -76,7 +79,7 @@ class bsp_union_info_t(C.Structure):
                 ("areas_r", C.c_int32), ("areas_c", C.c_int32), ("device", C.c_int32),
                 ("NLT", C.c_int64), ("nnz", C.c_uint64), ("total_values", C.c_uint64),
                 ("value_bytes", C.c_uint64), ("masks", C.c_void_p), ("offsets", C.c_void_p),
-                ("values", C.c_void_p)]
+                ("values", C.c_void_p), ("reordered", C.c_int32)]
 
 
 class BspError(RuntimeError):
@@ -202,6 +205,28 @@ def bsp_union_encode(W_ptr: int, bits: int, M: int, K: int, stream: int = 0) -> 
     h = C.c_void_p()
     _check("bsp_union_encode", lib().bsp_union_encode(W_ptr, bits, M, K, stream, C.byref(h)))
     return h.value
+
+
+def bsp_union_encode_reordered(W_ptr: int, bits: int, M: int, K: int, stream: int = 0) -> int:
+    h = C.c_void_p()
+    _check("bsp_union_encode_reordered", lib().bsp_union_encode_reordered(W_ptr, bits, M, K, stream, C.byref(h)))
+    return h.value
+
+
+def bsp_union_export_perms(h: int, perms_ptr: int, stream: int = 0) -> None:
+    _check("bsp_union_export_perms", lib().bsp_union_export_perms(h, perms_ptr, stream))
+
+
+def bsp_reorder_rows(tile, RA: int, CA: int, exact: bool = True):
+    """Host row reordering of one int8 tile [H][KL]: (perm int32 [H], cost)."""
+    import numpy as np
+    t = np.ascontiguousarray(tile, dtype=np.int8)
+    H, KL = t.shape
+    perm = np.zeros(H, dtype=np.int32)
+    cost = C.c_int64()
+    _check("bsp_reorder_rows", lib().bsp_reorder_rows(t.ctypes.data, H, KL, RA, CA, 1 if exact else 0,
+                                                      perm.ctypes.data, C.byref(cost)))
+    return perm, cost.value
 
 
 def bsp_union_destroy(h: int) -> None:
@@ -402,7 +427,7 @@ class UnionMatrix:
     in the signed ``bits``-bit range (4 or 8); ``spmm`` multiplies by an int8
     activation block X [N][K] into int32 Y [N][M]."""
 
-    def __init__(self, W, bits: int, stream=None):
+    def __init__(self, W, bits: int, stream=None, reorder: bool = False):
         import torch
         if W.dtype != torch.int8 or not W.is_cuda or W.dim() != 2:
             raise TypeError("W must be a 2-D int8 CUDA tensor")
@@ -410,7 +435,8 @@ class UnionMatrix:
         self.M, self.K = int(W.shape[0]), int(W.shape[1])
         self.bits = int(bits)
         self.device = W.device
-        self.h = bsp_union_encode(W.data_ptr(), self.bits, self.M, self.K, _stream(stream))
+        enc = bsp_union_encode_reordered if reorder else bsp_union_encode
+        self.h = enc(W.data_ptr(), self.bits, self.M, self.K, _stream(stream))
 
     def close(self):
         if getattr(self, "h", None):
@@ -446,6 +472,14 @@ class UnionMatrix:
         W = torch.empty((self.M, self.K), dtype=torch.int8, device=self.device)
         bsp_union_decode(self.h, W.data_ptr(), _stream(stream))
         return W
+
+    def perms(self, stream=None):
+        """Copy of the per-LT row permutations (uint8 [NLT, 64]) of a reordered encoding."""
+        import torch
+        o = bsp_union_info(self.h)
+        p = torch.empty((o.NLT, 64), dtype=torch.uint8, device=self.device)
+        bsp_union_export_perms(self.h, p.data_ptr(), _stream(stream))
+        return p
 
     def check(self, stream=None):
         bsp_union_check(self.h, _stream(stream))

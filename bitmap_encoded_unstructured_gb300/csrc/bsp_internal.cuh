@@ -61,6 +61,13 @@ bsp_status_t bsp_exclusive_scan_u32(const uint32_t* counts, int64_t n, uint32_t*
 // h->max_gt_nnz; synchronises s.
 bsp_status_t bsp_run_validate(bsp_handle* h, cudaStream_t s);
 
+// ---- IE-BME row reordering (union_reorder.cu), host ----
+// act[r]: grouped activity of row r of a tile of H rows (bit j = grouped
+// column j); writes the canonical permutation perm[H] of the optimal (exact:
+// subset DP, H <= 20) or heuristic (R_A = 2 pairing) grouping into groups of
+// RA rows and returns its cost.
+int64_t bsp_reorder_rows_act(const uint64_t* act, int H, int RA, int exact, int32_t* perm);
+
 // ---- CUDA-core decode-path product (spmm_decode.cu) ----
 // Everything the decode kernel reads and writes besides X and Y: the
 // encoded arrays, the shape, and the split-K scratch (workspace

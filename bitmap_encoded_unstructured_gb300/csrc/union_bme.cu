@@ -32,6 +32,8 @@
 
 #include <cstdlib>
 #include <new>
+#include <thread>
+#include <vector>
 
 #define BSP_UNION_MAGIC 0xB5B1E0BEu
 
@@ -47,6 +49,7 @@ struct bsp_union {
     uint64_t* masks;          // [NLT * 16]
     uint32_t* offsets;        // [NLT + 1]
     uint8_t* values;          // [value_bytes + 32 zeroed slack]
+    uint8_t* perms;           // row reordering: [NLT][64], row k of LT t is row perms[64 t + k]; or null
     int32_t* ws;              // split-K workspace [16][M], zero between calls
     uint32_t* counters;       // [Mp / 64], zero between calls
     int* err;
@@ -82,12 +85,38 @@ __device__ __forceinline__ int w_at(const int8_t* W, int64_t M, int64_t K, int64
     return (r < M && c < K) ? (int)W[r * K + c] : 0;
 }
 
+// Row of the LT that takes place k (0..63) of its reordered layout.
+__device__ __forceinline__ int lt_row(const uint8_t* perms, int64_t t, int k)
+{
+    return perms ? (int)perms[t * LT + k] : k;
+}
+
+// Grouped activity of every row of every LT (bit j: one of the row's values
+// in columns j and 32 + j of the LT is nonzero), for the row reordering.
+// One warp per LT, lane l: rows l and 32 + l.
+__global__ void ub_rowact_kernel(const int8_t* __restrict__ W, int64_t M, int64_t K, int64_t KT, int64_t NLT,
+                                 uint64_t* __restrict__ act)
+{
+    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int l = threadIdx.x & 31;
+    if (t >= NLT) return;
+    const int64_t r0 = (t / KT) * LT, c0 = (t % KT) * LT;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint64_t a = 0;
+        for (int j = 0; j < HALF; ++j)
+            if (w_at(W, M, K, r0 + h * HALF + l, c0 + j) != 0 || w_at(W, M, K, r0 + h * HALF + l, c0 + HALF + j) != 0)
+                a |= 1ull << j;
+        act[t * LT + h * HALF + l] = a;
+    }
+}
+
 // Pass 1, one warp per LT, lane i = logical row i: the row's union word
 // (bit j: one of the four area values at (i, j) is nonzero), 4 P_t per LT,
 // the nonzero count, and a flag for values outside the b-bit range.
 __global__ void ub_mask_kernel(const int8_t* __restrict__ W, int64_t M, int64_t K, int64_t KT, int64_t NLT,
-                               int bits, uint32_t* __restrict__ masks32, uint32_t* __restrict__ counts,
-                               unsigned long long* nnz, int* bad)
+                               int bits, const uint8_t* __restrict__ perms, uint32_t* __restrict__ masks32,
+                               uint32_t* __restrict__ counts, unsigned long long* nnz, int* bad)
 {
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int i = threadIdx.x & 31;
@@ -100,7 +129,7 @@ __global__ void ub_mask_kernel(const int8_t* __restrict__ W, int64_t M, int64_t 
         bool any = false;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int v = w_at(W, M, K, r0 + (a >> 1) * HALF + i, c0 + (a & 1) * HALF + j);
+            const int v = w_at(W, M, K, r0 + lt_row(perms, t, (a >> 1) * HALF + i), c0 + (a & 1) * HALF + j);
             any |= v != 0;
             nz += v != 0;
             out |= (v < lo) | (v > hi);
@@ -125,7 +154,7 @@ __global__ void ub_mask_kernel(const int8_t* __restrict__ W, int64_t M, int64_t 
 // Pass 2, one warp per LT: every area's value at every active position, at
 // value index o_t + a P_t + rank (int4: nibbles OR-ed into zeroed words).
 __global__ void ub_pack_kernel(const int8_t* __restrict__ W, int64_t M, int64_t K, int64_t KT, int64_t NLT,
-                               int bits, const uint32_t* __restrict__ masks32,
+                               int bits, const uint8_t* __restrict__ perms, const uint32_t* __restrict__ masks32,
                                const uint32_t* __restrict__ offsets, uint8_t* __restrict__ values)
 {
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -148,7 +177,7 @@ __global__ void ub_pack_kernel(const int8_t* __restrict__ W, int64_t M, int64_t 
         const uint32_t r = base + __popc(row & ((1u << j) - 1u));
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int v = w_at(W, M, K, r0 + (a >> 1) * HALF + i, c0 + (a & 1) * HALF + j);
+            const int v = w_at(W, M, K, r0 + lt_row(perms, t, (a >> 1) * HALF + i), c0 + (a & 1) * HALF + j);
             const uint64_t e = o + (uint64_t)a * P + r;
             if (bits == 8)
                 values[e] = (uint8_t)(int8_t)v;
@@ -160,8 +189,8 @@ __global__ void ub_pack_kernel(const int8_t* __restrict__ W, int64_t M, int64_t 
 
 // W back from the arrays (round trip), one warp per LT, lane i = row i.
 __global__ void ub_decode_kernel(const uint32_t* __restrict__ masks32, const uint32_t* __restrict__ offsets,
-                                 const uint8_t* __restrict__ values, int bits, int64_t M, int64_t K, int64_t KT,
-                                 int64_t NLT, int8_t* __restrict__ W)
+                                 const uint8_t* __restrict__ values, const uint8_t* __restrict__ perms, int bits,
+                                 int64_t M, int64_t K, int64_t KT, int64_t NLT, int8_t* __restrict__ W)
 {
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int i = threadIdx.x & 31;
@@ -183,7 +212,7 @@ __global__ void ub_decode_kernel(const uint32_t* __restrict__ masks32, const uin
         const uint32_t r = base + __popc(row & ((1u << j) - 1u));
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int64_t rr = r0 + (a >> 1) * HALF + i, cc = c0 + (a & 1) * HALF + j;
+            const int64_t rr = r0 + lt_row(perms, t, (a >> 1) * HALF + i), cc = c0 + (a & 1) * HALF + j;
             if (rr >= M || cc >= K) continue;
             int v = 0;
             if (act) {
@@ -204,23 +233,30 @@ __global__ void ub_decode_kernel(const uint32_t* __restrict__ masks32, const uin
 
 namespace {
 
-// Per-warp ring stage: union mask (128 B), the N rows of X over the LT's 64
-// columns (64 B each), the LT's value span rounded out to 16 B plus 32 B of
-// read-ahead (the four-value fetch reads one word past a rank).
-template <int BITS, int NT>
+// Per-warp ring stage: union mask (128 B), the LT's row permutation (64 B,
+// reordered formats), the N rows of X over the LT's 64 columns (64 B each),
+// the LT's value span rounded out to 16 B plus 32 B of read-ahead (the
+// four-value fetch reads one word past a rank).  PERM: per-warp row
+// accumulators [64][NT] that each LT's partial sums are scattered into
+// through its permutation.
+template <int BITS, int NT, bool PERM>
 struct UCfg {
     static constexpr int WARPS = 4, THREADS = 32 * WARPS;
-    static constexpr int X_OFF = 128;
+    static constexpr int P_OFF = 128;
+    static constexpr int X_OFF = 192;
     static constexpr int V_OFF = X_OFF + NT * 64;
     static constexpr int V_BYTES = (BITS == 8 ? 4096 : 2048) + 32;
     static constexpr int STAGE = V_OFF + V_BYTES;            // multiple of 16
-    static constexpr int BAR_OFF = WARPS * 2 * STAGE;
+    static constexpr int ACC_OFF = WARPS * 2 * STAGE;
+    static constexpr int ACC_BYTES = PERM ? WARPS * 64 * NT * 4 : 0;
+    static constexpr int BAR_OFF = ACC_OFF + ACC_BYTES;
     static constexpr int SMEM = BAR_OFF + WARPS * 2 * 8;
-    static_assert(WARPS * 64 * NT * 4 <= BAR_OFF, "reduction buffer aliases the rings");
+    static_assert(WARPS * 64 * NT * 4 <= ACC_OFF, "reduction buffer aliases the rings");
     static_assert((STAGE % 16) == 0 && (V_OFF % 16) == 0, "bulk-copy alignment");
 };
 
 struct UArgs {
+    const uint8_t* perms;  // [NLT][64] or null
     const uint32_t* masks32;
     const uint32_t* offsets;
     const uint8_t* values;
@@ -235,11 +271,11 @@ struct UArgs {
     uint32_t spin_cap;
 };
 
-template <int BITS, int NT>
+template <int BITS, int NT, bool PERM>
 __global__ void __launch_bounds__(128)
 union_spmm_kernel(const UArgs a)
 {
-    using C = UCfg<BITS, NT>;
+    using C = UCfg<BITS, NT, PERM>;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t sel_tbl[16];
     __shared__ int s_last;
@@ -259,6 +295,10 @@ union_spmm_kernel(const UArgs a)
         sel_tbl[n] = s;
     }
     if (threadIdx.x < C::WARPS * 2) bspx::mbar_init(bars + threadIdx.x, 1);
+    if constexpr (PERM) {
+        int32_t* z = reinterpret_cast<int32_t*>(smem + C::ACC_OFF);
+        for (int i = threadIdx.x; i < C::WARPS * 64 * NT; i += C::THREADS) z[i] = 0;
+    }
     bspx::fence_mbar_init();
     __syncthreads();
 
@@ -281,8 +321,9 @@ union_spmm_kernel(const UArgs a)
         const int64_t kv = K - kt * LT;
         const uint32_t xb = (uint32_t)(kv >= LT ? LT : kv);  // a multiple of 16 (K is)
         uint8_t* st = ring + s * C::STAGE;
-        bspx::mbar_arrive_expect_tx(wbar + s, 128u + (uint32_t)N * xb + vb);
+        bspx::mbar_arrive_expect_tx(wbar + s, 128u + (PERM ? 64u : 0u) + (uint32_t)N * xb + vb);
         bspx::bulk_g2s(st, a.masks32 + t * 32, 128, wbar + s);
+        if (PERM) bspx::bulk_g2s(st + C::P_OFF, a.perms + t * LT, 64, wbar + s);
         for (int n = 0; n < N; ++n) bspx::bulk_g2s(st + C::X_OFF + n * 64, a.X + n * K + kt * LT, xb, wbar + s);
         if (vb) bspx::bulk_g2s(st + C::V_OFF, a.values + c0, vb, wbar + s);
     };
@@ -309,6 +350,12 @@ union_spmm_kernel(const UArgs a)
             break;
         }
         const uint8_t* st = ring + s * C::STAGE;
+        if constexpr (PERM) {  // this LT's partial sums only; scattered below
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) acc[h][n] = 0;
+        }
         const int64_t t = gi * KT + k_begin + warp + (int64_t)C::WARPS * u;
         const uint32_t o0 = __ldg(a.offsets + t), o1 = __ldg(a.offsets + t + 1);
         const uint32_t P = (o1 - o0) / 4;
@@ -351,6 +398,17 @@ union_spmm_kernel(const UArgs a)
             }
             r += __popc(nb);
         }
+        if constexpr (PERM) {
+            // place k of the reordered LT is row perm[k]: distinct lanes,
+            // distinct rows
+            int32_t* accs = reinterpret_cast<int32_t*>(smem + C::ACC_OFF) + warp * 64 * NT;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rowp = st[C::P_OFF + h * 32 + lane];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) accs[rowp * NT + n] += acc[h][n];
+            }
+        }
         __syncwarp();
     }
     if (failed) {
@@ -361,13 +419,16 @@ union_spmm_kernel(const UArgs a)
         __syncwarp();
     }
 
-    // ---- CTA reduction over the warps (the buffer aliases the rings)
+    // ---- CTA reduction over the warps (the buffer aliases the rings, or is
+    // the row accumulators of a reordered format)
     __syncthreads();
-    int32_t* red = reinterpret_cast<int32_t*>(smem);  // [WARPS][64][NT]
+    int32_t* red = reinterpret_cast<int32_t*>(smem + (PERM ? C::ACC_OFF : 0));  // [WARPS][64][NT]
+    if constexpr (!PERM) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) red[(warp * 64 + h * 32 + lane) * NT + n] = acc[h][n];
+            for (int n = 0; n < NT; ++n) red[(warp * 64 + h * 32 + lane) * NT + n] = acc[h][n];
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < 64 * NT; i += C::THREADS) {
         const int rr = i / NT, n = i % NT;
@@ -395,14 +456,14 @@ union_spmm_kernel(const UArgs a)
     if (threadIdx.x == 0) a.counters[gi] = 0u;
 }
 
-template <int BITS, int NT>
+template <int BITS, int NT, bool PERM>
 bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y, cudaStream_t s)
 {
-    using C = UCfg<BITS, NT>;
+    using C = UCfg<BITS, NT, PERM>;
     static bool attr_done[64] = {};
     if (h->device < 0 || h->device >= 64) return BSP_ERR_INVALID_ARG;
     if (!attr_done[h->device]) {
-        if (cudaFuncSetAttribute(union_spmm_kernel<BITS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(union_spmm_kernel<BITS, NT, PERM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM) != cudaSuccess)
             return BSP_ERR_CUDA;
         attr_done[h->device] = true;
@@ -419,6 +480,7 @@ bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y
     const int per_split = (int)((KT + splits - 1) / splits);
     splits = (KT + per_split - 1) / per_split;
     UArgs a;
+    a.perms = h->perms;
     a.masks32 = reinterpret_cast<const uint32_t*>(h->masks);
     a.offsets = h->offsets;
     a.values = h->values;
@@ -435,18 +497,18 @@ bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y
     a.Y = Y;
     a.spin_cap = bspx::kSpinCap;
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
-    union_spmm_kernel<BITS, NT><<<dim3((unsigned)splits, (unsigned)strips), C::THREADS, C::SMEM, s>>>(a);
+    union_spmm_kernel<BITS, NT, PERM><<<dim3((unsigned)splits, (unsigned)strips), C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
-template <int BITS>
+template <int BITS, bool PERM>
 bsp_status_t dispatch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y, cudaStream_t s)
 {
-    if (N <= 1) return launch_union<BITS, 1>(h, X, N, Y, s);
-    if (N <= 2) return launch_union<BITS, 2>(h, X, N, Y, s);
-    if (N <= 4) return launch_union<BITS, 4>(h, X, N, Y, s);
-    if (N <= 8) return launch_union<BITS, 8>(h, X, N, Y, s);
-    return launch_union<BITS, 16>(h, X, N, Y, s);
+    if (N <= 1) return launch_union<BITS, 1, PERM>(h, X, N, Y, s);
+    if (N <= 2) return launch_union<BITS, 2, PERM>(h, X, N, Y, s);
+    if (N <= 4) return launch_union<BITS, 4, PERM>(h, X, N, Y, s);
+    if (N <= 8) return launch_union<BITS, 8, PERM>(h, X, N, Y, s);
+    return launch_union<BITS, 16, PERM>(h, X, N, Y, s);
 }
 
 void free_union(bsp_union* h)
@@ -455,6 +517,7 @@ void free_union(bsp_union* h)
     cudaFree(h->masks);
     cudaFree(h->offsets);
     cudaFree(h->values);
+    cudaFree(h->perms);
     cudaFree(h->ws);
     cudaFree(h->counters);
     cudaFree(h->err);
@@ -464,10 +527,45 @@ void free_union(bsp_union* h)
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-bsp_status_t bsp_union_encode(const int8_t* W, int bits, int64_t M, int64_t K, bsp_stream_t stream,
-                              bsp_union_t* out)
+// Per-LT row permutations by the host solver (pairing heuristic for the
+// 64-row LTs, R_A = 2), in parallel over LTs.
+bsp_status_t solve_perms(bsp_union* h, const int8_t* W, int64_t KT, cudaStream_t s)
+{
+    uint64_t* act = nullptr;
+    if (cudaMalloc(&act, (size_t)h->NLT * LT * 8) != cudaSuccess) return BSP_ERR_OOM;
+    ub_rowact_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, s>>>(W, h->M, h->K, KT, h->NLT, act);
+    std::vector<uint64_t> hact((size_t)h->NLT * LT);
+    const bool ok = cudaGetLastError() == cudaSuccess &&
+                    cudaMemcpyAsync(hact.data(), act, hact.size() * 8, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+                    cudaStreamSynchronize(s) == cudaSuccess;
+    cudaFree(act);
+    if (!ok) return BSP_ERR_CUDA;
+    std::vector<uint8_t> hperm((size_t)h->NLT * LT);
+    const int64_t nlt = h->NLT;
+    unsigned nt = std::thread::hardware_concurrency();
+    nt = nt < 1 ? 1 : (nt > 64 ? 64 : nt);
+    if ((int64_t)nt > nlt) nt = (unsigned)nlt;
+    std::vector<std::thread> pool;
+    for (unsigned w = 0; w < nt; ++w)
+        pool.emplace_back([&, w] {
+            int32_t perm[LT];
+            for (int64_t t = w; t < nlt; t += nt) {
+                bsp_reorder_rows_act(hact.data() + t * LT, LT, 2, 0, perm);
+                for (int k = 0; k < LT; ++k) hperm[t * LT + k] = (uint8_t)perm[k];
+            }
+        });
+    for (auto& th : pool) th.join();
+    if (cudaMalloc(&h->perms, hperm.size()) != cudaSuccess) return BSP_ERR_OOM;
+    if (cudaMemcpyAsync(h->perms, hperm.data(), hperm.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    return BSP_OK;
+}
+
+bsp_status_t union_encode(const int8_t* W, int bits, int64_t M, int64_t K, bool reorder, bsp_stream_t stream,
+                          bsp_union_t* out)
 {
     if (!out) return BSP_ERR_INVALID_ARG;
     *out = nullptr;
@@ -513,7 +611,8 @@ bsp_status_t bsp_union_encode(const int8_t* W, int bits, int64_t M, int64_t K, b
         st = BSP_ERR_CUDA;
         goto done;
     }
-    ub_mask_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, s>>>(W, M, K, KT, h->NLT, bits,
+    if (reorder && (st = solve_perms(h, W, KT, s)) != BSP_OK) goto done;
+    ub_mask_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, s>>>(W, M, K, KT, h->NLT, bits, h->perms,
                                                                 reinterpret_cast<uint32_t*>(h->masks), counts, nnz,
                                                                 flags + 1);
     if (cudaGetLastError() != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
@@ -535,7 +634,7 @@ bsp_status_t bsp_union_encode(const int8_t* W, int bits, int64_t M, int64_t K, b
     // read up to 16 B past the last span
     if (cudaMalloc(&h->values, h->value_bytes + 32) != cudaSuccess) { st = BSP_ERR_OOM; goto done; }
     if (cudaMemsetAsync(h->values, 0, h->value_bytes + 32, s) != cudaSuccess) { st = BSP_ERR_CUDA; goto done; }
-    ub_pack_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, s>>>(W, M, K, KT, h->NLT, bits,
+    ub_pack_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, s>>>(W, M, K, KT, h->NLT, bits, h->perms,
                                                                 reinterpret_cast<const uint32_t*>(h->masks),
                                                                 h->offsets, h->values);
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) st = BSP_ERR_CUDA;
@@ -549,6 +648,34 @@ done:
     }
     *out = h;
     return BSP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsp_status_t bsp_union_encode(const int8_t* W, int bits, int64_t M, int64_t K, bsp_stream_t stream,
+                              bsp_union_t* out)
+{
+    return union_encode(W, bits, M, K, false, stream, out);
+}
+
+bsp_status_t bsp_union_encode_reordered(const int8_t* W, int bits, int64_t M, int64_t K, bsp_stream_t stream,
+                                        bsp_union_t* out)
+{
+    return union_encode(W, bits, M, K, true, stream, out);
+}
+
+bsp_status_t bsp_union_export_perms(bsp_union_t h, uint8_t* perms, bsp_stream_t stream)
+{
+    if (!valid(h) || !perms) return BSP_ERR_INVALID_ARG;
+    if (!h->perms) return BSP_ERR_INVALID_ARG;  // not a reordered encoding
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    return cudaMemcpyAsync(perms, h->perms, (size_t)h->NLT * LT, cudaMemcpyDefault, (cudaStream_t)stream) ==
+                   cudaSuccess
+               ? BSP_OK
+               : BSP_ERR_CUDA;
 }
 
 bsp_status_t bsp_union_destroy(bsp_union_t h)
@@ -569,8 +696,12 @@ bsp_status_t bsp_union_spmm(bsp_union_t h, const int8_t* X, int64_t N, int32_t* 
     cudaStream_t s = (cudaStream_t)stream;
     for (int64_t n0 = 0; n0 < N; n0 += BSP_DECODE_MAX_N) {  // blocks of 16 columns of Y
         const int nb = (int)((N - n0) < BSP_DECODE_MAX_N ? (N - n0) : BSP_DECODE_MAX_N);
-        const bsp_status_t st = h->bits == 8 ? dispatch_union<8>(h, X + n0 * h->K, nb, Y + n0 * h->M, s)
-                                             : dispatch_union<4>(h, X + n0 * h->K, nb, Y + n0 * h->M, s);
+        const int8_t* Xb = X + n0 * h->K;
+        int32_t* Yb = Y + n0 * h->M;
+        const bsp_status_t st = h->perms ? (h->bits == 8 ? dispatch_union<8, true>(h, Xb, nb, Yb, s)
+                                                         : dispatch_union<4, true>(h, Xb, nb, Yb, s))
+                                         : (h->bits == 8 ? dispatch_union<8, false>(h, Xb, nb, Yb, s)
+                                                         : dispatch_union<4, false>(h, Xb, nb, Yb, s));
         if (st != BSP_OK) return st;
     }
     return BSP_OK;
@@ -600,6 +731,7 @@ bsp_status_t bsp_union_info(bsp_union_t h, bsp_union_info_t* o)
     o->masks = h->masks;
     o->offsets = h->offsets;
     o->values = h->values;
+    o->reordered = h->perms != nullptr;
     return BSP_OK;
 }
 
@@ -626,8 +758,8 @@ bsp_status_t bsp_union_decode(bsp_union_t h, int8_t* W_out, bsp_stream_t stream)
     DeviceGuard g(h->device);
     if (!g.ok) return BSP_ERR_CUDA;
     ub_decode_kernel<<<blocks_for(h->NLT * 32, 256), 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const uint32_t*>(h->masks), h->offsets, h->values, h->bits, h->M, h->K, h->Kp / LT, h->NLT,
-        W_out);
+        reinterpret_cast<const uint32_t*>(h->masks), h->offsets, h->values, h->perms, h->bits, h->M, h->K, h->Kp / LT,
+        h->NLT, W_out);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 

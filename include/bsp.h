@@ -334,6 +334,7 @@ typedef struct {
     const uint64_t *masks;    /* device, [NLT * 16]                           */
     const uint32_t *offsets;  /* device, [NLT + 1]                            */
     const uint8_t *values;    /* device, [value_bytes] (+32 B slack)          */
+    int32_t reordered;        /* 1: rows reordered per LT (bsp_union_encode_reordered) */
 } bsp_union_info_t;
 
 /*
@@ -348,6 +349,40 @@ typedef struct {
  */
 bsp_status_t bsp_union_encode(const int8_t *W, int bits, int64_t M, int64_t K,
                               bsp_stream_t stream, bsp_union_t *out);
+
+/*
+ * The same with bitmap-aware row reordering ("UnionSparse", "Bitmap-aware
+ * row reordering"): each LT's 64 rows are regrouped into the 32 pairs of
+ * its logical rows so as to activate fewer union-mask entries, the LT is
+ * encoded in that row order, and the permutation is kept with it
+ * (u8 [NLT][64]: place k of the reordered LT holds row perm[k] of the LT).
+ * Products write Y in the original row order.  The pairing is found on the
+ * host (offline): the better of the identity pairing and a greedy pairing,
+ * each improved by pair swaps (the page's exact subset DP needs 2^64 states
+ * at 64 rows; bsp_reorder_rows runs it on small tiles).  Synchronises stream.
+ */
+bsp_status_t bsp_union_encode_reordered(const int8_t *W, int bits, int64_t M, int64_t K,
+                                        bsp_stream_t stream, bsp_union_t *out);
+
+/* Copy of the per-LT row permutations of a reordered handle into perms
+ * (u8 [NLT * 64], host or device); BSP_ERR_INVALID_ARG if not reordered. */
+bsp_status_t bsp_union_export_perms(bsp_union_t h, uint8_t *perms, bsp_stream_t stream);
+
+/*
+ * Row reordering of one tile, on the host ("UnionSparse", "Grouped Cost
+ * Formulation", "Grouped Subset Dynamic Programming").
+ *   tile   host int8 [H][KL]; rows are grouped into groups of RA, the KL
+ *          columns into KL / CA grouped columns (column j, w + j, ... of the
+ *          C_A column areas, w = KL / CA <= 64).
+ *   exact  1: the page's subset DP, the minimum grouped cost (H <= 20);
+ *          0: the pairing heuristic of bsp_union_encode_reordered (RA = 2).
+ *   perm   [H] the canonical permutation (rows ascending in a group, groups
+ *          in lexicographic order, taken partition-wise); cost: its grouped
+ *          cost (the union-mask entries it activates).
+ * BSP_ERR_SHAPE for sizes outside those limits.
+ */
+bsp_status_t bsp_reorder_rows(const int8_t *tile, int H, int KL, int RA, int CA, int exact,
+                              int32_t *perm, int64_t *cost);
 
 /* Free a union handle (synchronises the device first). */
 bsp_status_t bsp_union_destroy(bsp_union_t h);

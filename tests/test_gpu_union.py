@@ -137,3 +137,60 @@ def test_llama7b_ffn_shape_sampled_rows(bits):
         Y = A.spmm(_dev(X[:N])).cpu().numpy().astype(np.int64)
         np.testing.assert_array_equal(Y[:, rows], ref[:N])
     A.check()
+
+
+def _paired_rows(M, K, bits, seed):
+    """Weights whose rows come in identical-pattern pairs (2k, 2k + 1) with
+    independent values: row reordering can halve the active union entries."""
+    rng = np.random.default_rng(seed)
+    lo, hi = -(1 << (bits - 1)), (1 << (bits - 1))
+    pat = np.repeat(rng.random((M // 2, K)) < 0.3, 2, axis=0)
+    vals = rng.integers(lo, hi - 1, size=(M, K))
+    vals[vals >= 0] += 1
+    return (vals * pat).astype(np.int8)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("kind", ["paired", "random"])
+def test_reordered_encode_matches_oracle(bits, kind):
+    W = _paired_rows(192, 320, bits, 61 + bits) if kind == "paired" else _weights(130, 208, bits, 0.6, 62 + bits)
+    A = bsp.UnionMatrix(_dev(W), bits, reorder=True)
+    assert A.info()["reordered"] == 1
+    perms = A.perms().cpu().numpy().astype(np.int64)
+    for p in perms:
+        assert sorted(p.tolist()) == list(range(64))
+    enc = u.union_encode(W, bits, perms=perms)
+    masks, offsets, values = A.arrays()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(masks.cpu().numpy().view(np.uint64), enc["masks"])
+    np.testing.assert_array_equal(offsets.cpu().numpy().view(np.uint32), enc["offsets"])
+    np.testing.assert_array_equal(values.cpu().numpy(), u.pack_values(enc["values"], bits))
+    assert A.storage_bytes() == u.storage_bytes(enc)
+    np.testing.assert_array_equal(A.decode().cpu().numpy(), W)
+    plain = u.union_encode(W, bits)
+    assert int(enc["offsets"][-1]) <= int(plain["offsets"][-1])
+    if kind == "paired":
+        assert int(enc["offsets"][-1]) < int(plain["offsets"][-1])
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("N", [1, 5, 16, 20])
+def test_reordered_spmm_exact(bits, N):
+    """Products of a reordered encoding come out in the original row order."""
+    W = _paired_rows(256, 1024, bits, 70 + bits)
+    X = _acts(N, 1024, bits, 71 + N)
+    A = bsp.UnionMatrix(_dev(W), bits, reorder=True)
+    Y = A.spmm(_dev(X)).cpu().numpy().astype(np.int64)
+    A.check()
+    np.testing.assert_array_equal(Y, u.union_spmm(W, X))
+
+
+def test_reordered_split_k_forced(monkeypatch):
+    W = _paired_rows(320, 1024, 8, 81)
+    X = _acts(8, 1024, 8, 82)
+    ref = u.union_spmm(W, X)
+    A = bsp.UnionMatrix(_dev(W), 8, reorder=True)
+    for sp in (1, 5, 16):
+        monkeypatch.setenv("BSP_UNION_SPLITK", str(sp))
+        np.testing.assert_array_equal(A.spmm(_dev(X)).cpu().numpy().astype(np.int64), ref)
+    A.check()
