@@ -485,17 +485,26 @@ def run_union_leg(bsp, torch, dev, stream, ws, steps=20):
     over the b-bit range), N = 1, 8, 16.  GB/s of the algorithmic bytes
     (union storage + int8 X + int32 Y) with the four layers rotating through
     L2 (178 MB of W4 storage, 340 MB of W8); also the storage against dense
-    b-bit bytes and the page's PMR."""
+    b-bit bytes and the page's PMR.  W4A4 is measured twice: as encoded and
+    with bitmap-aware row reordering (encode time, union entries saved)."""
     peak, peak_kind = _peaks()
     out = {"unit": "GB/s", "peak": peak, "peak_kind": peak_kind}
-    for bits in (4, 8):
+    for bits, reorder in ((4, False), (4, True), (8, False)):
         mats, X, Y, bpc = {}, {}, {}, {}
-        stor_total = dense_total = payload_total = 0
+        stor_total = dense_total = payload_total = values_total = 0
+        enc_s = 0.0
         for li, (name, M, K) in enumerate(LAYERS):
             W = synth.weights_int(M, K, bits, 0.5, synth.seed_for(6, 10 * bits + li), exact=False)
-            A = bsp.UnionMatrix(torch.from_numpy(W).to(dev), bits)
-            info = A.info()
+            Wd = torch.from_numpy(W).to(dev)
             del W
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            A = bsp.UnionMatrix(Wd, bits, reorder=reorder)
+            torch.cuda.synchronize()
+            enc_s += time.perf_counter() - t0
+            del Wd
+            info = A.info()
+            values_total += info["total_values"]
             stor = A.storage_bytes()
             stor_total += stor
             dense_total += M * K * bits // 8
@@ -507,7 +516,8 @@ def run_union_leg(bsp, torch, dev, stream, ws, steps=20):
                 bpc[(name, N)] = stor + K * N + 4 * M * N
         leg = {"storage_bytes": stor_total, "dense_bytes": dense_total,
                "compression_ratio": round(dense_total / stor_total, 4),
-               "pmr": round(payload_total / (stor_total - payload_total), 4), "points": {}}
+               "pmr": round(payload_total / (stor_total - payload_total), 4),
+               "stored_values": values_total, "encode_seconds": round(enc_s, 3), "points": {}}
         for N in UNION_NS:
             def rnd():
                 for name, _, _ in LAYERS:
@@ -529,7 +539,7 @@ def run_union_leg(bsp, torch, dev, stream, ws, steps=20):
         for A in mats.values():
             A.check()
             A.close()
-        out[f"W{bits}A{bits}"] = leg
+        out[f"W{bits}A{bits}" + ("_reordered" if reorder else "")] = leg
     return out
 
 
