@@ -270,6 +270,28 @@ def run_case(args):
     layer, n = args.case.split(":")
     N = int(n)
     dev = torch.device("cuda", 0)
+    if layer[:3] in ("w4_", "w8_"):  # IE-BME: w4_qkv:8 = W4A4 on the QKV projection, N = 8
+        bits, lname = int(layer[1]), layer[3:]
+        (name, M, K), = [l for l in LAYERS if l[0] == lname]
+        A = bsp.UnionMatrix(torch.from_numpy(synth.weights_int(M, K, bits, 0.5, synth.seed_for(6, bits),
+                                                               exact=False)).to(dev), bits)
+        X = torch.from_numpy(synth.activations_int(N, K, bits, synth.seed_for(6, N))).to(dev)
+        Y = torch.empty((N, M), dtype=torch.int32, device=dev)
+        for _ in range(args.warmup):
+            A.spmm(X, out=Y)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            A.spmm(X, out=Y)
+        e.record()
+        torch.cuda.synchronize()
+        A.check()
+        us = s.elapsed_time(e) * 1e3 / args.steps
+        b = A.storage_bytes() + K * N + 4 * M * N
+        print(json.dumps({"case": args.case, "us_per_call": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                          "note": "same layer every call"}))
+        return 0
     if layer in dict((l[0], l) for l in PREFILL_LAYERS):
         (name, M, K), = [l for l in PREFILL_LAYERS if l[0] == layer]
         A = bsp.BitmapMatrix(torch.from_numpy(prefill_weights(name, M, K).view(np.float16)).to(dev))
