@@ -269,6 +269,7 @@ struct UArgs {
     int* err;
     int32_t* Y;
     uint32_t spin_cap;
+    int stall_first;  // test only: each warp skips the copies of its first LT
 };
 
 template <int BITS, int NT, bool PERM>
@@ -336,7 +337,7 @@ union_spmm_kernel(const UArgs a)
 
     bool failed = false;
     int issued = 0;
-    if (cnt > 0 && lane == 0) issue(0, 0);
+    if (cnt > 0 && lane == 0 && !a.stall_first) issue(0, 0);  // stalled: nothing completes stage 0
     issued = cnt > 0 ? 1 : 0;
     int u = 0;
     for (; u < cnt; ++u) {
@@ -497,6 +498,7 @@ bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y
     a.Y = Y;
     a.spin_cap = bspx::kSpinCap;
     if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
     union_spmm_kernel<BITS, NT, PERM><<<dim3((unsigned)splits, (unsigned)strips), C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }

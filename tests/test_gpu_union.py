@@ -194,3 +194,26 @@ def test_reordered_split_k_forced(monkeypatch):
         monkeypatch.setenv("BSP_UNION_SPLITK", str(sp))
         np.testing.assert_array_equal(A.spmm(_dev(X)).cpu().numpy().astype(np.int64), ref)
     A.check()
+
+
+def test_wait_that_runs_out_reports_timeout(monkeypatch):
+    """Each warp's producer skips its first tile's copies (a barrier nothing
+    completes); the bounded wait gives up, the kernel records
+    BSP_ERR_TIMEOUT, drains its other copies and returns; the next call is
+    exact (workspace and counters were left clean)."""
+    W = _weights(256, 1024, 8, 0.5, 91)
+    X = _acts(4, 1024, 8, 92)
+    A = bsp.UnionMatrix(_dev(W), 8)
+    Xd = _dev(X)
+    monkeypatch.setenv("BSP_TEST_STALL", "1")
+    monkeypatch.setenv("BSP_SPIN_CAP", "2000")
+    monkeypatch.setenv("BSP_UNION_SPLITK", "4")
+    A.spmm(Xd)
+    with pytest.raises(bsp.BspError) as e:
+        A.check()
+    assert e.value.status == 7
+    monkeypatch.delenv("BSP_TEST_STALL")
+    monkeypatch.delenv("BSP_SPIN_CAP")
+    A.check()  # cleared
+    np.testing.assert_array_equal(A.spmm(Xd).cpu().numpy().astype(np.int64), u.union_spmm(W, X))
+    A.check()
