@@ -239,18 +239,22 @@ namespace {
 // four-value fetch reads one word past a rank).  PERM: per-warp row
 // accumulators [64][NT] that each LT's partial sums are scattered into
 // through its permutation.
+#ifndef BSP_UNION_STAGES
+#define BSP_UNION_STAGES 2
+#endif
 template <int BITS, int NT, bool PERM>
 struct UCfg {
     static constexpr int WARPS = 4, THREADS = 32 * WARPS;
+    static constexpr int S = BSP_UNION_STAGES;  // ring stages per warp
     static constexpr int P_OFF = 128;
     static constexpr int X_OFF = 192;
     static constexpr int V_OFF = X_OFF + NT * 64;
     static constexpr int V_BYTES = (BITS == 8 ? 4096 : 2048) + 32;
     static constexpr int STAGE = V_OFF + V_BYTES;            // multiple of 16
-    static constexpr int ACC_OFF = WARPS * 2 * STAGE;
+    static constexpr int ACC_OFF = WARPS * S * STAGE;
     static constexpr int ACC_BYTES = PERM ? WARPS * 64 * NT * 4 : 0;
     static constexpr int BAR_OFF = ACC_OFF + ACC_BYTES;
-    static constexpr int SMEM = BAR_OFF + WARPS * 2 * 8;
+    static constexpr int SMEM = BAR_OFF + WARPS * S * 8;
     static_assert(WARPS * 64 * NT * 4 <= ACC_OFF, "reduction buffer aliases the rings");
     static_assert((STAGE % 16) == 0 && (V_OFF % 16) == 0, "bulk-copy alignment");
 };
@@ -295,7 +299,7 @@ union_spmm_kernel(const UArgs a)
         }
         sel_tbl[n] = s;
     }
-    if (threadIdx.x < C::WARPS * 2) bspx::mbar_init(bars + threadIdx.x, 1);
+    if (threadIdx.x < C::WARPS * C::S) bspx::mbar_init(bars + threadIdx.x, 1);
     if constexpr (PERM) {
         int32_t* z = reinterpret_cast<int32_t*>(smem + C::ACC_OFF);
         for (int i = threadIdx.x; i < C::WARPS * 64 * NT; i += C::THREADS) z[i] = 0;
@@ -309,8 +313,8 @@ union_spmm_kernel(const UArgs a)
     const int64_t k_begin = (int64_t)blockIdx.x * a.per_split;
     const int64_t k_cnt = min((int64_t)a.per_split, KT - k_begin);
     const int cnt = k_cnt > warp ? (int)((k_cnt - warp + C::WARPS - 1) / C::WARPS) : 0;  // this warp's LTs
-    uint8_t* ring = smem + warp * 2 * C::STAGE;
-    uint64_t* wbar = bars + warp * 2;
+    uint8_t* ring = smem + warp * C::S * C::STAGE;
+    uint64_t* wbar = bars + warp * C::S;
 
     auto issue = [&](int u, int s) {  // lane 0: the copies of this warp's LT u into stage s
         const int64_t kt = k_begin + warp + (int64_t)C::WARPS * u;
@@ -336,17 +340,19 @@ union_spmm_kernel(const UArgs a)
         for (int n = 0; n < NT; ++n) acc[h][n] = 0;
 
     bool failed = false;
-    int issued = 0;
-    if (cnt > 0 && lane == 0 && !a.stall_first) issue(0, 0);  // stalled: nothing completes stage 0
-    issued = cnt > 0 ? 1 : 0;
+    // prefetch S - 1 tiles ahead; stalled (test): nothing completes stage 0
+    int issued = cnt < C::S - 1 ? cnt : C::S - 1;
+    if (lane == 0)
+        for (int v = 0; v < issued; ++v)
+            if (v > 0 || !a.stall_first) issue(v, v);
     int u = 0;
     for (; u < cnt; ++u) {
-        const int s = u & 1;
-        if (u + 1 < cnt) {  // stage s ^ 1 was released by the __syncwarp that ended LT u - 1
-            if (lane == 0) issue(u + 1, s ^ 1);
-            issued = u + 2;
+        const int s = u % C::S;
+        if (u + C::S - 1 < cnt) {  // its stage was released by the __syncwarp that ended LT u - 1
+            if (lane == 0) issue(u + C::S - 1, (u + C::S - 1) % C::S);
+            issued = u + C::S;
         }
-        if (!__all_sync(FULL, bspx::mbar_wait_bounded(wbar + s, (uint32_t)((u >> 1) & 1), a.spin_cap))) {
+        if (!__all_sync(FULL, bspx::mbar_wait_bounded(wbar + s, (uint32_t)((u / C::S) & 1), a.spin_cap))) {
             failed = true;
             break;
         }
@@ -415,7 +421,8 @@ union_spmm_kernel(const UArgs a)
     if (failed) {
         if (lane == 0) {
             atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
-            for (int v = u; v < issued; ++v) bspx::mbar_wait_bounded(wbar + (v & 1), (uint32_t)((v >> 1) & 1), a.spin_cap);
+            for (int v = u; v < issued; ++v)
+                bspx::mbar_wait_bounded(wbar + (v % C::S), (uint32_t)((v / C::S) & 1), a.spin_cap);
         }
         __syncwarp();
     }
