@@ -472,6 +472,10 @@ def run_gpu(args):
     if not args.no_union:
         union = run_union_leg(bsp, torch, dev, stream, ws)
 
+    sweep = None
+    if not args.no_sweep:
+        sweep = run_sweep_leg(bsp, torch, dev, stream, ws)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = time_oracle(Ws, xs, relu, bpc, stor, target_s=10.0)
@@ -483,6 +487,7 @@ def run_gpu(args):
                 "data": "synthetic (seeded numpy: N(0,0.02) weights, magnitude 50% mask, N(0,1) X)",
                 "config": _config(), "frac_hbm": round(value / ws / peak, 4),
                 "breakdown": breakdown, "prefill": prefill, "union_ie_bme": union,
+                "sparsity_sweep": sweep,
                 "roofline": {"bound": "hbm",
                              "kernel": STEP_KERNELS,
                              "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
@@ -606,6 +611,71 @@ def run_prefill_leg(bsp, torch, dev, stream, ws, reps=5):
     return out
 
 
+SWEEP_SHAPE = (8192, 8192)
+SWEEP_SPARSITY = (0.3, 0.4, 0.5, 0.6, 0.7)
+SWEEP_NS = (1, 4, 8, 16)
+L2_BYTES = 129 * 10**6
+
+
+def sweep_closed_form(M, K, s):
+    """Storage of an M x K fp16 layer (M, K multiples of 64) at sparsity s,
+    written from the format's parts: 2 bytes per kept value, one 8-byte
+    bitmap per 8 x 8 tile, one 4-byte offset per 64 x 64 group plus the
+    end offset."""
+    return 2 * (M * K - round(s * M * K)) + 8 * (M * K // 64) + 4 * (M * K // 4096 + 1)
+
+
+def run_sweep_leg(bsp, torch, dev, stream, ws, steps=20):
+    """Sparsity sweep of the decode product on a square 8192 x 8192 fp16
+    layer: uniform exact-count masks at 30-70%, N(0, 0.02) values, N(0, 1)
+    activations, N = 1, 4, 8, 16.  Per sparsity: the library's storage
+    against the closed form, CR = dense fp16 bytes / storage; per point the
+    GB/s of the algorithmic bytes (storage + 2KN + 2MN) and its fraction of
+    the HBM peak.  The layer is encoded into enough separate copies that the
+    copies together hold at least three times L2 and the calls rotate over
+    them, so every call reads its weight from HBM."""
+    peak, peak_kind = _peaks()
+    M, K = SWEEP_SHAPE
+    out = {"shape": f"{M}x{K} fp16", "unit": "GB/s", "peak": peak, "peak_kind": peak_kind, "points": {}}
+    for s in SWEEP_SPARSITY:
+        W = synth.weights_f16(M, K, s, "uniform", synth.seed_for(2, round(s * 10)))
+        nnz = int(np.count_nonzero(W))
+        Wd = torch.from_numpy(W.view(np.float16)).to(dev)
+        del W
+        first = bsp.BitmapMatrix(Wd)
+        stor = first.storage_bytes()
+        copies = max(2, -(-3 * L2_BYTES // stor))
+        mats = [first] + [bsp.BitmapMatrix(Wd) for _ in range(copies - 1)]
+        del Wd
+        torch.cuda.synchronize()
+        row = {"nnz": nnz, "storage_bytes": stor, "closed_form_bytes": sweep_closed_form(M, K, s),
+               "compression_ratio": round(2 * M * K / stor, 4), "copies": copies}
+        for N in SWEEP_NS:
+            X = torch.from_numpy(synth.activations_f16(N, K, synth.seed_for(2, N)).view(np.float16)).to(dev)
+            Y = torch.empty((N, M), dtype=torch.float16, device=dev)
+
+            def rnd():
+                for A in mats:
+                    A.spmm(X, out=Y, stream=stream)
+            for _ in range(3):
+                rnd()
+            torch.cuda.synchronize()
+            s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(steps):
+                rnd()
+            e0.record(stream)
+            torch.cuda.synchronize()
+            us = _max_over_ranks(s0.elapsed_time(e0) / (steps * copies), ws) * 1e3
+            gbps = (stor + 2 * K * N + 2 * M * N) / (us * 1e-6) / 1e9
+            row[f"N={N}"] = {"us": round(us, 2), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4)}
+        for A in mats:
+            A.check()
+            A.close()
+        out["points"][f"s={s:.1f}"] = row
+    return out
+
+
 def _kernel_hash():
     """Hash of the kernel sources the decode step launches (the stored DRAM
     traffic is used only while they are unchanged)."""
@@ -627,6 +697,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-union", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--case", default=None,
                     help="LAYER:N, one configuration only (N=0: spMspV), for profiler captures")
     args = ap.parse_args()

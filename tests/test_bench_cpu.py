@@ -1,0 +1,38 @@
+"""Host-side pieces of bench.py that need no GPU: the closed-form storage
+the sparsity sweep reports equals the bytes of the oracle's encoding of the
+same kind of weight (exact-count uniform masks), and the per-call
+algorithmic bytes of the decode step count the encoded weight plus X and Y.
+CPU only."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from bitmap_encoded_unstructured_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("s", [0.0, 0.3, 0.5, 0.7, 1.0])
+@pytest.mark.parametrize("M,K", [(64, 64), (128, 320), (256, 192)])
+def test_sweep_closed_form_matches_the_oracle(M, K, s):
+    W = synth.weights_f16(M, K, s, "uniform", 7 + M + K)
+    enc = oracle.encode(W)
+    # every kept N(0, 0.02) draw is a nonzero fp16 at these sizes
+    assert int(np.count_nonzero(W)) == M * K - round(s * M * K)
+    assert bench.sweep_closed_form(M, K, s) == oracle.storage_bytes(enc)
+
+
+def test_decode_step_bytes_count_weight_x_and_y():
+    Ws = {"out": synth.weights_f16(5120, 5120, 0.5, "uniform", 3)}
+    relu = synth.activations_relu_f16(20480, 4)
+    bpc, stor, _ = bench.algorithmic_bytes(Ws, relu)
+    enc_bytes = oracle.storage_bytes(oracle.encode(Ws["out"]))
+    assert stor["out"] == enc_bytes
+    for N in bench.NS:
+        assert bpc[("out", N)] == enc_bytes + 2 * 5120 * N + 2 * 5120 * N
