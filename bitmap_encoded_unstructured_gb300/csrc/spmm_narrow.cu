@@ -53,6 +53,12 @@
 #ifndef BSP_NARROW_CTA_COST
 #define BSP_NARROW_CTA_COST 6
 #endif
+// resident CTAs per SM: 1 gives a CTA the whole shared memory (the deepest
+// C ring); 2 halves it and caps the registers at 48 per thread, so that a
+// second CTA's 21 warps hide the decoders' latency
+#ifndef BSP_NARROW_MINB
+#define BSP_NARROW_MINB 2
+#endif
 
 namespace {
 
@@ -72,7 +78,11 @@ constexpr uint32_t kSleepNs = 1000;        // suspend hint of the waiting polls
 constexpr int SB = 8;                      // X sub-tile stages
 constexpr int SA = 2;                      // decoded A tile stages
 constexpr int SC_MAX = 12;                 // barrier slots of the C ring
-constexpr int SMEM_MAX = 227 * 1024;
+constexpr int MINB = BSP_NARROW_MINB;
+static_assert(MINB == 1 || MINB == 2, "one or two CTAs per SM");
+// shared memory of a CTA: all of it, or half of the SM's 228 KB less the
+// 1 KB the driver reserves per resident CTA
+constexpr int SMEM_MAX = MINB == 1 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
 constexpr int B_STAGE = BN * BK * 2;       // 2 KB
 constexpr int OFF_B = 0;                   // 1024-B aligned regions first
 constexpr int OFF_A = OFF_B + SB * B_STAGE;
@@ -211,7 +221,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 // Grid: tiles x splits CTAs, split fastest; CTA (tile, part) takes the
 // balanced share [part * KT / splits, (part + 1) * KT / splits) of the GT
 // columns (at least one: the host keeps splits <= KT).
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, MINB)
 spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
 {
     const int SC = a.sc;
@@ -571,10 +581,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 
 int bsp_narrow_splits_auto(const bsp_decode_problem& p)
 {
-    // the critical path: CTA waves (one CTA per SM) times the GT columns of
-    // a CTA plus a fixed cost per CTA (start, epilogue)
+    // the critical path: CTA waves (MINB CTAs per SM) times the GT columns
+    // of a CTA plus a fixed cost per CTA (start, epilogue)
     const int64_t tiles = (p.Mp + BM - 1) / BM, KT = p.Kp / 64;
-    const int64_t slots = p.num_sms > 0 ? p.num_sms : 1;
+    const int64_t slots = (p.num_sms > 0 ? p.num_sms : 1) * MINB;
     int64_t best = 1, best_cost = INT64_MAX;
     for (int64_t sp = 1; sp <= KT && sp <= 64; ++sp) {
         const int64_t cost = ((tiles * sp + slots - 1) / slots) * ((KT + sp - 1) / sp + BSP_NARROW_CTA_COST);
