@@ -5,7 +5,7 @@ out 5120x5120, FC1 20480x5120, FC2 5120x20480), fp16, 50% magnitude-style
 unstructured mask, synthetic N(0, 0.02) weights (no checkpoints needed).
 One step = bsp_spmm on every layer at N = 1, 2, 8, 16, plus bsp_spmspv on
 FC2 with a post-ReLU activation (~85% zeros): 17 launches of the decode
-kernel.  The step's working set (354 MB of encoded weights) is larger than
+kernels.  The step's working set (354 MB of encoded weights) is larger than
 L2 (129 MB), and each layer is re-read only after the three others have
 passed through L2.
 
@@ -41,11 +41,11 @@ NS = (1, 2, 8, 16)
 PREFILL_LAYERS = [("llama_up", 28672, 8192), ("llama_down", 8192, 28672)]
 PREFILL_NS = (256, 1024, 4096)
 METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
-# kernels of the decode step and their sources: fp16 N <= 2 and spMspV on
-# the GT-per-warp kernel, N = 3..8 on the team kernel, N >= 9 on the narrow
-# tcgen05 kernel
-STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_decode_kernel (N=8) + spmm_narrow_kernel (N=16)"
-STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu")
+# kernels of the decode step and their sources (with the dispatch): fp16
+# N <= 2 and spMspV on the GT-per-warp kernel, N = 3, 4 on the team kernel,
+# N >= 5 on the narrow tcgen05 kernel
+STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_narrow_kernel (N=8, 16)"
+STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu")
 FALLBACK_HBM_GBS = 6800.0
 
 

@@ -83,12 +83,13 @@ bool shape_ok(bsp_dtype_t dtype, int64_t M, int64_t K)
 
 // Smallest fp16 N (up to BSP_DECODE_MAX_N) that runs the tcgen05 narrow
 // kernel instead of the CUDA-core decode kernels.  Measured on the OPT-13B
-// projections: the narrow kernel runs at about 1.25 TB/s for every N (its
-// decode sets the pace), the CUDA-core kernels at 2.58 TB/s at N = 1, 1.29
-// at N = 8 and 0.83 at N = 16 (FMA issue grows with N).  BSP_NARROW_MIN_N
-// overrides it (17 or more: never).
+// projections (four layers rotating through L2): the narrow kernel runs at
+// 1.65 TB/s at N = 3 and 1.48 at N = 16 (its decode sets the pace), the
+// CUDA-core team kernel at 1.71 TB/s at N = 3, 1.68 at N = 4, 1.39 at N = 5
+// and 1.32 at N = 8 (FMA issue grows with N).  BSP_NARROW_MIN_N overrides
+// it (17 or more: never).
 #ifndef BSP_NARROW_MIN_N_DEFAULT
-#define BSP_NARROW_MIN_N_DEFAULT 9
+#define BSP_NARROW_MIN_N_DEFAULT 5
 #endif
 int64_t narrow_min_n()
 {

@@ -33,9 +33,9 @@ def _capture(fn):
     return g
 
 
-@pytest.mark.parametrize("N", [1, 2, 5, 16, 40])
+@pytest.mark.parametrize("N", [1, 2, 4, 5, 16, 40])
 def test_spmm_graph_replay(N):
-    """N = 1, 2: GT-per-warp kernel; 5: team kernel; 16: narrow tcgen05
+    """N = 1, 2: GT-per-warp kernel; 4: team kernel; 5, 16: narrow tcgen05
     kernel; 40: prefill tcgen05 kernel."""
     M, K = 512, 2048
     W = synth.weights_f16(M, K, 0.5, "uniform", 600 + N)
