@@ -389,15 +389,18 @@ union_spmm_kernel(const UArgs a)
                 const int ra = ar >> 1, ca = ar & 1;
                 const uint32_t e = (uint32_t)ar * P + r;  // value index of the segment's first rank
                 uint32_t v4;
+                // the funnel shift takes its amount modulo 32: pos << 3 is
+                // 8 (pos % 4), np << 2 is 4 (np % 8)
                 if constexpr (BITS == 8) {
                     const uint32_t pos = shift + e;
-                    v4 = __funnelshift_r(vw[pos >> 2], vw[(pos >> 2) + 1], 8 * (pos & 3));
+                    v4 = __funnelshift_r(vw[pos >> 2], vw[(pos >> 2) + 1], pos << 3);
                 } else {
                     const uint32_t np = 2 * shift + e;  // nibble position
-                    const uint32_t v16 = __funnelshift_r(vw[np >> 3], vw[(np >> 3) + 1], 4 * (np & 7));
-                    // four signed nibbles -> four signed bytes
-                    const uint32_t v = __byte_perm(v16 & 0x0F0Fu, (v16 >> 4) & 0x0F0Fu, 0x5140);
-                    v4 = v | ((v & 0x08080808u) * 0x1Eu);
+                    const uint32_t v16 = __funnelshift_r(vw[np >> 3], vw[(np >> 3) + 1], np << 2);
+                    // four signed nibbles into the high halves of four bytes:
+                    // each byte is 16 v, so dp4a accumulates 16 times the
+                    // product, divided out (exactly) after the reduction
+                    v4 = __byte_perm((v16 << 4) & 0xF0F0u, v16 & 0xF0F0u, 0x5140);
                 }
                 const int wv = (int)__byte_perm(v4, 0u, sel);
 #pragma unroll
@@ -443,6 +446,7 @@ union_spmm_kernel(const UArgs a)
         int32_t sum = 0;
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) sum += red[w * 64 * NT + i];
+        if constexpr (BITS == 4) sum >>= 4;  // a multiple of 16: exact
         const int64_t m = gi * 64 + rr;
         if (n < N && m < M) {
             if (a.splits == 1) a.Y[(int64_t)n * M + m] = sum;
@@ -580,6 +584,9 @@ bsp_status_t union_encode(const int8_t* W, int bits, int64_t M, int64_t K, bool 
     *out = nullptr;
     if (!W || (bits != 4 && bits != 8)) return BSP_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || (K % 16) != 0) return BSP_ERR_SHAPE;
+    // W4A4 accumulates 16 times each product: exact while 16 |sum| < 2^31,
+    // which |w x| <= 64 and K < 2^21 guarantee
+    if (bits == 4 && K >= ((int64_t)1 << 21)) return BSP_ERR_SHAPE;
     if (!aligned16(W)) return BSP_ERR_ALIGN;
     bsp_union* h = new (std::nothrow) bsp_union{};
     if (!h) return BSP_ERR_OOM;

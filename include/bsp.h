@@ -341,7 +341,9 @@ typedef struct {
  * Encode an integer weight into IE-BME on the device.
  *   W      device int8 [M][K], values in the signed `bits`-bit range
  *          (bits 4: -8..7, BSP_ERR_INVALID_ARG otherwise), 16-B aligned.
- *   M, K   M >= 1, K a multiple of 16 (BSP_ERR_SHAPE otherwise).
+ *   M, K   M >= 1, K a multiple of 16; bits = 4: K < 2^21, so that the
+ *          W4A4 product's int32 accumulation of 16 w x stays exact
+ *          (BSP_ERR_SHAPE otherwise).
  *   stream ordered on it; synchronises it (sizes the values array), so W may
  *          be freed on return.
  *   out    a new handle owning its device arrays and an int32 split-K

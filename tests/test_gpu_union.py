@@ -89,6 +89,19 @@ def test_spmm_extremes_int8():
     assert np.all(Y == 128 * 128 * 4096)
 
 
+@pytest.mark.parametrize("w,x", [(-8, -8), (7, -8), (-8, 7)])
+def test_spmm_extremes_int4(w, x):
+    """Dense int4 extremes, N = 3: exact int32 (the int4 path accumulates
+    16 w x per product and divides by 16 after the reduction)."""
+    K = 8192
+    W = np.full((192, K), w, dtype=np.int8)
+    X = np.full((3, K), x, dtype=np.int8)
+    A = bsp.UnionMatrix(_dev(W), 4)
+    Y = A.spmm(_dev(X)).cpu().numpy().astype(np.int64)
+    A.check()
+    assert np.all(Y == w * x * K)
+
+
 def test_all_zero_weight():
     W = np.zeros((128, 256), dtype=np.int8)
     A = bsp.UnionMatrix(_dev(W), 4)
@@ -118,6 +131,8 @@ def test_errors():
     assert L.bsp_union_encode(W.data_ptr(), 5, 64, 64, None, ctypes.byref(h)) == 1    # bits
     assert L.bsp_union_encode(W.data_ptr(), 4, 64, 60, None, ctypes.byref(h)) == 2    # K % 16
     assert L.bsp_union_encode(W.data_ptr() + 1, 4, 64, 48, None, ctypes.byref(h)) == 4  # alignment
+    Wk = torch.zeros((1, 1 << 21), dtype=torch.int8, device=DEV)
+    assert L.bsp_union_encode(Wk.data_ptr(), 4, 1, 1 << 21, None, ctypes.byref(h)) == 2  # W4 K >= 2^21
     W8 = torch.full((64, 64), 9, dtype=torch.int8, device=DEV)
     assert L.bsp_union_encode(W8.data_ptr(), 4, 64, 64, None, ctypes.byref(h)) == 1   # outside int4
     torch.cuda.synchronize()
