@@ -26,7 +26,7 @@
 // Warp roles (21 warps): warp 0 C producer; warp 1 TMEM allocation and the
 // MMA issuer (tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 16, K = 16);
 // warps 2-3 scanners (row starts of every BT row); warps 4-19 decoders
-// (half row-bytes into the swizzled A tile); warp 20 B producer; warps 4-7
+// (whole row-bytes into the swizzled A tile); warp 20 B producer; warps 4-7
 // then the epilogue (tcgen05.ld of their TMEM lane quadrant).
 // Every wait is bounded; a wait that gives up stores BSP_ERR_TIMEOUT in the
 // error word, and the CTA still drains its copies, waits for its MMAs and
@@ -66,8 +66,8 @@ constexpr int BM = 128, BN = 16, BK = 64;  // tile rows, MMA columns, GT columns
 constexpr int A_BYTES = BM * BK * 2;       // 16384
 constexpr int DEC_WARPS = 16;              // eight per GroupTile
 constexpr int WPG = DEC_WARPS / 2;         // decoder warps per GroupTile
-constexpr int NU = 32 / WPG;               // units (half row-bytes) per lane and step
-constexpr int TCW = NU / 2;                // TCTile columns per warp
+constexpr int NR = 2;                      // row-bytes per decoder lane and step
+static_assert(WPG * 32 * NR == 512, "the decoder warps of a GT cover its 64 x 8 row-bytes");
 constexpr int DEC0 = 4;                    // first decoder warp (after producer, MMA, 2 scanners)
 constexpr int BPROD = DEC0 + DEC_WARPS;    // B (X tile) producer, the last warp
 constexpr int WARPS = BPROD + 1;
@@ -425,29 +425,24 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
         }
     } else if (warp < BPROD) {
-        // ---------------- decoders.  Unit j of a lane: row 16q + 8 (lane / 16)
-        // + lane % 8 of the GT, octet bc = 2 (p0 + j / 2) + j % 2, and of its
-        // 8 positions the low (lane bit 3 clear) or the high half.  One unit
-        // of a warp reads the values of two BTs adjacent in value order
-        // (about 128 B at 50% density); each half-warp writes eight whole
-        // 16-B chunks of eight consecutive rows, which the swizzle puts in
-        // distinct banks.
+        // ---------------- decoders.  Row-byte j of a lane: row 16q + lane % 16
+        // of the GT, octet bc = 2 p0 + 2 (lane / 16) + j; its eight positions
+        // become one whole 16-B chunk of the A tile.  Each quarter-warp
+        // writes the chunks of eight consecutive rows of one octet, which the
+        // swizzle puts in distinct banks.
         const int dw = warp - DEC0;
         const int gsel = dw / WPG, wq = dw % WPG;
-        const int q = wq / (4 / TCW);           // TCTile row of the warp (16 GT rows)
-        const int p0 = (wq % (4 / TCW)) * TCW;  // first TCTile column (octet pair)
-        const int row = 16 * q + 8 * (lane >> 4) + (lane & 7);  // row inside the GT
-        const int trow = 64 * gsel + row;                       // row inside the 128-row tile
-        const int half = (lane >> 3) & 1;
-        const uint32_t nsh = 4u * (uint32_t)half;  // the lane's half of the row-byte
-        const uint32_t lowm = half ? 0xFu : 0u;    // positions before it
-        int ent[NU];       // BT row entry: 8 g + row % 8 (bitmap byte / row start)
-        uint32_t dst[NU];  // byte offset of the unit's 8 bytes in A (128-B swizzle)
+        const int q = wq / 2;         // TCTile row of the warp (16 GT rows)
+        const int p0 = (wq % 2) * 2;  // first TCTile column (octet pair) of the warp
+        const int row = 16 * q + (lane & 15);  // row inside the GT
+        const int trow = 64 * gsel + row;      // row inside the 128-row tile
+        int ent[NR];       // BT row entry: 8 g + row % 8 (bitmap byte / row start)
+        uint32_t dst[NR];  // byte offset of the row-byte's 16-B chunk in A (128-B swizzle)
 #pragma unroll
-        for (int j = 0; j < NU; ++j) {
-            const int bc = 2 * (p0 + j / 2) + (j & 1);
+        for (int j = 0; j < NR; ++j) {
+            const int bc = 2 * p0 + 2 * (lane >> 4) + j;
             ent[j] = 8 * bt_local(row >> 3, bc) + (row & 7);
-            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4) + 8 * half);
+            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4));
         }
         const bool active = gsel == 0 || has_b;
         uint32_t sc = 0, pc = 0, sa = 0, pa = 0;
@@ -463,24 +458,24 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + C_RS + gsel * RS_BYTES);
                 const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
 #pragma unroll
-                for (int j = 0; j < NU; ++j) {
+                for (int j = 0; j < NR; ++j) {
                     const uint32_t byte = bmb[ent[j]];
-                    uint32_t start = (uint32_t)rst[ent[j]] + (uint32_t)__popc(byte & lowm);
+                    uint32_t start = (uint32_t)rst[ent[j]];
 #if BSP_NW_CHECKS
-                    if (2u * (start + 4u) > SLOT - 512u) { atomicCAS(a.err, 0, 110); start = 0; }
+                    if (2u * (start + 8u) > SLOT - 512u) { atomicCAS(a.err, 0, 110); start = 0; }
 #endif
-                    const uint32_t nib = byte >> nsh;
                     uint32_t addr = vbase + 2u * start;
-                    uint32_t h[4];
+                    uint32_t h[8];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) h[c] = take_f16(addr, nib, 1u << c);
-                    *reinterpret_cast<uint2*>(at + dst[j]) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+                    for (int c = 0; c < 8; ++c) h[c] = take_f16(addr, byte, 1u << c);
+                    *reinterpret_cast<uint4*>(at + dst[j]) =
+                        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
                 }
             } else {
                 // rows of a missing second strip: zeros, so that the MMA
                 // reads defined values (their Y rows are not written)
 #pragma unroll
-                for (int j = 0; j < NU; ++j) *reinterpret_cast<uint2*>(at + dst[j]) = make_uint2(0u, 0u);
+                for (int j = 0; j < NR; ++j) *reinterpret_cast<uint4*>(at + dst[j]) = make_uint4(0u, 0u, 0u, 0u);
             }
             // make the generic-proxy writes of A visible to the tensor cores
             bspx::fence_proxy_async_smem();
