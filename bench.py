@@ -45,6 +45,15 @@ METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
 # N <= 2 and spMspV on the GT-per-warp kernel, N = 3, 4 on the team kernel,
 # N >= 5 on the narrow tcgen05 kernel
 STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_narrow_kernel (N=8, 16)"
+
+
+def step_kernel(key):
+    """The kernel a call of the step launches, by the library's fp16
+    dispatch (BSP_NARROW_MIN_N, default 5, as in bsp_api.cu)."""
+    _, N = key
+    if N == "spmspv" or N <= 2:
+        return "spmm_decode_gtw_kernel"
+    return "spmm_narrow_kernel" if N >= int(os.environ.get("BSP_NARROW_MIN_N", "5")) else "spmm_decode_kernel"
 STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -420,6 +429,15 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     launch_ms = sum(statistics.mean(v) for v in per_call.values())
     achieved = step_bytes / (launch_ms * 1e-3) / 1e9
+    # per kernel: algorithmic bytes and mean launch time of its calls; the
+    # dominant kernel (largest share of the launch time) gives the roofline
+    by_kernel = {}
+    for k, _ in calls:
+        e = by_kernel.setdefault(step_kernel(k), {"launches": 0, "bytes": 0, "ms": 0.0})
+        e["launches"] += 1
+        e["bytes"] += bpc[k]
+        e["ms"] += statistics.mean(per_call[k])
+    dom = max(by_kernel, key=lambda n: by_kernel[n]["ms"])
 
     breakdown = {}
     for N in NS:
@@ -434,12 +452,14 @@ def run_gpu(args):
                                "speedup_vs_spmm_n1": round(statistics.median(per_call[("fc2", 1)]) / t_sp, 3)}
 
     traffic = None
+    traffic_kernels = {}
     tp = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if os.path.exists(tp):
         with open(tp) as f:
             tr = json.load(f)
         if tr.get("kernel_source_hash") == _kernel_hash():
-            traffic = tr.get("dram_bytes_per_launch")
+            traffic_kernels = tr.get("kernels", {})
+            traffic = traffic_kernels.get(dom, {}).get("dram_bytes_per_launch")
 
     # ---- e2e: same step through the host-buffer C-ABI call
     e2e = None
@@ -480,6 +500,22 @@ def run_gpu(args):
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = time_oracle(Ws, xs, relu, bpc, stor, target_s=10.0)
 
+    d = by_kernel[dom]
+    dach = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dach, 1), "peak": peak, "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": round(dach / peak, 4),
+                "algorithmic_bytes_per_launch": round(d["bytes"] / d["launches"]),
+                "launches_per_step": d["launches"], "share_of_step_time": round(d["ms"] / launch_ms, 4),
+                "traffic": traffic,
+                "by_kernel": {n: {"launches_per_step": e["launches"],
+                                  "achieved": round(e["bytes"] / (e["ms"] * 1e-3) / 1e9, 1),
+                                  "frac": round(e["bytes"] / (e["ms"] * 1e-3) / 1e9 / peak, 4),
+                                  "share_of_step_time": round(e["ms"] / launch_ms, 4),
+                                  "traffic": traffic_kernels.get(n, {}).get("dram_bytes_per_launch")}
+                              for n, e in by_kernel.items()},
+                "step": {"kernels": STEP_KERNELS, "achieved": round(achieved, 1),
+                         "frac": round(achieved / peak, 4),
+                         "algorithmic_bytes_per_launch": round(step_bytes / n_calls)}}
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -488,12 +524,7 @@ def run_gpu(args):
                 "config": _config(), "frac_hbm": round(value / ws / peak, 4),
                 "breakdown": breakdown, "prefill": prefill, "union_ie_bme": union,
                 "sparsity_sweep": sweep,
-                "roofline": {"bound": "hbm",
-                             "kernel": STEP_KERNELS,
-                             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
-                             "unit": "GB/s", "frac": round(achieved / peak, 4),
-                             "algorithmic_bytes_per_launch": round(step_bytes / n_calls),
-                             "traffic": traffic},
+                "roofline": roofline,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * args.steps,
                 "clocks": clk}
         print(json.dumps(line))

@@ -36,3 +36,14 @@ def test_decode_step_bytes_count_weight_x_and_y():
     assert stor["out"] == enc_bytes
     for N in bench.NS:
         assert bpc[("out", N)] == enc_bytes + 2 * 5120 * N + 2 * 5120 * N
+
+
+def test_step_kernel_follows_the_dispatch(monkeypatch):
+    monkeypatch.delenv("BSP_NARROW_MIN_N", raising=False)
+    got = {N: bench.step_kernel(("qkv", N)) for N in (1, 2, 3, 4, 5, 8, 16)}
+    assert got == {1: "spmm_decode_gtw_kernel", 2: "spmm_decode_gtw_kernel", 3: "spmm_decode_kernel",
+                   4: "spmm_decode_kernel", 5: "spmm_narrow_kernel", 8: "spmm_narrow_kernel",
+                   16: "spmm_narrow_kernel"}
+    assert bench.step_kernel(("fc2", "spmspv")) == "spmm_decode_gtw_kernel"
+    monkeypatch.setenv("BSP_NARROW_MIN_N", "17")
+    assert bench.step_kernel(("qkv", 16)) == "spmm_decode_kernel"
