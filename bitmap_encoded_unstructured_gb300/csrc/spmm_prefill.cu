@@ -39,7 +39,9 @@
 //   warps 4-19 decoders: eight per GT, each on 16 of its rows and half of
 //              its columns; per half row-byte one byte of bitmap, one row
 //              start and four predicated shared-memory loads (no branch per
-//              position) give 8 bytes of A; then "a_full" / "c_empty".
+//              position) give 8 bytes of A (with one 256-column sub-tile:
+//              per whole row-byte, eight loads give a 16-B chunk); then
+//              "a_full" / "c_empty".
 //   warps 4-19 after the K loop: epilogue, tcgen05.ld of their TMEM lane
 //              quadrant (warp % 4) and a quarter of the columns, fp32 ->
 //              fp16, stores to Y[n][m].
@@ -540,16 +542,24 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
         // row-bytes per lane would span four BTs.  Each half-warp writes
         // eight whole 16-B chunks of eight consecutive rows, which the
         // swizzle puts in distinct banks.
-        const int row = 16 * q + 8 * (lane >> 4) + (lane & 7);  // row inside the GT
+        //
+        // One 256-column sub-tile (N <= 256): the decode, not shared-memory
+        // bandwidth, sets the pace, so each lane takes whole row-bytes
+        // instead: row 16q + lane % 16, octet 2 p0 + 2 (lane / 16) + j, its
+        // eight positions one 16-B chunk (the same chunk addresses as the
+        // two halves above; fewer instructions, loads spanning four BTs).
+        constexpr bool FULLROW = NSUB == 1 && DEC_WARPS == 16;
+        constexpr int NJ = FULLROW ? 2 : NU;  // row-bytes, or half row-bytes, per lane and step
+        const int row = FULLROW ? 16 * q + (lane & 15) : 16 * q + 8 * (lane >> 4) + (lane & 7);  // row in the GT
         const int trow = 64 * gsel + row;                       // row inside the 128-row tile
-        const int half = (lane >> 3) & 1;
+        const int half = FULLROW ? 0 : (lane >> 3) & 1;
         const uint32_t nsh = 4u * (uint32_t)half;            // the lane's half of the row-byte
         const uint32_t lowm = half ? 0xFu : 0u;              // positions before it
-        int ent[NU];        // BT row entry: 8 g + row % 8 (bitmap byte / row start)
-        uint32_t dst[NU];   // byte offset of the unit's 8 bytes in A (128-B swizzle)
+        int ent[NJ];        // BT row entry: 8 g + row % 8 (bitmap byte / row start)
+        uint32_t dst[NJ];   // byte offset of the unit's 8 (or 16) bytes in A (128-B swizzle)
 #pragma unroll
-        for (int j = 0; j < NU; ++j) {
-            const int bc = 2 * (p0 + j / 2) + (j & 1);
+        for (int j = 0; j < NJ; ++j) {
+            const int bc = FULLROW ? 2 * p0 + 2 * (lane >> 4) + j : 2 * (p0 + j / 2) + (j & 1);
             ent[j] = 8 * bt_local(row >> 3, bc) + (row & 7);
             dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4) + 8 * half);
         }
@@ -566,16 +576,29 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
                 const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + C_RS + gsel * RS_BYTES);
                 const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
                 uint8_t* at = a_stage(sa);
+                if constexpr (FULLROW) {
 #pragma unroll
-                for (int j = 0; j < NU; ++j) {
-                    const uint32_t byte = bmb[ent[j]];
-                    const uint32_t start = (uint32_t)rst[ent[j]] + (uint32_t)__popc(byte & lowm);
-                    const uint32_t nib = byte >> nsh;
-                    uint32_t addr = vbase + 2u * start;
-                    uint32_t h[4];
+                    for (int j = 0; j < NJ; ++j) {
+                        const uint32_t byte = bmb[ent[j]];
+                        uint32_t addr = vbase + 2u * (uint32_t)rst[ent[j]];
+                        uint32_t h[8];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) h[c] = take_f16(addr, nib, 1u << c);
-                    *reinterpret_cast<uint2*>(at + dst[j]) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+                        for (int c = 0; c < 8; ++c) h[c] = take_f16(addr, byte, 1u << c);
+                        *reinterpret_cast<uint4*>(at + dst[j]) = make_uint4(
+                            h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        const uint32_t byte = bmb[ent[j]];
+                        const uint32_t start = (uint32_t)rst[ent[j]] + (uint32_t)__popc(byte & lowm);
+                        const uint32_t nib = byte >> nsh;
+                        uint32_t addr = vbase + 2u * start;
+                        uint32_t h[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) h[c] = take_f16(addr, nib, 1u << c);
+                        *reinterpret_cast<uint2*>(at + dst[j]) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+                    }
                 }
             }
             // make the generic-proxy writes of A visible to the tensor cores
