@@ -208,3 +208,16 @@ def test_permuted_encoding_round_trip(bits):
             tile = W[ti * 64:(ti + 1) * 64, tj * 64:(tj + 1) * 64][perms[t]]
             assert int(enc["offsets"][t + 1] - enc["offsets"][t]) == 4 * u.union_active(tile, 2, 2)
             t += 1
+
+
+def test_pmr_of_the_fig7_example():
+    """UnionSparse's PMR for the Fig. 7 LT in W4: 40 nonzeros are 20 payload
+    bytes; the LT stores 2 offsets (8 B), one mask word (8 B) and 160 int4
+    values (80 B), so the rest is 96 - 20 = 76 bytes."""
+    enc = u.union_encode(_fig7_weight(), 4, lt=(8, 32), areas=(2, 2))
+    assert enc["nnz"] == 40
+    assert u.storage_bytes(enc) == 96
+    assert u.payload_to_metadata(enc) == 20 / 76
+    # W8: 40 payload bytes of 8 + 8 + 160
+    enc8 = u.union_encode(_fig7_weight(), 8, lt=(8, 32), areas=(2, 2))
+    assert u.payload_to_metadata(enc8) == 40 / (176 - 40)

@@ -379,3 +379,18 @@ def test_prune_activations_i8():
     x = np.array([-127, -60, -59, 0, 59, 60, 61, 127], dtype=np.int8)
     np.testing.assert_array_equal(oracle.prune_activations_i8(x, 60),
                                   np.array([-127, 0, 0, 0, 0, 0, 61, 127], dtype=np.int8))
+
+
+# ----------------------------------------------------------- payload-to-metadata ratio
+
+def test_pmr_of_dense_and_half_dense_grouptiles():
+    """PMR = value bytes / (bitmap + offset bytes), counted by hand: one
+    64 x 64 GroupTile holds 64 bitmaps (512 B) and two offsets (8 B)."""
+    dense = _f16(np.full((64, 64), 0.5))
+    assert oracle.payload_to_metadata(oracle.encode(dense)) == 8192 / 520
+    half = dense.copy()
+    half[:, ::2] = 0                       # 2048 values of 2 B
+    assert oracle.payload_to_metadata(oracle.encode(half)) == 4096 / 520
+    two = np.zeros((64, 128), dtype=np.uint16)
+    two[3, 70] = dense[0, 0]               # one value, two GroupTiles: 128 bitmaps + 3 offsets
+    assert oracle.payload_to_metadata(oracle.encode(two)) == 2 / (1024 + 12)
