@@ -45,20 +45,20 @@ METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
 # N <= 2 and spMspV on the GT-per-warp kernel, N = 3, 4 on the team kernel,
 # N >= 5 on the narrow tcgen05 kernel
 STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_narrow_kernel (N=8, 16)"
+STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu")
+NARROW_MIN_N_DEFAULT = 5  # BSP_NARROW_MIN_N_DEFAULT of bsp_api.cu (a CPU test holds them equal)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0
 
 
 def step_kernel(key):
     """The kernel a call of the step launches, by the library's fp16
-    dispatch (BSP_NARROW_MIN_N, default 5, as in bsp_api.cu)."""
+    dispatch (BSP_NARROW_MIN_N, else the library's default)."""
     _, N = key
     if N == "spmspv" or N <= 2:
         return "spmm_decode_gtw_kernel"
-    return "spmm_narrow_kernel" if N >= int(os.environ.get("BSP_NARROW_MIN_N", "5")) else "spmm_decode_kernel"
-STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu")
-FALLBACK_HBM_GBS = 6800.0
-
-
-FALLBACK_TFLOPS = 1900.0
+    min_n = int(os.environ.get("BSP_NARROW_MIN_N", str(NARROW_MIN_N_DEFAULT)))
+    return "spmm_narrow_kernel" if N >= min_n else "spmm_decode_kernel"
 
 
 def _peaks():

@@ -47,3 +47,12 @@ def test_step_kernel_follows_the_dispatch(monkeypatch):
     assert bench.step_kernel(("fc2", "spmspv")) == "spmm_decode_gtw_kernel"
     monkeypatch.setenv("BSP_NARROW_MIN_N", "17")
     assert bench.step_kernel(("qkv", 16)) == "spmm_decode_kernel"
+
+
+def test_step_kernel_default_is_the_librarys():
+    """bench.step_kernel labels the step's launches with the library's
+    default fp16 dispatch threshold, read here from its source."""
+    import re
+    src = open(os.path.join(ROOT, "bitmap_encoded_unstructured_gb300", "csrc", "bsp_api.cu")).read()
+    m = re.search(r"#define\s+BSP_NARROW_MIN_N_DEFAULT\s+(\d+)", src)
+    assert m and int(m.group(1)) == bench.NARROW_MIN_N_DEFAULT
