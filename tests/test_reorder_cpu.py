@@ -74,3 +74,43 @@ def test_argument_errors():
     assert L.bsp_reorder_rows(T.ctypes.data, 64, 64, 4, 2, 0, perm.ctypes.data, ctypes.byref(c)) == 2  # heuristic, RA != 2
     assert L.bsp_reorder_rows(T.ctypes.data, 63, 64, 2, 2, 0, perm.ctypes.data, ctypes.byref(c)) == 2  # RA does not divide H
     assert L.bsp_reorder_rows(None, 8, 8, 2, 2, 1, perm.ctypes.data, ctypes.byref(c)) == 1
+
+
+def _matching_optimum(T):
+    """With groups of two rows and two column areas the grouped cost is a sum
+    over pairs of popcount(folded(a) | folded(b)), so its minimum over all
+    groupings is a minimum-weight perfect matching (networkx, Edmonds)."""
+    nx = pytest.importorskip("networkx")
+    nz = T != 0
+    f = nz[:, : T.shape[1] // 2] | nz[:, T.shape[1] // 2:]
+    G = nx.Graph()
+    H = T.shape[0]
+    for a in range(H):
+        for b in range(a + 1, H):
+            G.add_edge(a, b, weight=-int((f[a] | f[b]).sum()))
+    m = nx.max_weight_matching(G, maxcardinality=True)
+    assert len(m) == H // 2
+    return sum(int((f[a] | f[b]).sum()) for a, b in m)
+
+
+@pytest.mark.parametrize("H,KL,p", [(8, 16, 0.3), (12, 32, 0.25), (16, 64, 0.5), (20, 64, 0.1)])
+def test_oracle_dp_is_the_matching_optimum(H, KL, p):
+    """The oracle's subset DP against an independent library optimum."""
+    T = _tile(H, KL, p, 7 * H + KL).astype(np.int64)
+    _, cost = u.reorder_rows(T, 2, 2)
+    assert cost == _matching_optimum(T)
+
+
+@pytest.mark.parametrize("p", [0.5, 0.3, 0.1])
+def test_pairing_heuristic_near_the_matching_optimum(p):
+    """On 64-row tiles the library's heuristic stays within 3% of the
+    optimum (measured gaps: about 1% at 50% density, 2.6% at 10%)."""
+    tot_h = tot_o = 0
+    for seed in range(6):
+        T = _tile(64, 64, p, 1000 + seed + int(100 * p))
+        _, cost = bsp.bsp_reorder_rows(T, 2, 2, exact=False)
+        opt = _matching_optimum(T)
+        assert cost >= opt
+        tot_h += cost
+        tot_o += opt
+    assert tot_h <= 1.03 * tot_o
