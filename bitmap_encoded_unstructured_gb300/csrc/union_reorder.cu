@@ -15,7 +15,9 @@
 //    pairing, where the DP's 2^64 states are out of reach): the better of
 //    the identity pairing and a greedy pairing (the smallest free row with
 //    its cheapest free partner), each improved by pair swaps ((a, b), (c,
-//    d) -> (a, c), (b, d) or (a, d), (b, c)) while a swap lowers the cost.
+//    d) -> (a, c), (b, d) or (a, d), (b, c)) while a swap lowers the cost,
+//    then an iterated local search (re-pair a few random pairs, descend
+//    again, keep what is cheaper).
 // Either result is made canonical as on the page: rows ascending inside a
 // group, groups in lexicographic order, and the permutation taken
 // partition-wise (the p-th row of every group, for p = 0 .. R_A - 1).
@@ -88,42 +90,74 @@ int64_t solve_dp(const uint64_t* act, int H, int RA, std::vector<std::vector<int
     return F[full];
 }
 
-int64_t pair_cost(const uint64_t* act, const std::vector<std::pair<int, int>>& P)
+// cost of every row pair of a tile: popcount(act[a] | act[b]), computed once
+struct PairCosts {
+    int H;
+    std::vector<uint8_t> c;
+    PairCosts(const uint64_t* act, int h) : H(h), c((size_t)h * h)
+    {
+        for (int a = 0; a < H; ++a)
+            for (int b = a; b < H; ++b)
+                c[(size_t)a * H + b] = c[(size_t)b * H + a] = (uint8_t)popc64(act[a] | act[b]);
+    }
+    int operator()(int a, int b) const { return c[(size_t)a * H + b]; }
+};
+
+int64_t pair_cost(const PairCosts& C, const std::vector<std::pair<int, int>>& P)
 {
     int64_t c = 0;
-    for (auto& p : P) c += popc64(act[p.first] | act[p.second]);
+    for (auto& p : P) c += C(p.first, p.second);
     return c;
 }
 
-// pair swaps while one lowers the cost
-void improve_pairs(const uint64_t* act, std::vector<std::pair<int, int>>& P)
+// pair swaps ((a, b), (c, d) -> (a, c), (b, d) or (a, d), (b, c)) that
+// involve a pair of the worklist, until none lowers the cost; a pair that
+// changes joins the worklist.  Started with every pair listed, it ends in a
+// grouping where no swap helps; started from such a grouping with only the
+// pairs changed since listed, it ends in one again, at O(worklist x pairs)
+// cost.  Every swap lowers an integer cost, so it ends.
+void improve_from(const PairCosts& C, std::vector<std::pair<int, int>>& P, std::vector<int>& work)
 {
     const int np = (int)P.size();
-    for (int pass = 0; pass < 4 * np; ++pass) {
-        bool changed = false;
-        for (int x = 0; x < np; ++x)
-            for (int y = x + 1; y < np; ++y) {
-                const int a = P[x].first, b = P[x].second, c = P[y].first, d = P[y].second;
-                const int now = popc64(act[a] | act[b]) + popc64(act[c] | act[d]);
-                const int s1 = popc64(act[a] | act[c]) + popc64(act[b] | act[d]);
-                const int s2 = popc64(act[a] | act[d]) + popc64(act[b] | act[c]);
-                if (s1 < now && s1 <= s2) {
-                    P[x] = {a, c};
-                    P[y] = {b, d};
-                    changed = true;
-                } else if (s2 < now) {
-                    P[x] = {a, d};
-                    P[y] = {b, c};
-                    changed = true;
-                }
+    std::vector<char> queued(np, 0);
+    for (int x : work) queued[x] = 1;
+    for (size_t it = 0; it < work.size(); ++it) {
+        const int x = work[it];
+        queued[x] = 0;
+        for (int y = 0; y < np; ++y) {
+            if (y == x) continue;
+            const int a = P[x].first, b = P[x].second, c = P[y].first, d = P[y].second;
+            const int now = C(a, b) + C(c, d);
+            const int s1 = C(a, c) + C(b, d);
+            const int s2 = C(a, d) + C(b, c);
+            if (s1 >= now && s2 >= now) continue;
+            if (s1 <= s2) {
+                P[x] = {a, c};
+                P[y] = {b, d};
+            } else {
+                P[x] = {a, d};
+                P[y] = {b, c};
             }
-        if (!changed) break;
+            if (!queued[y]) {
+                queued[y] = 1;
+                work.push_back(y);
+            }
+        }
     }
 }
+
+// iterated local search of the pairing heuristic: rounds, pairs re-paired per round
+#ifndef BSP_REORDER_ROUNDS
+#define BSP_REORDER_ROUNDS 192
+#endif
+#ifndef BSP_REORDER_KICK
+#define BSP_REORDER_KICK 3
+#endif
 
 int64_t solve_pairs(const uint64_t* act, int H, std::vector<std::vector<int>>& groups)
 {
     const int h = H / 2;
+    const PairCosts C(act, H);
     std::vector<std::pair<int, int>> ident, greedy;
     for (int i = 0; i < h; ++i) ident.push_back({i, h + i});
     std::vector<char> used(H, 0);
@@ -133,22 +167,64 @@ int64_t solve_pairs(const uint64_t* act, int H, std::vector<std::vector<int>>& g
         int best = -1, bc = 1 << 30;
         for (int q = r + 1; q < H; ++q) {
             if (used[q]) continue;
-            const int c = popc64(act[r] | act[q]);
-            if (c < bc) {
-                bc = c;
+            if (C(r, q) < bc) {
+                bc = C(r, q);
                 best = q;
             }
         }
         used[best] = 1;
         greedy.push_back({r, best});
     }
-    improve_pairs(act, ident);
-    improve_pairs(act, greedy);
-    const int64_t ci = pair_cost(act, ident), cg = pair_cost(act, greedy);
-    const auto& P = cg < ci ? greedy : ident;
+    std::vector<int> all(h);
+    for (int i = 0; i < h; ++i) all[i] = i;
+    std::vector<int> work = all;
+    improve_from(C, ident, work);
+    work = all;
+    improve_from(C, greedy, work);
+    const int64_t ci = pair_cost(C, ident), cg = pair_cost(C, greedy);
+    std::vector<std::pair<int, int>> best = cg < ci ? greedy : ident;
+    int64_t best_cost = cg < ci ? cg : ci;
+    // iterated local search: re-pair the rows of KICK random pairs of the
+    // best grouping, descend again from those pairs, keep the result if it
+    // is cheaper.  The random source is a fixed-seed xorshift, so the
+    // grouping is a function of the tile alone.
+    constexpr int ROUNDS = BSP_REORDER_ROUNDS, KICK = BSP_REORDER_KICK;
+    if (h > KICK) {
+        uint64_t rs = 0x9E3779B97F4A7C15ull;
+        auto next = [&rs]() {
+            rs ^= rs << 13;
+            rs ^= rs >> 7;
+            rs ^= rs << 17;
+            return rs;
+        };
+        std::vector<std::pair<int, int>> P;
+        for (int round = 0; round < ROUNDS && best_cost > 0; ++round) {
+            P = best;
+            int pick[KICK], rows[2 * KICK];
+            for (int k = 0; k < KICK; ++k) {
+                bool fresh;
+                do {  // KICK distinct pairs
+                    pick[k] = (int)(next() % (uint64_t)h);
+                    fresh = true;
+                    for (int q = 0; q < k; ++q) fresh = fresh && pick[q] != pick[k];
+                } while (!fresh);
+                rows[2 * k] = P[pick[k]].first;
+                rows[2 * k + 1] = P[pick[k]].second;
+            }
+            for (int i = 2 * KICK - 1; i > 0; --i) std::swap(rows[i], rows[next() % (uint64_t)(i + 1)]);
+            for (int k = 0; k < KICK; ++k) P[pick[k]] = {rows[2 * k], rows[2 * k + 1]};
+            work.assign(pick, pick + KICK);
+            improve_from(C, P, work);
+            const int64_t c = pair_cost(C, P);
+            if (c < best_cost) {
+                best_cost = c;
+                best = P;
+            }
+        }
+    }
     groups.clear();
-    for (auto& p : P) groups.push_back({p.first, p.second});
-    return cg < ci ? cg : ci;
+    for (auto& p : best) groups.push_back({p.first, p.second});
+    return best_cost;
 }
 
 }  // namespace

@@ -103,8 +103,8 @@ def test_oracle_dp_is_the_matching_optimum(H, KL, p):
 
 @pytest.mark.parametrize("p", [0.5, 0.3, 0.1])
 def test_pairing_heuristic_near_the_matching_optimum(p):
-    """On 64-row tiles the library's heuristic stays within 3% of the
-    optimum (measured gaps: about 1% at 50% density, 2.6% at 10%)."""
+    """On 64-row tiles the library's heuristic stays within 1.5% of the
+    optimum (measured gaps: 0.14% at 50% density, 0.57% at 10%)."""
     tot_h = tot_o = 0
     for seed in range(6):
         T = _tile(64, 64, p, 1000 + seed + int(100 * p))
@@ -113,4 +113,4 @@ def test_pairing_heuristic_near_the_matching_optimum(p):
         assert cost >= opt
         tot_h += cost
         tot_o += opt
-    assert tot_h <= 1.03 * tot_o
+    assert tot_h <= 1.015 * tot_o
