@@ -12,15 +12,21 @@ Two layers:
 
 The library is loaded on first use; if it is missing or fails to load, the
 call raises ``RuntimeError`` (there is no fallback of any kind).
+
+``test_library()`` routes the calls made inside a ``with`` block to
+``libbsp_test.so``, the test build, which alone exports the switches of
+``include/bsp_testing.h``.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbsp.so")
+TEST_LIB_PATH = os.path.join(_HERE, "libbsp_test.so")
 
 BSP_FP16 = 0
 BSP_INT8 = 1
@@ -53,6 +59,8 @@ SIGNATURES = {
     "bsp_import": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, C.c_uint64, _P, C.POINTER(_P)]),
     "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
     "bsp_set_deterministic": (C.c_int, [_P, C.c_int]),
+    "bsp_set_tuning": (C.c_int, [C.c_int, _I64]),
+    "bsp_get_tuning": (C.c_int, [C.c_int, C.POINTER(_I64)]),
     "bsp_union_encode": (C.c_int, [_P, C.c_int, _I64, _I64, _P, C.POINTER(_P)]),
     "bsp_union_destroy": (C.c_int, [_P]),
     "bsp_union_spmm": (C.c_int, [_P, _P, _I64, _P, _P]),
@@ -65,6 +73,16 @@ SIGNATURES = {
     "bsp_union_export_perms": (C.c_int, [_P, _P, _P]),
     "bsp_reorder_rows": (C.c_int, [_P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, C.POINTER(_I64)]),
 }
+
+# Entry points of the test build only (include/bsp_testing.h).
+TESTING_SIGNATURES = {
+    "bsp_testing_set_stall": (C.c_int, [C.c_int]),
+    "bsp_testing_set_spin_cap": (C.c_int, [C.c_uint32]),
+}
+
+# bsp_tune_t of include/bsp.h
+TUNE = {"splitk": 0, "narrow_splitk": 1, "union_splitk": 2, "narrow_min_n": 3,
+        "prefill_ksplit": 4, "prefill_cstages": 5}
 
 
 class bsp_info_t(C.Structure):
@@ -89,23 +107,79 @@ class BspError(RuntimeError):
 
 
 _lib = None
+_test_lib = None
+_use_test = 0
 _lock = threading.Lock()
 
 
+def _load(path: str, sigs: dict) -> C.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing")
+    L = C.CDLL(path)
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+def testing_lib() -> C.CDLL:
+    """Load libbsp_test.so, the test build (same kernels, plus the switches
+    of include/bsp_testing.h)."""
+    global _test_lib
+    with _lock:
+        if _test_lib is None:
+            _test_lib = _load(TEST_LIB_PATH, {**SIGNATURES, **TESTING_SIGNATURES})
+        return _test_lib
+
+
 def lib() -> C.CDLL:
-    """Load libbsp.so (built by ``build.build_library`` / ``__graft_entry__.build``)."""
+    """Load libbsp.so (built by ``build.build_library`` / ``__graft_entry__.build``);
+    inside ``test_library()``, the test build instead."""
     global _lib
+    if _use_test:
+        return testing_lib()
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing")
-            L = C.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = _load(LIB_PATH, SIGNATURES)
         return _lib
+
+
+@contextlib.contextmanager
+def test_library():
+    """Route this module's calls to libbsp_test.so inside the block.  Handles
+    made inside must be used and closed inside."""
+    global _use_test
+    L = testing_lib()
+    _use_test += 1
+    try:
+        yield L
+    finally:
+        _use_test -= 1
+
+
+def set_tuning(knob: str, value: int) -> None:
+    """bsp_set_tuning by name (a key of ``TUNE``)."""
+    _check("bsp_set_tuning", lib().bsp_set_tuning(TUNE[knob], int(value)))
+
+
+def get_tuning(knob: str) -> int:
+    v = C.c_int64()
+    _check("bsp_get_tuning", lib().bsp_get_tuning(TUNE[knob], C.byref(v)))
+    return v.value
+
+
+@contextlib.contextmanager
+def tuning(**knobs):
+    """Set tuning knobs (``TUNE`` names) for the block, then restore them."""
+    old = {k: get_tuning(k) for k in knobs}
+    try:
+        for k, v in knobs.items():
+            set_tuning(k, v)
+        yield
+    finally:
+        for k, v in old.items():
+            set_tuning(k, v)
 
 
 def _check(fn: str, st: int) -> None:

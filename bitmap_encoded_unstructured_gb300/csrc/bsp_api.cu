@@ -81,22 +81,6 @@ bool shape_ok(bsp_dtype_t dtype, int64_t M, int64_t K)
     return (K % (dtype == BSP_INT8 ? 16 : 8)) == 0;
 }
 
-// Smallest fp16 N (up to BSP_DECODE_MAX_N) that runs the tcgen05 narrow
-// kernel instead of the CUDA-core decode kernels.  Measured on the OPT-13B
-// projections (four layers rotating through L2): the narrow kernel runs at
-// 1.65 TB/s at N = 3 and 1.48 at N = 16 (its decode sets the pace), the
-// CUDA-core team kernel at 1.71 TB/s at N = 3, 1.68 at N = 4, 1.39 at N = 5
-// and 1.32 at N = 8 (FMA issue grows with N).  BSP_NARROW_MIN_N overrides
-// it (17 or more: never).
-#ifndef BSP_NARROW_MIN_N_DEFAULT
-#define BSP_NARROW_MIN_N_DEFAULT 5
-#endif
-int64_t narrow_min_n()
-{
-    if (const char* e = std::getenv("BSP_NARROW_MIN_N")) return std::atol(e);
-    return BSP_NARROW_MIN_N_DEFAULT;
-}
-
 bsp_handle* new_handle(bsp_dtype_t dtype, int64_t M, int64_t K)
 {
     bsp_handle* h = new (std::nothrow) bsp_handle{};
@@ -175,7 +159,7 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_str
     cudaStream_t s = (cudaStream_t)stream;
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     if (N <= BSP_DECODE_MAX_N) {
-        if (h->dtype == BSP_FP16 && N >= narrow_min_n())
+        if (h->dtype == BSP_FP16 && N >= bsp_tune(BSP_TUNE_NARROW_MIN_N))
             return bsp_run_spmm_narrow(bsp_problem_of(h), X, N, Y, s);
         return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, mode, nullptr, false, s);
     }

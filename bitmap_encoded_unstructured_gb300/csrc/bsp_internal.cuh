@@ -124,3 +124,35 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
 // slots when those are in use), and the automatic choice alone.
 int bsp_narrow_splits(const bsp_decode_problem& p);
 int bsp_narrow_splits_auto(const bsp_decode_problem& p);
+
+// ---- process-wide tuning (bsp_tuning.cu) ----
+// Tuning knobs of the dispatch, read once per process from the environment
+// (BSP_SPLITK, BSP_NARROW_SPLITK, BSP_UNION_SPLITK, BSP_NARROW_MIN_N,
+// BSP_PF_KSPLIT, BSP_PF_SC) on first use and changed afterwards only by
+// bsp_set_tuning.  0 means "automatic" for the split counts and the C ring
+// depth; BSP_TUNE_PREFILL_KSPLIT is -1 (automatic), 0 or 1.
+int64_t bsp_tune(bsp_tune_t knob);
+// Spin cap of the kernels' bounded waits, and whether producers skip their
+// first copies (a wait that runs out, for the timeout tests).  Both are
+// fixed (bspx::kSpinCap, no skipping) unless the library was built with
+// BSP_TESTING (libbsp_test.so), where bsp_testing.h can change them.
+uint32_t bsp_spin_cap();
+int bsp_test_stall();
+
+#include <mutex>
+// Per-device one-time setup of a kernel's launch attributes (opt-in
+// shared memory), safe when several host threads make their first call at
+// the same time.  run() returns the setter's error, and tries again on the
+// next call if it failed.
+struct bsp_attr_once {
+    std::mutex mu;
+    bool done[64] = {};
+    template <class F>
+    bool run(int device, F set)
+    {
+        if (device < 0 || device >= 64) return false;
+        std::lock_guard<std::mutex> g(mu);
+        if (!done[device]) done[device] = set() == cudaSuccess;
+        return done[device];
+    }
+};

@@ -92,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
     return false;
 }
 
-// ---- thread-block clusters (CTA pairs)
+// ---- thread-block clusters (the prefill kernel's split-K pairs)
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -127,50 +127,6 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t x, uint32_
 {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
                  : "memory");
-}
-
-// Arrive on the mbarrier at the same shared-memory offset as `bar` in the
-// CTA of cluster rank `rank`.  CLUSTER_SCOPE: release at cluster scope (a
-// fence the arriving thread waits for); else the default release
-#ifndef BSP_REMOTE_ARRIVE_CLUSTER_SCOPE
-#define BSP_REMOTE_ARRIVE_CLUSTER_SCOPE 0
-#endif
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank)
-{
-#if BSP_REMOTE_ARRIVE_CLUSTER_SCOPE
-    asm volatile(
-        "{\n\t.reg .b32 ra;\n\t"
-        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
-        "r"(rank)
-        : "memory");
-#else
-    asm volatile(
-        "{\n\t.reg .b32 ra;\n\t"
-        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
-        "r"(rank)
-        : "memory");
-#endif
-}
-
-// mbar_wait_sleep for a barrier that threads of another CTA of the cluster
-// arrive on: the poll acquires at cluster scope.
-__device__ __forceinline__ bool mbar_wait_sleep_cluster(uint64_t* bar, uint32_t parity, uint32_t cap,
-                                                        uint32_t hint_ns = 1000)
-{
-    for (uint32_t i = 0; i < cap; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-            : "memory");
-        if (ok) return true;
-    }
-    return false;
 }
 
 // Bulk copy global -> shared of `bytes` (multiple of 16, both addresses

@@ -1251,13 +1251,11 @@ int gtw_splits_auto(int64_t strips, int64_t KT, int64_t slots)
     return (int)best;
 }
 
-// BSP_SPLITK overrides the choice (tests and tuning)
+// BSP_TUNE_SPLITK overrides the choice (tests and tuning)
 int gtw_splits(int64_t strips, int64_t KT, int64_t slots)
 {
-    if (const char* e = std::getenv("BSP_SPLITK")) {
-        const int64_t v = std::atol(e);
-        if (v >= 1) return (int)std::min<int64_t>(v, KT);
-    }
+    const int64_t v = bsp_tune(BSP_TUNE_SPLITK);
+    if (v >= 1) return (int)std::min<int64_t>(v, KT);
     return gtw_splits_auto(strips, KT, slots);
 }
 
@@ -1283,17 +1281,16 @@ template <int NT, bool SKIP>
 bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void* Y, float tau, cudaStream_t s)
 {
     using namespace gtw;
-    static bool attr_done[64] = {};
+    static bsp_attr_once attr;
     if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
     uint32_t stage_bytes = 0, val_off = 0;
     stage_geometry(NT, 4096, stage_bytes, val_off);
     const size_t smem_max = smem_bytes(stage_bytes);
-    if (!attr_done[p.device]) {
-        if (cudaFuncSetAttribute(spmm_decode_gtw_kernel<NT, SKIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_max) != cudaSuccess)
-            return BSP_ERR_CUDA;
-        attr_done[p.device] = true;
-    }
+    if (!attr.run(p.device, [&] {
+            return cudaFuncSetAttribute(spmm_decode_gtw_kernel<NT, SKIP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+        }))
+        return BSP_ERR_CUDA;
     stage_geometry(NT, std::min<uint32_t>(p.max_gt_nnz, 4096u), stage_bytes, val_off);
     const size_t smem = smem_bytes(stage_bytes);
     const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
@@ -1316,11 +1313,10 @@ bsp_status_t launch_gtw(const bsp_decode_problem& p, const void* X, int N, void*
     a.counters = p.counters;
     a.err = p.err;
     a.Y = (__half*)Y;
-    a.spin_cap = bspx::kSpinCap;
-    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    a.spin_cap = bsp_spin_cap();
     a.stage_bytes = stage_bytes;
     a.val_off = val_off;
-    a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    a.stall_first = bsp_test_stall();
     a.tau = tau;
     dim3 grid((unsigned)splits, (unsigned)strips);
     spmm_decode_gtw_kernel<NT, SKIP><<<grid, THREADS, smem, s>>>(a);
@@ -1333,14 +1329,13 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
 {
     using C = DecCfg<NT, I8>;
     // the opt-in shared-memory size is set once per device
-    static bool attr_done[64] = {};
+    static bsp_attr_once attr;
     if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
-    if (!attr_done[p.device]) {
-        if (cudaFuncSetAttribute(spmm_decode_kernel<NT, I8, SKIP>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return BSP_ERR_CUDA;
-        attr_done[p.device] = true;
-    }
+    if (!attr.run(p.device, [&] {
+            return cudaFuncSetAttribute(spmm_decode_kernel<NT, I8, SKIP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        }))
+        return BSP_ERR_CUDA;
     const int64_t KT = p.Kp / 64;
     int splits = clamp_det(p, bsp_decode_splits(p, N));
     const int per_split = (int)((KT + splits - 1) / splits);
@@ -1363,9 +1358,8 @@ bsp_status_t launch(const bsp_decode_problem& p, const void* X, int N, void* Y, 
     a.Y = Y;
     a.mode = mode;
     a.row_scale = row_scale;
-    a.spin_cap = bspx::kSpinCap;
-    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
-    a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    a.spin_cap = bsp_spin_cap();
+    a.stall_first = bsp_test_stall();
     a.tau = tau;
     dim3 grid((unsigned)splits, (unsigned)(p.Mp / 64));
     spmm_decode_kernel<NT, I8, SKIP><<<grid, C::THREADS, C::SMEM, s>>>(a);
@@ -1396,9 +1390,9 @@ int team_splits(const bsp_decode_problem& p, bool env)
     // each team run must fit kMaxRun GTs
     const int64_t min_splits = (KT + (int64_t)kMaxRun * kTeams - 1) / ((int64_t)kMaxRun * kTeams);
     int64_t splits;
-    const char* e = env ? std::getenv("BSP_SPLITK") : nullptr;
-    if (e) {
-        splits = std::atol(e);
+    const int64_t forced = env ? bsp_tune(BSP_TUNE_SPLITK) : 0;
+    if (forced >= 1) {
+        splits = forced;
     } else {
         // about 8 GTs per team run, and at least ~2 CTAs per SM
         splits = (KT + 8 * kTeams - 1) / (8 * kTeams);

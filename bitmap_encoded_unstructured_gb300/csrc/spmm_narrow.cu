@@ -595,7 +595,7 @@ int bsp_narrow_splits(const bsp_decode_problem& p)
 {
     const int64_t KT = p.Kp / 64;
     int64_t best = bsp_narrow_splits_auto(p);
-    if (const char* e = std::getenv("BSP_NARROW_SPLITK")) best = std::atol(e);  // tests, tuning
+    if (const int64_t v = bsp_tune(BSP_TUNE_NARROW_SPLITK)) best = v;  // tests, tuning
     if (best > KT) best = KT;
     if (best < 1) best = 1;
     if (p.ws_det && best > p.det_slots) best = p.det_slots;
@@ -621,13 +621,11 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return BSP_ERR_INVALID_ARG;
 
-    static bool attr_done[64] = {};
-    if (!attr_done[p.device]) {
-        if (cudaFuncSetAttribute(spmm_narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) !=
-            cudaSuccess)
-            return BSP_ERR_CUDA;
-        attr_done[p.device] = true;
-    }
+    static bsp_attr_once attr;
+    if (!attr.run(p.device, [] {
+            return cudaFuncSetAttribute(spmm_narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+        }))
+        return BSP_ERR_CUDA;
     NarrowArgs a = {};
     a.bitmaps = p.bitmaps;
     a.offsets = p.offsets;
@@ -646,8 +644,7 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     a.ngt = (p.Mp / 64) * (p.Kp / 64);
     a.values_bytes = p.values_bytes;
     a.err = p.err;
-    a.spin_cap = bspx::kSpinCap;
-    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    a.spin_cap = bsp_spin_cap();
     // C ring: as many stages as fit, each sized for the densest GT
     a.c_slot = c_slot_bytes(std::min<uint32_t>(p.max_gt_nnz, 4096u));
     a.c_stage = c_stage_bytes(a.c_slot);

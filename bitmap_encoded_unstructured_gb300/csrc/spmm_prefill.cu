@@ -86,23 +86,9 @@ constexpr int THREADS = WARPS * 32;
 
 // NSUB 256-column sub-tiles of N per CTA, each with its own TMEM
 // accumulator: every decoded A tile feeds NSUB x 4 MMAs.
-//
-// PAIR: two CTAs of a cluster (consecutive 128-row tiles) share each MMA
-// (tcgen05.mma.cta_group::2, M = 256): each CTA decodes its own 128 rows of
-// A and loads its own 128 of the 256 X rows of a sub-tile; the leader CTA
-// (cluster rank 0) issues the MMAs, and each CTA's TMEM receives its own
-// 128 rows.  A CTA thus holds and the tensor cores read half of the X
-// tile, which frees shared memory for deeper rings.
-// ring depths (X sub-tiles) of the single-CTA kernel with one 256-column
-// sub-tile, and of the pair kernel
+// X sub-tile ring depth with one 256-column sub-tile per CTA
 #ifndef BSP_PF1_SB
 #define BSP_PF1_SB 3
-#endif
-#ifndef BSP_PF2_SB
-#define BSP_PF2_SB 6
-#endif
-#ifndef BSP_PF2_SA
-#define BSP_PF2_SA 3
 #endif
 constexpr int SC_MAX = 12;        // barrier slots of the C ring
 constexpr int SMEM_MAX = 227 * 1024;
@@ -120,21 +106,20 @@ __host__ __device__ constexpr uint32_t c_stage_bytes(uint32_t slot)
     return (2u * slot + 16u + 2u * (uint32_t)RS_BYTES + 127u) & ~127u;
 }
 
-template <int NSUB, bool PAIR>
+template <int NSUB>
 struct PCfg {
     static constexpr int BN_CTA = BN * NSUB;
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // X rows of a sub-tile held by this CTA
     // three rings with their own depths; the C ring takes the rest of the
     // shared memory, in stages sized at launch
-    static constexpr int SB = PAIR ? BSP_PF2_SB : (NSUB == 1 ? BSP_PF1_SB : 4);  // X sub-tiles (TMA) -> MMA
-    static constexpr int SA = PAIR ? BSP_PF2_SA : 2;                             // decoded A tiles   -> MMA
-    static constexpr int B_STAGE = B_ROWS * BK * 2;   // one sub-tile (this CTA's rows) per stage
+    static constexpr int SB = NSUB == 1 ? BSP_PF1_SB : 4;  // X sub-tiles (TMA) -> MMA
+    static constexpr int SA = 2;                             // decoded A tiles   -> MMA
+    static constexpr int B_STAGE = BN * BK * 2;       // one sub-tile per stage
     static constexpr int OFF_B = 0;                   // 1024-B aligned regions first
     static constexpr int OFF_A = OFF_B + SB * B_STAGE;
     static constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
     // barriers: c_full[SC_MAX] c_empty[SC_MAX] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc
-    // c_scan[SC_MAX] b_peer[SB]
-    static constexpr int NBAR = 3 * SC_MAX + 3 * SB + 2 * SA + 1;
+    // c_scan[SC_MAX]
+    static constexpr int NBAR = 3 * SC_MAX + 2 * SB + 2 * SA + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int OFF_C = (OFF_TMEM + 16 + 127) & ~127;
     static constexpr int C_BYTES = SMEM_MAX - 1024 - OFF_C;  // 1024: slack to align the base to 1024 B
@@ -144,9 +129,8 @@ struct PCfg {
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
-// N = 256, M = 128 (one CTA) or 256 (a CTA pair).
+// N = 256, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-constexpr uint32_t kIdesc2 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzled canonical layout: rows of 128 B, 8-row atoms of 1 KB (stride
@@ -225,31 +209,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
                  : "memory");
 }
 
-// CTA pair: issued by the leader; A rows 0-127 / 128-255 and X rows 0-127 /
-// 128-255 of the sub-tile come from the shared memory of ranks 0 / 1 at the
-// same offsets, D rows go to each CTA's own TMEM at the same address.
-__device__ __forceinline__ void umma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc2), "r"(accum)
-        : "memory");
-}
-
-// CTA pair: arrive on the mbarrier at this offset in both CTAs once the
-// MMAs issued so far are done.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar)
-{
-    const uint16_t mask = 0x3;
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bspx::smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -271,12 +230,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 // launches KS only for KT >= 2); each accumulates in its own TMEM, then rank
 // 1 stores its fp32 partial tile into rank 0's rings (idle by then) and
 // rank 0 writes Y = RN(own + partner).
-template <int NSUB, bool PAIR, bool KS>
+template <int NSUB, bool KS>
 __global__ void __launch_bounds__(THREADS, 1)
 spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a)
 {
-    using P = PCfg<NSUB, PAIR>;
-    static_assert(!KS || (!PAIR && NSUB == 1), "split-K: single-CTA MMAs, one 256-column sub-tile");
+    using P = PCfg<NSUB>;
+    static_assert(!KS || NSUB == 1, "split-K: one 256-column sub-tile");
     static_assert(!KS || P::OFF_BAR >= BM * BN * 4, "split-K exchange buffer: the rings, below the barriers");
     constexpr int SA = P::SA, SB = P::SB;
     const int SC = a.sc;
@@ -298,7 +257,6 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     uint64_t* a_empty = a_full + SA;
     uint64_t* acc_bar = a_empty + SA;
     uint64_t* c_scan = acc_bar + 1;
-    uint64_t* b_peer = c_scan + SC_MAX;  // pair leader: the peer's X sub-tile has landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::OFF_TMEM);
     auto b_stage = [&](int s) { return smem + P::OFF_B + s * P::B_STAGE; };
     auto a_stage = [&](int s) { return smem + P::OFF_A + s * A_BYTES; };
@@ -310,34 +268,23 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     const uint32_t KT0 = KS ? (KTA + 1) / 2 : KTA;
     const uint32_t k0 = krank ? KT0 : 0u;                // first GT column of this CTA
     const uint32_t KT = krank ? KTA - KT0 : KT0;         // GT columns of this CTA
-    // linear grid of clusters (one CTA, a pair of consecutive M tiles, or
-    // the two K halves of one tile), N tiles fastest, so that the CTAs
-    // streaming one W row strip run at about the same time and share it in L2
-    const int64_t cl = (int64_t)blockIdx.x / ((PAIR || KS) ? 2 : 1);
-    const int64_t mt = (cl / a.ntiles) * (PAIR ? 2 : 1) + (PAIR ? (int64_t)(blockIdx.x & 1) : 0);
+    // linear grid of clusters (one CTA, or the two K halves of one tile), N
+    // tiles fastest, so that the CTAs streaming one W row strip run at about
+    // the same time and share it in L2
+    const int64_t cl = (int64_t)blockIdx.x / (KS ? 2 : 1);
+    const int64_t mt = cl / a.ntiles;
     const int64_t n0 = (cl % a.ntiles) * P::BN_CTA;
     const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
     const bool has_b = strip1 * 64 < a.Mp;  // second GT row strip of the tile exists
     const uint32_t cap = a.spin_cap;
-    const uint32_t rank = PAIR ? bspx::cluster_ctarank() : 0u;  // pair: 0 = leader (issues the MMAs)
-    const bool leader = rank == 0;
 
     if (warp == 1) {
-        // allocate the accumulators: 128 lanes x 256*NSUB fp32 columns (a
-        // pair: one warp of each CTA, collectively, the same columns in both)
-        if constexpr (PAIR) {
-            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             bspx::smem_u32(tmem_slot)),
-                         "r"(TMEM_COLS)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-        } else {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             bspx::smem_u32(tmem_slot)),
-                         "r"(TMEM_COLS)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
+        // allocate the accumulators: 128 lanes x 256*NSUB fp32 columns
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         bspx::smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < SC; ++s) {
@@ -349,18 +296,15 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             bspx::mbar_init(b_empty + s, 1);
         }
         for (int s = 0; s < SA; ++s) {
-            // pair leader: its own decoders and one relayed arrival for the peer's
-            bspx::mbar_init(a_full + s, (PAIR && leader) ? DEC_WARPS + 1 : DEC_WARPS);
+            bspx::mbar_init(a_full + s, DEC_WARPS);
             bspx::mbar_init(a_empty + s, 1);
         }
         bspx::mbar_init(acc_bar, 1);
         for (int s = 0; s < SC; ++s) bspx::mbar_init(c_scan + s, 2 * 32);  // every scanner lane
-        for (int s = 0; s < SB; ++s) bspx::mbar_init(b_peer + s, 1);
         bspx::fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) bspx::cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     bool failed = false;
@@ -430,74 +374,41 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             if (lane == 0) {
                 const uint32_t kx = i / NSUB, u = i % NSUB;
                 bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)P::B_STAGE);
-                tma_load_2d(b_stage(s), &tmX, (int)((k0 + kx) * BK), (int)(n0 + u * BN + rank * P::B_ROWS),
-                            b_full + s);
+                tma_load_2d(b_stage(s), &tmX, (int)((k0 + kx) * BK), (int)(n0 + u * BN), b_full + s);
             }
             if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
         }
         for (uint32_t k = (i > (uint32_t)SB ? i - SB : 0); k < i; ++k)
             bspx::mbar_wait_bounded(b_full + (k % SB), (k / SB) & 1u, cap);
-    } else if (warp == 1 && !leader) {
-        // ---------------- pair peer: tell the leader, in step order, when this
-        // CTA's decoded A tile is written and when each of its X sub-tiles has
-        // landed (the leader's MMAs read them): one remote arrival each
-        uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
-        for (uint32_t kb = 0; kb < KT && !failed; ++kb) {
-            if (!__all_sync(FULL, bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs))) { failed = true; break; }
-            if (lane == 0) bspx::mbar_arrive_remote(a_full + sa, 0);
-            __syncwarp();
-            if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
-            for (int u = 0; u < NSUB; ++u) {
-                if (!__all_sync(FULL, bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs))) { failed = true; break; }
-                if (lane == 0) bspx::mbar_arrive_remote(b_peer + sb, 0);
-                __syncwarp();
-                if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
-            }
-        }
     } else if (warp == 1) {
         // ---------------- MMA issuer
         uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
         for (uint32_t kb = 0; kb < KT && !failed; ++kb) {
-            const bool oka = PAIR ? bspx::mbar_wait_sleep_cluster(a_full + sa, pa, cap, kSleepNs)
-                                  : bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs);
+            const bool oka = bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs);
             if (!__all_sync(FULL, oka)) { failed = true; break; }
             const uint64_t ad = smem_desc_sw128(bspx::smem_u32(a_stage(sa)));
 #pragma unroll
             for (int u = 0; u < NSUB; ++u) {
-                bool okb = bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
-                if (PAIR) okb = okb && bspx::mbar_wait_sleep_cluster(b_peer + sb, pb, cap, kSleepNs);
+                const bool okb = bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
                 if (!__all_sync(FULL, okb)) { failed = true; break; }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint64_t bd = smem_desc_sw128(bspx::smem_u32(b_stage(sb)));
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j) {  // K = 16 per MMA: 32 B along the swizzled row
-                        if constexpr (PAIR)
-                            umma_f16_pair(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j),
-                                          bd + (uint64_t)(2 * j), (kb | j) ? 1u : 0u);
-                        else
-                            umma_f16(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
-                                     (kb | j) ? 1u : 0u);
-                    }
-                    // fires (in both CTAs of a pair) once the MMAs above are done
-                    if constexpr (PAIR) umma_commit_pair(b_empty + sb);
-                    else umma_commit(b_empty + sb);
+                    for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
+                        umma_f16(tmem_base + (uint32_t)(u * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
+                                 (kb | j) ? 1u : 0u);
+                    umma_commit(b_empty + sb);  // fires once the MMAs above are done
                 }
                 __syncwarp();
                 if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
             }
             if (failed) break;
-            if (lane == 0) {
-                if constexpr (PAIR) umma_commit_pair(a_empty + sa);
-                else umma_commit(a_empty + sa);
-            }
+            if (lane == 0) umma_commit(a_empty + sa);
             __syncwarp();
             if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
         }
-        if (lane == 0) {  // fires once every MMA issued above is done
-            if constexpr (PAIR) umma_commit_pair(acc_bar);
-            else umma_commit(acc_bar);
-        }
+        if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
         __syncwarp();
         bspx::mbar_wait_bounded(acc_bar, 0, cap);
     } else if (warp < DEC0) {
@@ -605,7 +516,7 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
             bspx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                bspx::mbar_arrive(a_full + sa);  // a pair's peer: relayed to the leader by warp 1
+                bspx::mbar_arrive(a_full + sa);
                 bspx::mbar_arrive(c_empty + sc);
             }
             if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
@@ -699,17 +610,10 @@ spmm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const PrefillArgs a
     if (failed && lane == 0) atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    // a pair: neither CTA frees the columns (collectively) or exits while the
-    // other may still read its TMEM or signal its barriers
-    if constexpr (PAIR) bspx::cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        if constexpr (PAIR)
-            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                         : "memory");
-        else
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                         : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
     }
 }
 
@@ -732,23 +636,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 
 namespace {
 
-template <int NSUB, bool PAIR, bool KS>
+template <int NSUB, bool KS>
 bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64_t M, int64_t N,
                             uint32_t max_gt_nnz, int device, cudaStream_t s)
 {
-    using P = PCfg<NSUB, PAIR>;
-    static bool attr_done[64] = {};
-    if (!attr_done[device]) {
-        const cudaError_t e = cudaFuncSetAttribute(spmm_prefill_kernel<NSUB, PAIR, KS>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
-        if (e != cudaSuccess) {
-            if (std::getenv("BSP_DEBUG"))
-                std::fprintf(stderr, "spmm_prefill_kernel<%d, %d, %d> attribute: %s\n", NSUB, (int)PAIR, (int)KS,
-                             cudaGetErrorString(e));
-            return BSP_ERR_CUDA;
-        }
-        attr_done[device] = true;
-    }
+    using P = PCfg<NSUB>;
+    static bsp_attr_once attr_once;
+    if (!attr_once.run(device, [] {
+            return cudaFuncSetAttribute(spmm_prefill_kernel<NSUB, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_MAX);
+        }))
+        return BSP_ERR_CUDA;
     if (KS && a0.KT < 2) return BSP_ERR_INTERNAL;  // rank 1 would have no GT column
     const int64_t bn_cta = (int64_t)BN * NSUB;
     const int64_t ntiles = (N + bn_cta - 1) / bn_cta;
@@ -760,7 +658,7 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
     a.c_slot = c_slot_bytes(std::min<uint32_t>(max_gt_nnz, 4096u));
     a.c_stage = c_stage_bytes(a.c_slot);
     a.sc = std::min<int>(SC_MAX, P::C_BYTES / (int)a.c_stage);
-    if (const char* e = std::getenv("BSP_PF_SC")) a.sc = std::max(2, std::min(a.sc, std::atoi(e)));  // tuning
+    if (const int64_t v = bsp_tune(BSP_TUNE_PREFILL_CSTAGES)) a.sc = std::max(2, std::min<int>(a.sc, (int)v));
     const int smem = P::OFF_C + a.sc * (int)a.c_stage + 1024;
     dim3 grid((unsigned)ctas, 1);
     cudaLaunchConfig_t cfg = {};
@@ -769,7 +667,7 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    if (PAIR || KS) {  // two consecutive CTAs form a cluster: two 128-row tiles, or two K halves
+    if (KS) {  // two consecutive CTAs form a cluster: the two K halves of a tile
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -777,18 +675,7 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, spmm_prefill_kernel<NSUB, PAIR, KS>, map, a);
-    if (e != cudaSuccess) {
-        if (std::getenv("BSP_DEBUG")) {
-            int nc = -1;
-            const cudaError_t oe = cudaOccupancyMaxActiveClusters(&nc, spmm_prefill_kernel<NSUB, PAIR, KS>, &cfg);
-            std::fprintf(stderr, "spmm_prefill_kernel<%d, %d, %d> launch grid (%u, %u) smem %d: %s; max active clusters %d (%s)\n",
-                         NSUB, (int)PAIR, (int)KS, grid.x, grid.y, smem, cudaGetErrorString(e), nc,
-                         cudaGetErrorString(oe));
-        }
-        return BSP_ERR_CUDA;
-    }
-    return BSP_OK;
+    return cudaLaunchKernelEx(&cfg, spmm_prefill_kernel<NSUB, KS>, map, a) == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
 }  // namespace
@@ -796,11 +683,11 @@ bsp_status_t launch_prefill(const CUtensorMap& map, const PrefillArgs& a0, int64
 // Split K over two CTAs (N <= 256: one tile column) when that shortens the
 // critical path: CTA waves times GT columns per CTA, plus a fixed cost per
 // CTA (start, epilogue; about 4 GT columns) and the exchange (about 2).
-// BSP_PF_KSPLIT=0/1 forces the choice (tests), for KT >= 2.
+// BSP_TUNE_PREFILL_KSPLIT = 0 / 1 forces the choice (tests), for KT >= 2.
 static bool prefill_split_k(int64_t tiles, int64_t KT, int num_sms)
 {
     if (KT < 2) return false;
-    if (const char* e = std::getenv("BSP_PF_KSPLIT")) return e[0] == '1';
+    if (const int64_t v = bsp_tune(BSP_TUNE_PREFILL_KSPLIT); v >= 0) return v == 1;
     const int64_t slots = num_sms > 0 ? num_sms : 1;  // one CTA per SM (shared memory)
     const int64_t one = ((tiles + slots - 1) / slots) * (KT + 4);
     const int64_t two = ((2 * tiles + slots - 1) / slots) * ((KT + 1) / 2 + 6);
@@ -814,19 +701,12 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     auto encode = get_encode_fn();
     if (!encode) return BSP_ERR_CUDA;
     if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
-    // CTA pairs (opt-in, BSP_PF_PAIR=1) when the 128-row tiles pair up (M a
-    // multiple of 256).  Measured on the Llama-2-70B FFN shapes the pair is
-    // slower than single CTAs (1317 against 1452 TFLOP/s at N = 4096): the
-    // cross-CTA handshakes and the co-scheduling of cluster pairs cost more
-    // than the halved X-tile traffic saves.
-    const char* pe = std::getenv("BSP_PF_PAIR");
-    const bool pair = pe && pe[0] == '1' && (p.Mp % 256) == 0;
-    // X: [N][K] fp16, K contiguous; box = 64 (K) x 256 (N) rows, or 128 for a
-    // CTA of a pair, with the 128-B swizzle
+    // X: [N][K] fp16, K contiguous; box = 64 (K) x 256 (N) rows, with the
+    // 128-B swizzle
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)(pair ? BN / 2 : BN)};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -843,14 +723,10 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
     a.Mp = p.Mp;
     a.KT = p.Kp / 64;
     a.err = p.err;
-    a.spin_cap = bspx::kSpinCap;
-    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
+    a.spin_cap = bsp_spin_cap();
     // one 256-column sub-tile per CTA for N <= 256, two (512 columns) above
-    if (N > BN)
-        return pair ? launch_prefill<2, true, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s)
-                    : launch_prefill<2, false, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
-    if (pair) return launch_prefill<1, true, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+    if (N > BN) return launch_prefill<2, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
     if (prefill_split_k(p.Mp / BM + (p.Mp % BM ? 1 : 0), a.KT, p.num_sms))
-        return launch_prefill<1, false, true>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
-    return launch_prefill<1, false, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+        return launch_prefill<1, true>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
+    return launch_prefill<1, false>(map, a, p.Mp, N, p.max_gt_nnz, p.device, s);
 }

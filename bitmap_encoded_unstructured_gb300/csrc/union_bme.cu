@@ -472,21 +472,21 @@ template <int BITS, int NT, bool PERM>
 bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y, cudaStream_t s)
 {
     using C = UCfg<BITS, NT, PERM>;
-    static bool attr_done[64] = {};
+    static bsp_attr_once attr;
     if (h->device < 0 || h->device >= 64) return BSP_ERR_INVALID_ARG;
-    if (!attr_done[h->device]) {
-        if (cudaFuncSetAttribute(union_spmm_kernel<BITS, NT, PERM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM) != cudaSuccess)
-            return BSP_ERR_CUDA;
-        attr_done[h->device] = true;
-    }
+    if (!attr.run(h->device, [] {
+            return cudaFuncSetAttribute(union_spmm_kernel<BITS, NT, PERM>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        }))
+        return BSP_ERR_CUDA;
     const int64_t strips = h->Mp / LT, KT = h->Kp / LT;
     // about four CTAs per SM, and at least two LTs per warp
     int64_t splits = (4 * (int64_t)h->num_sms + strips - 1) / strips;
     const int64_t max_splits = (KT + 2 * C::WARPS - 1) / (2 * C::WARPS);
-    if (const char* e = std::getenv("BSP_UNION_SPLITK")) splits = std::atol(e);
+    const int64_t forced = bsp_tune(BSP_TUNE_UNION_SPLITK);
+    if (forced >= 1) splits = forced;
     splits = splits < 1 ? 1 : splits;
-    if (splits > max_splits && !std::getenv("BSP_UNION_SPLITK")) splits = max_splits;
+    if (splits > max_splits && forced < 1) splits = max_splits;
     if (splits > KT) splits = KT;
     if (splits < 1) splits = 1;
     const int per_split = (int)((KT + splits - 1) / splits);
@@ -507,9 +507,8 @@ bsp_status_t launch_union(const bsp_union* h, const int8_t* X, int N, int32_t* Y
     a.counters = h->counters;
     a.err = h->err;
     a.Y = Y;
-    a.spin_cap = bspx::kSpinCap;
-    if (const char* e = std::getenv("BSP_SPIN_CAP")) a.spin_cap = (uint32_t)std::strtoul(e, nullptr, 10);
-    a.stall_first = std::getenv("BSP_TEST_STALL") != nullptr;
+    a.spin_cap = bsp_spin_cap();
+    a.stall_first = bsp_test_stall();
     union_spmm_kernel<BITS, NT, PERM><<<dim3((unsigned)splits, (unsigned)strips), C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }

@@ -112,10 +112,12 @@ int64_t pair_cost(const PairCosts& C, const std::vector<std::pair<int, int>>& P)
 
 // pair swaps ((a, b), (c, d) -> (a, c), (b, d) or (a, d), (b, c)) that
 // involve a pair of the worklist, until none lowers the cost; a pair that
-// changes joins the worklist.  Started with every pair listed, it ends in a
+// changes joins the worklist, and a pair x whose scan made a swap scans
+// every other pair again (its new partner may now improve with a pair
+// checked before the swap).  Started with every pair listed, it ends in a
 // grouping where no swap helps; started from such a grouping with only the
-// pairs changed since listed, it ends in one again, at O(worklist x pairs)
-// cost.  Every swap lowers an integer cost, so it ends.
+// pairs changed since listed, it ends in one again.  Every swap lowers an
+// integer cost, so it ends.
 void improve_from(const PairCosts& C, std::vector<std::pair<int, int>>& P, std::vector<int>& work)
 {
     const int np = (int)P.size();
@@ -142,6 +144,7 @@ void improve_from(const PairCosts& C, std::vector<std::pair<int, int>>& P, std::
                 queued[y] = 1;
                 work.push_back(y);
             }
+            y = -1;  // P[x] changed: rescan from the first pair
         }
     }
 }

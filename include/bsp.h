@@ -151,6 +151,42 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void *X, int64_t N, void *Y,
 bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
 
 /*
+ * Process-wide tuning of the dispatch (the pages fix none of these; they
+ * are launch choices of this library).  Each knob starts from the
+ * environment variable named beside it, read once, at the first product
+ * call or bsp_get_tuning / bsp_set_tuning of the process; afterwards only
+ * bsp_set_tuning changes it.  A change applies to calls made after it
+ * returns; it is not synchronised with calls other threads make meanwhile.
+ *   BSP_TUNE_SPLITK          (BSP_SPLITK)        split-K count of the
+ *                            CUDA-core decode kernels; 0 = automatic
+ *   BSP_TUNE_NARROW_SPLITK   (BSP_NARROW_SPLITK) split-K count of the
+ *                            tcgen05 decode kernel; 0 = automatic
+ *   BSP_TUNE_UNION_SPLITK    (BSP_UNION_SPLITK)  split-K count of the IE-BME
+ *                            product; 0 = automatic
+ *   BSP_TUNE_NARROW_MIN_N    (BSP_NARROW_MIN_N)  smallest fp16 N <= 16 that
+ *                            runs the tcgen05 decode kernel; larger than 16:
+ *                            never; default 5
+ *   BSP_TUNE_PREFILL_KSPLIT  (BSP_PF_KSPLIT)     prefill split-K over a CTA
+ *                            pair: -1 automatic, 0 off, 1 on (N <= 256)
+ *   BSP_TUNE_PREFILL_CSTAGES (BSP_PF_SC)         compressed-ring depth of the
+ *                            prefill kernel; 0 = as many as fit
+ * Split counts are clamped to the problem (at most one per GroupTile
+ * column).  BSP_ERR_INVALID_ARG for an unknown knob or a value out of range
+ * (split counts and stages 0..4096, NARROW_MIN_N 1..1024, KSPLIT -1..1).
+ */
+typedef enum {
+    BSP_TUNE_SPLITK = 0,
+    BSP_TUNE_NARROW_SPLITK = 1,
+    BSP_TUNE_UNION_SPLITK = 2,
+    BSP_TUNE_NARROW_MIN_N = 3,
+    BSP_TUNE_PREFILL_KSPLIT = 4,
+    BSP_TUNE_PREFILL_CSTAGES = 5
+} bsp_tune_t;
+
+bsp_status_t bsp_set_tuning(bsp_tune_t knob, int64_t value);
+bsp_status_t bsp_get_tuning(bsp_tune_t knob, int64_t *value);
+
+/*
  * INT8 with per-row dequantisation: Y[n][m] = fp32(acc[n][m]) * row_scale[m],
  * one round-to-nearest int->float conversion and one fp32 multiply.
  *   X device int8 [N][K]; row_scale device fp32 [M]; Y device fp32 [N][M].

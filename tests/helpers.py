@@ -35,3 +35,24 @@ def sample_rows(M: int, per_strip: int, seed: int) -> np.ndarray:
     g = np.random.Generator(np.random.PCG64(seed))
     rows = [s * 64 + np.sort(g.choice(64, size=per_strip, replace=False)) for s in range(M // 64)]
     return np.concatenate(rows)
+
+
+_TUNE_DEFAULTS = {}
+
+
+def tune(knob: str, value=None):
+    """Set a process-wide tuning knob of the library (bsp_set_tuning; names
+    as in ``bitmap_encoded_unstructured_gb300.TUNE``); value None restores
+    the value it had when the first test touched the knobs."""
+    import bitmap_encoded_unstructured_gb300 as bsp
+    if not _TUNE_DEFAULTS:
+        _TUNE_DEFAULTS.update({k: bsp.get_tuning(k) for k in bsp.TUNE})
+    bsp.set_tuning(knob, _TUNE_DEFAULTS[knob] if value is None else int(value))
+
+
+def restore_tuning():
+    """Every knob back to its starting value (after a test that changed some)."""
+    if _TUNE_DEFAULTS:
+        import bitmap_encoded_unstructured_gb300 as bsp
+        for k, v in _TUNE_DEFAULTS.items():
+            bsp.set_tuning(k, v)

@@ -53,6 +53,6 @@ def test_step_kernel_default_is_the_librarys():
     """bench.step_kernel labels the step's launches with the library's
     default fp16 dispatch threshold, read here from its source."""
     import re
-    src = open(os.path.join(ROOT, "bitmap_encoded_unstructured_gb300", "csrc", "bsp_api.cu")).read()
+    src = open(os.path.join(ROOT, "bitmap_encoded_unstructured_gb300", "csrc", "bsp_tuning.cu")).read()
     m = re.search(r"#define\s+BSP_NARROW_MIN_N_DEFAULT\s+(\d+)", src)
     assert m and int(m.group(1)) == bench.NARROW_MIN_N_DEFAULT

@@ -8,7 +8,7 @@ import torch
 import bitmap_encoded_unstructured_gb300 as bsp
 import oracle
 from bitmap_encoded_unstructured_gb300 import synth
-from helpers import assert_within_bound, to_dev_f16
+from helpers import assert_within_bound, to_dev_f16, tune
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -25,14 +25,14 @@ def _need_gpu():
 def splitk(monkeypatch):
     def set_(s):
         if s is None:
-            monkeypatch.delenv("BSP_SPLITK", raising=False)
-            monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+            tune("splitk")
+            tune("narrow_splitk")
         else:
-            monkeypatch.setenv("BSP_SPLITK", str(s))
-            monkeypatch.setenv("BSP_NARROW_SPLITK", str(s))
+            tune("splitk", str(s))
+            tune("narrow_splitk", str(s))
     yield set_
-    monkeypatch.delenv("BSP_SPLITK", raising=False)
-    monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+    tune("splitk")
+    tune("narrow_splitk")
 
 
 def _repeat(fn):

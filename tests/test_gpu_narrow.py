@@ -9,7 +9,7 @@ import torch
 import bitmap_encoded_unstructured_gb300 as bsp
 import oracle
 from bitmap_encoded_unstructured_gb300 import synth
-from helpers import assert_within_bound, to_dev_f16
+from helpers import assert_within_bound, to_dev_f16, tune
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -19,10 +19,10 @@ DEV = torch.device("cuda:0")
 def _narrow(monkeypatch):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    monkeypatch.setenv("BSP_NARROW_MIN_N", "1")
+    tune("narrow_min_n", "1")
     yield
-    monkeypatch.delenv("BSP_NARROW_MIN_N", raising=False)
-    monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+    tune("narrow_min_n")
+    tune("narrow_splitk")
 
 
 def _run(W, X):
@@ -52,7 +52,7 @@ def test_narrow_forced_splits(splits, monkeypatch):
     W = synth.weights_f16(M, K, 0.6, "uniform", 510)
     X = synth.activations_f16(N, K, 511)
     Yref, S = oracle.spmm_f16(W, X)
-    monkeypatch.setenv("BSP_NARROW_SPLITK", str(splits))
+    tune("narrow_splitk", str(splits))
     A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
     Xd = to_dev_f16(X, DEV)
     for _ in range(3):  # the workspace and counters are clean after each call
@@ -61,7 +61,7 @@ def test_narrow_forced_splits(splits, monkeypatch):
 
 
 def test_narrow_small_integers_exact(monkeypatch):
-    monkeypatch.setenv("BSP_NARROW_SPLITK", "3")
+    tune("narrow_splitk", "3")
     W = synth.small_int_f16((256, 256), -8, 8, seed=521, sparsity=0.5)
     X = synth.small_int_f16((9, 256), -8, 8, seed=522)
     Yref, _ = oracle.spmm_f16(W, X)
@@ -75,7 +75,7 @@ def test_narrow_then_cores_share_workspace(monkeypatch):
     W = synth.weights_f16(M, K, 0.5, "uniform", 531)
     A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
     for i, N in enumerate((8, 16, 3, 16, 1, 8)):
-        monkeypatch.setenv("BSP_NARROW_MIN_N", "1" if i % 2 == 0 else "17")
+        tune("narrow_min_n", "1" if i % 2 == 0 else "17")
         X = synth.activations_f16(N, K, 540 + i)
         Yref, S = oracle.spmm_f16(W, X)
         assert_within_bound(A.spmm(to_dev_f16(X, DEV)).cpu().numpy(), Yref, S, f"call {i} N={N}")

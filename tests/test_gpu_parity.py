@@ -14,7 +14,7 @@ import oracle
 import bitmap_encoded_unstructured_gb300 as bsp
 from bitmap_encoded_unstructured_gb300 import synth
 
-from helpers import assert_within_bound, sample_rows, to_dev, to_dev_f16
+from helpers import assert_within_bound, sample_rows, to_dev, to_dev_f16, tune
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -33,23 +33,23 @@ def splitk(monkeypatch):
     """Force the split-K factor of the decode and narrow kernels for one test."""
     def set_(v):
         if v is None:
-            monkeypatch.delenv("BSP_SPLITK", raising=False)
-            monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+            tune("splitk")
+            tune("narrow_splitk")
         else:
-            monkeypatch.setenv("BSP_SPLITK", str(v))
-            monkeypatch.setenv("BSP_NARROW_SPLITK", str(v))
+            tune("splitk", str(v))
+            tune("narrow_splitk", str(v))
     yield set_
-    monkeypatch.delenv("BSP_SPLITK", raising=False)
-    monkeypatch.delenv("BSP_NARROW_SPLITK", raising=False)
+    tune("splitk")
+    tune("narrow_splitk")
 
 
 @pytest.fixture(params=["cuda_cores", "tcgen05_narrow"])
 def path(request, monkeypatch):
     """fp16 N <= 16 on the CUDA-core decode kernels, or on the tcgen05
     narrow kernel (every N forced onto it)."""
-    monkeypatch.setenv("BSP_NARROW_MIN_N", "17" if request.param == "cuda_cores" else "1")
+    tune("narrow_min_n", "17" if request.param == "cuda_cores" else "1")
     yield request.param
-    monkeypatch.delenv("BSP_NARROW_MIN_N", raising=False)
+    tune("narrow_min_n")
 
 
 def _encode(W):
@@ -367,30 +367,34 @@ def test_check_ok_after_normal_calls():
 
 
 @pytest.mark.parametrize("spmspv", [False, True])
-def test_wait_that_runs_out_reports_timeout(spmspv, monkeypatch):
-    """Each warp's producer skips its first GT's copies (a barrier nothing
-    completes); the consumers' bounded wait gives up, the kernel records
-    BSP_ERR_TIMEOUT and returns; the context stays usable."""
+def test_wait_that_runs_out_reports_timeout(spmspv):
+    """In the test build of the library (libbsp_test.so) each warp's producer
+    skips its first GT's copies (a barrier nothing completes); the
+    consumers' bounded wait gives up, the kernel records BSP_ERR_TIMEOUT and
+    returns; the context stays usable and the next call is correct."""
     W = synth.weights_f16(256, 1024, 0.5, "uniform", 93)
     X = synth.activations_f16(1, 1024, 94)
-    A = _encode(W)
-    Xd = to_dev_f16(X, DEV)
-    monkeypatch.setenv("BSP_TEST_STALL", "1")
-    monkeypatch.setenv("BSP_SPIN_CAP", "2000")
-    if spmspv:
-        A.spmspv(Xd[0].contiguous())
-    else:
-        A.spmm(Xd)
-    with pytest.raises(bsp.BspError) as e:
+    with bsp.test_library() as T:
+        A = _encode(W)
+        Xd = to_dev_f16(X, DEV)
+        try:
+            assert T.bsp_testing_set_stall(1) == 0 and T.bsp_testing_set_spin_cap(2000) == 0
+            if spmspv:
+                A.spmspv(Xd[0].contiguous())
+            else:
+                A.spmm(Xd)
+            with pytest.raises(bsp.BspError) as e:
+                A.check()
+            assert e.value.status == 7
+        finally:
+            T.bsp_testing_set_stall(0)
+            T.bsp_testing_set_spin_cap(0)
+        A.check()  # cleared
+        Y = A.spmm(Xd).cpu().numpy()
+        Yref, S = oracle.spmm_f16(W, X)
+        assert_within_bound(Y, Yref, S, "after timeout")
         A.check()
-    assert e.value.status == 7
-    monkeypatch.delenv("BSP_TEST_STALL")
-    monkeypatch.delenv("BSP_SPIN_CAP")
-    A.check()  # cleared
-    Y = A.spmm(Xd).cpu().numpy()
-    Yref, S = oracle.spmm_f16(W, X)
-    assert_within_bound(Y, Yref, S, "after timeout")
-    A.check()
+        A.close()
 
 
 def test_spmspv_mixed_selective_and_whole_fetch():

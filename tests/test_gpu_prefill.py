@@ -6,7 +6,7 @@ import oracle
 import bitmap_encoded_unstructured_gb300 as bsp
 from bitmap_encoded_unstructured_gb300 import synth
 
-from helpers import assert_within_bound, sample_rows, to_dev_f16
+from helpers import assert_within_bound, sample_rows, to_dev_f16, tune
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -44,20 +44,6 @@ def test_prefill_small_shapes(M, K, N):
     assert_within_bound(Y, Yref, S, f"prefill {M}x{K} N={N}")
 
 
-@pytest.mark.parametrize("M,K,N", [(256, 1024, 513), (512, 448, 300), (768, 640, 256), (1024, 128, 40)])
-def test_prefill_cta_pairs(M, K, N, monkeypatch):
-    """The opt-in CTA-pair kernel (tcgen05.mma.cta_group::2: two 128-row
-    tiles share each MMA, each CTA holding half of the X sub-tile) matches
-    the oracle, then the default path again."""
-    W = synth.weights_f16(M, K, 0.5, "uniform", 350 + M + K + N)
-    X = synth.activations_f16(N, K, 351 + N)
-    Yref, S = oracle.spmm_f16(W, X)
-    monkeypatch.setenv("BSP_PF_PAIR", "1")
-    assert_within_bound(_run(W, X), Yref, S, f"pair prefill {M}x{K} N={N}")
-    monkeypatch.delenv("BSP_PF_PAIR")
-    assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
-
-
 @pytest.mark.parametrize("M,K,N", [(128, 128, 32),     # KT = 2: one GT column per CTA of the cluster
                                    (192, 320, 17),     # KT = 5: 3 + 2; half tile
                                    (130, 136, 256),    # ragged M and K (KT = 3 over the padded grid)
@@ -69,9 +55,9 @@ def test_prefill_split_k(M, K, N, monkeypatch):
     W = synth.weights_f16(M, K, 0.5, "uniform", 370 + M + K + N)
     X = synth.activations_f16(N, K, 371 + N)
     Yref, S = oracle.spmm_f16(W, X)
-    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    tune("prefill_ksplit", "1")
     assert_within_bound(_run(W, X), Yref, S, f"split-K prefill {M}x{K} N={N}")
-    monkeypatch.setenv("BSP_PF_KSPLIT", "0")
+    tune("prefill_ksplit", "0")
     assert_within_bound(_run(W, X), Yref, S, f"prefill {M}x{K} N={N}")
 
 
@@ -79,7 +65,7 @@ def test_prefill_split_k(M, K, N, monkeypatch):
 def test_prefill_split_k_repeated(M, K, N, monkeypatch):
     """Twenty calls in a row (the cluster barriers of the exchange run
     every time): every result within the bound and all bitwise equal."""
-    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    tune("prefill_ksplit", "1")
     W = synth.weights_f16(M, K, 0.5, "uniform", 390 + M)
     X = synth.activations_f16(N, K, 391)
     Yref, S = oracle.spmm_f16(W, X)
@@ -94,7 +80,7 @@ def test_prefill_split_k_repeated(M, K, N, monkeypatch):
 
 def test_prefill_split_k_small_integers_exact(monkeypatch):
     """Both partial sums and their sum are small integers: exact."""
-    monkeypatch.setenv("BSP_PF_KSPLIT", "1")
+    tune("prefill_ksplit", "1")
     W = synth.small_int_f16((256, 256), -8, 8, seed=381, sparsity=0.5)
     X = synth.small_int_f16((40, 256), -8, 8, seed=382)
     Yref, _ = oracle.spmm_f16(W, X)

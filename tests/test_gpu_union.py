@@ -7,7 +7,7 @@ import torch
 
 import bitmap_encoded_unstructured_gb300 as bsp
 from oracle import ie_bme as u
-from helpers import sample_rows
+from helpers import sample_rows, tune
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -72,7 +72,7 @@ def test_spmm_split_k_forced(splits, monkeypatch):
     W = _weights(320, 1024, 4, 0.6, 41)
     X = _acts(8, 1024, 4, 42)
     ref = u.union_spmm(W, X)
-    monkeypatch.setenv("BSP_UNION_SPLITK", str(splits))
+    tune("union_splitk", str(splits))
     A = bsp.UnionMatrix(_dev(W), 4)
     Xd = _dev(X)
     for _ in range(3):
@@ -206,29 +206,33 @@ def test_reordered_split_k_forced(monkeypatch):
     ref = u.union_spmm(W, X)
     A = bsp.UnionMatrix(_dev(W), 8, reorder=True)
     for sp in (1, 5, 16):
-        monkeypatch.setenv("BSP_UNION_SPLITK", str(sp))
+        tune("union_splitk", str(sp))
         np.testing.assert_array_equal(A.spmm(_dev(X)).cpu().numpy().astype(np.int64), ref)
     A.check()
 
 
-def test_wait_that_runs_out_reports_timeout(monkeypatch):
-    """Each warp's producer skips its first tile's copies (a barrier nothing
-    completes); the bounded wait gives up, the kernel records
-    BSP_ERR_TIMEOUT, drains its other copies and returns; the next call is
-    exact (workspace and counters were left clean)."""
+def test_wait_that_runs_out_reports_timeout():
+    """In the test build of the library (libbsp_test.so) each warp's producer
+    skips its first tile's copies (a barrier nothing completes); the bounded
+    wait gives up, the kernel records BSP_ERR_TIMEOUT, drains its other
+    copies and returns; the next call is exact (workspace and counters were
+    left clean)."""
     W = _weights(256, 1024, 8, 0.5, 91)
     X = _acts(4, 1024, 8, 92)
-    A = bsp.UnionMatrix(_dev(W), 8)
-    Xd = _dev(X)
-    monkeypatch.setenv("BSP_TEST_STALL", "1")
-    monkeypatch.setenv("BSP_SPIN_CAP", "2000")
-    monkeypatch.setenv("BSP_UNION_SPLITK", "4")
-    A.spmm(Xd)
-    with pytest.raises(bsp.BspError) as e:
+    with bsp.test_library() as T:
+        A = bsp.UnionMatrix(_dev(W), 8)
+        Xd = _dev(X)
+        tune("union_splitk", 4)
+        try:
+            assert T.bsp_testing_set_stall(1) == 0 and T.bsp_testing_set_spin_cap(2000) == 0
+            A.spmm(Xd)
+            with pytest.raises(bsp.BspError) as e:
+                A.check()
+            assert e.value.status == 7
+        finally:
+            T.bsp_testing_set_stall(0)
+            T.bsp_testing_set_spin_cap(0)
+        A.check()  # cleared
+        np.testing.assert_array_equal(A.spmm(Xd).cpu().numpy().astype(np.int64), u.union_spmm(W, X))
         A.check()
-    assert e.value.status == 7
-    monkeypatch.delenv("BSP_TEST_STALL")
-    monkeypatch.delenv("BSP_SPIN_CAP")
-    A.check()  # cleared
-    np.testing.assert_array_equal(A.spmm(Xd).cpu().numpy().astype(np.int64), u.union_spmm(W, X))
-    A.check()
+        A.close()

@@ -114,3 +114,23 @@ def test_pairing_heuristic_near_the_matching_optimum(p):
         tot_h += cost
         tot_o += opt
     assert tot_h <= 1.015 * tot_o
+
+
+@pytest.mark.parametrize("p", [0.5, 0.3, 0.1])
+def test_pairing_heuristic_ends_at_a_pair_swap_local_optimum(p):
+    """No exchange of partners between two pairs of the returned grouping
+    lowers its cost: the descent really ends at a local optimum of pair
+    swaps (costs recomputed here from the folded row patterns)."""
+    for seed in range(4):
+        T = _tile(64, 64, p, 2000 + seed + int(100 * p))
+        perm, _ = bsp.bsp_reorder_rows(T, 2, 2, exact=False)
+        nz = T != 0
+        f = nz[:, 32:] | nz[:, :32]
+        c = lambda a, b: int((f[a] | f[b]).sum())
+        pairs = [(int(perm[i]), int(perm[32 + i])) for i in range(32)]
+        for i in range(32):
+            a, b = pairs[i]
+            for j in range(i + 1, 32):
+                d, e = pairs[j]
+                now = c(a, b) + c(d, e)
+                assert c(a, d) + c(b, e) >= now and c(a, e) + c(b, d) >= now, (seed, i, j)
