@@ -41,6 +41,11 @@ NS = (1, 2, 8, 16)
 PREFILL_LAYERS = [("llama_up", 28672, 8192), ("llama_down", 8192, 28672)]
 PREFILL_NS = (256, 1024, 4096)
 METRIC = "bitmap-SpMM decode GB/s (% of HBM peak) at N=1-16; prefill TFLOP/s"
+# INT8 bitmap SpMM: W 11008x4096 and 4096x11008, nonzeros uniform in
+# [-127, 127] \ {0}, 50% and 60% uniform masks, int8 X, N = 1, 8, 16
+INT8_LAYERS = [("int8_11008x4096", 11008, 4096), ("int8_4096x11008", 4096, 11008)]
+INT8_SPARSITY = (0.5, 0.6)
+INT8_NS = (1, 8, 16)
 # kernels of the decode step and their sources (with the dispatch): fp16
 # N <= 2 and spMspV on the GT-per-warp kernel, N = 3, 4 on the team kernel,
 # N >= 5 on the narrow tcgen05 kernel
@@ -85,6 +90,32 @@ def _tensor_peak():
 def prefill_weights(name, M, K):
     i = [l[0] for l in PREFILL_LAYERS].index(name)
     return synth.weights_f16(M, K, 0.5, "uniform", synth.seed_for(4, i))
+
+
+def prefill_acts(N, K):
+    return synth.activations_f16(N, K, synth.seed_for(4, 2))
+
+
+def int8_inputs(li, s):
+    """Seeded inputs of one INT8 configuration: layer index li of
+    INT8_LAYERS, sparsity s: (W int8 [M][K], X int8 [16][K], row scales
+    fp32 [M])."""
+    _, M, K = INT8_LAYERS[li]
+    W = synth.weights_i8(M, K, s, synth.seed_for(5, 2 * li + INT8_SPARSITY.index(s)))
+    X = synth.activations_i8(max(INT8_NS), K, synth.seed_for(5, 4 + li))
+    return W, X, synth.row_scales(M, synth.seed_for(5, 6 + li))
+
+
+def sweep_weights(s):
+    """Seeded weight of one sparsity-sweep point: fp16 bits [8192][8192] at
+    sparsity s (uniform exact-count mask)."""
+    M, K = SWEEP_SHAPE
+    return synth.weights_f16(M, K, s, "uniform", synth.seed_for(2, round(s * 10)))
+
+
+def sweep_acts(N):
+    """Seeded activations of the sparsity sweep: fp16 bits [N][8192]."""
+    return synth.activations_f16(N, SWEEP_SHAPE[1], synth.seed_for(2, N))
 
 
 def make_workload(only=None):
@@ -234,6 +265,29 @@ def time_oracle(Ws, xs, relu, bytes_per_call, stor, rows_per_layer=128, target_s
             "sample": f"first min({rows}, M) rows of each layer, every N in {list(NS)} plus the FC2 "
                       f"spMspV, {passes} pass(es) of the step on that row fraction; fp64 dense triple "
                       f"loop over fp16 inputs"}
+
+
+def time_oracle_extra(Ws, xs, relu, bytes_per_call, stor, target_s=5.0):
+    """Beside the all-cores figure: the same oracle product pinned to one
+    thread on a row sample sized to about target_s seconds, and the
+    oracle's encoder on the out-projection (5120 x 5120), whole."""
+    import oracle
+    oracle.build()
+    n_all = oracle.num_threads()
+    oracle.set_threads(1)
+    try:
+        one = time_oracle(Ws, xs, relu, bytes_per_call, stor, rows_per_layer=8, target_s=target_s)
+    finally:
+        oracle.set_threads(n_all)
+    W = Ws["out"]
+    t0 = time.perf_counter()
+    enc = oracle.encode(W)
+    enc_s = time.perf_counter() - t0
+    return {"single_thread_value": one["value"], "single_thread_cores": 1,
+            "single_thread_seconds": one["seconds"], "single_thread_rows_per_layer": one["rows_per_layer"],
+            "encode_seconds": round(enc_s, 3), "encode_layer": "out 5120x5120 fp16 50% magnitude",
+            "encode_MB_per_s": round(W.nbytes / enc_s / 1e6, 2),
+            "encode_storage_bytes": int(oracle.storage_bytes(enc))}
 
 
 def run_reference(args):
@@ -496,9 +550,14 @@ def run_gpu(args):
     if not args.no_sweep:
         sweep = run_sweep_leg(bsp, torch, dev, stream, ws)
 
+    int8 = None
+    if not args.no_int8:
+        int8 = run_int8_leg(bsp, torch, dev, stream, ws)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = time_oracle(Ws, xs, relu, bpc, stor, target_s=10.0)
+        cpu.update(time_oracle_extra(Ws, xs, relu, bpc, stor))
 
     d = by_kernel[dom]
     dach = d["bytes"] / (d["ms"] * 1e-3) / 1e9
@@ -516,6 +575,37 @@ def run_gpu(args):
                 "step": {"kernels": STEP_KERNELS, "achieved": round(achieved, 1),
                          "frac": round(achieved / peak, 4),
                          "algorithmic_bytes_per_launch": round(step_bytes / n_calls)}}
+    # flat scalars beside the nested records (readers that keep only the
+    # scalar fields of each object still see every headline figure)
+    for key, b in breakdown.items():
+        if key.startswith("N="):
+            roofline[f"frac_hbm_N{key[2:]}"] = b["frac_hbm"]
+            roofline[f"GBps_N{key[2:]}"] = b["GBps"]
+    roofline["spmspv_fc2_GBps"] = breakdown["spmspv_fc2"]["GBps"]
+    roofline["spmspv_fc2_us"] = breakdown["spmspv_fc2"]["us"]
+    roofline["spmspv_fc2_speedup_vs_spmm_n1"] = breakdown["spmspv_fc2"]["speedup_vs_spmm_n1"]
+    for n, e in roofline["by_kernel"].items():
+        roofline[f"{n}_frac"] = e["frac"]
+        roofline[f"{n}_share"] = e["share_of_step_time"]
+    roofline["step_achieved"] = roofline["step"]["achieved"]
+    roofline["step_frac"] = roofline["step"]["frac"]
+    if sweep:
+        for sk, row in sweep["points"].items():
+            for N in SWEEP_NS:
+                roofline[f"sweep_{sk.replace('=', '').replace('.', '')}_N{N}_frac"] = row[f"N={N}"]["frac_hbm"]
+            roofline[f"sweep_{sk.replace('=', '').replace('.', '')}_N1_us"] = row["N=1"]["us"]
+    if int8:
+        best = 0.0
+        for pk, row in int8["points"].items():
+            tag = pk.replace(" s=", "_s").replace(".", "")
+            for N in INT8_NS:
+                roofline[f"{tag}_N{N}_GBps"] = row[f"N={N}"]["GBps"]
+                best = max(best, row[f"N={N}"]["frac_hbm"])
+        roofline["int8_best_frac"] = best
+    if union:
+        for lk in ("W4A4", "W4A4_reordered", "W8A8"):
+            for N in UNION_NS:
+                roofline[f"union_{lk}_N{N}_frac"] = union[lk]["points"][f"N={N}"]["frac_hbm"]
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -523,7 +613,7 @@ def run_gpu(args):
                 "data": "synthetic (seeded numpy: N(0,0.02) weights, magnitude 50% mask, N(0,1) X)",
                 "config": _config(), "frac_hbm": round(value / ws / peak, 4),
                 "breakdown": breakdown, "prefill": prefill, "union_ie_bme": union,
-                "sparsity_sweep": sweep,
+                "sparsity_sweep": sweep, "int8": int8,
                 "roofline": roofline,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * args.steps,
                 "clocks": clk}
@@ -601,6 +691,51 @@ def run_union_leg(bsp, torch, dev, stream, ws, steps=20):
     return out
 
 
+def run_int8_leg(bsp, torch, dev, stream, ws, steps=20):
+    """INT8 bitmap SpMM (int8 W and X, exact int32 accumulation) on the
+    11008 x 4096 and 4096 x 11008 layers at 50% and 60%, N = 1, 8, 16.
+    Each configuration is encoded into enough copies to hold three times L2,
+    and the calls rotate over them, so every call reads its weight from HBM;
+    GB/s of the algorithmic bytes (storage + K*N + 4*M*N) per call."""
+    peak, peak_kind = _peaks()
+    out = {"unit": "GB/s", "peak": peak, "peak_kind": peak_kind, "points": {}}
+    for li, (name, M, K) in enumerate(INT8_LAYERS):
+        for s in INT8_SPARSITY:
+            W, X, _ = int8_inputs(li, s)
+            Wd = torch.from_numpy(W).to(dev)
+            first = bsp.BitmapMatrix(Wd)
+            stor = first.storage_bytes()
+            copies = max(2, -(-3 * L2_BYTES // stor))
+            mats = [first] + [bsp.BitmapMatrix(Wd) for _ in range(copies - 1)]
+            del Wd
+            torch.cuda.synchronize()
+            row = {"storage_bytes": stor, "compression_ratio": round(M * K / stor, 4), "copies": copies}
+            for N in INT8_NS:
+                Xd = torch.from_numpy(X[:N].copy()).to(dev)
+                Y = torch.empty((N, M), dtype=torch.int32, device=dev)
+
+                def rnd():
+                    for A in mats:
+                        A.spmm(Xd, out=Y, stream=stream)
+                for _ in range(3):
+                    rnd()
+                torch.cuda.synchronize()
+                s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+                for _ in range(steps):
+                    rnd()
+                e0.record(stream)
+                torch.cuda.synchronize()
+                us = _max_over_ranks(s0.elapsed_time(e0) / (steps * copies), ws) * 1e3
+                gbps = (stor + K * N + 4 * M * N) / (us * 1e-6) / 1e9
+                row[f"N={N}"] = {"us": round(us, 2), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4)}
+            for A in mats:
+                A.check()
+                A.close()
+            out["points"][f"{name} s={s:.1f}"] = row
+    return out
+
+
 def run_prefill_leg(bsp, torch, dev, stream, ws, reps=5):
     """Prefill TFLOP/s (tcgen05 kernel) on the Llama-2-70B FFN shapes.
 
@@ -617,7 +752,7 @@ def run_prefill_leg(bsp, torch, dev, stream, ws, reps=5):
         A = bsp.BitmapMatrix(torch.from_numpy(W.view(np.float16)).to(dev))
         del W
         for N in PREFILL_NS:
-            X = torch.from_numpy(synth.activations_f16(N, K, synth.seed_for(4, 2)).view(np.float16)).to(dev)
+            X = torch.from_numpy(prefill_acts(N, K).view(np.float16)).to(dev)
             Y = torch.empty((N, M), dtype=torch.float16, device=dev)
             for _ in range(3):
                 A.spmm(X, out=Y, stream=stream)
@@ -633,12 +768,17 @@ def run_prefill_leg(bsp, torch, dev, stream, ws, reps=5):
             out["points"][f"{name} {M}x{K} N={N}"] = {
                 "ms": round(ms, 4), "TFLOPs": round(tf, 1), "frac": round(tf / peak, 4),
                 "useful_TFLOPs": round(2.0 * nnz * N / (ms * 1e-3) / 1e12, 1)}
+            out[f"{name}_N{N}_TFLOPs"] = round(tf, 1)
+            out[f"{name}_N{N}_frac"] = round(tf / peak, 4)
             if best is None or tf > best[0]:
                 best = (tf, f"{name} N={N}")
             del X, Y
         A.check()
         A.close()
     out["best"] = {"TFLOPs": round(best[0], 1), "frac": round(best[0] / peak, 4), "at": best[1]}
+    out["best_TFLOPs"] = out["best"]["TFLOPs"]
+    out["best_frac"] = out["best"]["frac"]
+    out["best_at"] = best[1]
     return out
 
 
@@ -648,12 +788,19 @@ SWEEP_NS = (1, 4, 8, 16)
 L2_BYTES = 129 * 10**6
 
 
-def sweep_closed_form(M, K, s):
-    """Storage of an M x K fp16 layer (M, K multiples of 64) at sparsity s,
-    written from the format's parts: 2 bytes per kept value, one 8-byte
-    bitmap per 8 x 8 tile, one 4-byte offset per 64 x 64 group plus the
-    end offset."""
-    return 2 * (M * K - round(s * M * K)) + 8 * (M * K // 64) + 4 * (M * K // 4096 + 1)
+def sweep_closed_form(M, K, nnz):
+    """Storage of an M x K fp16 layer (M, K multiples of 64) holding nnz
+    stored values, written from the format's parts: 2 bytes per value, one
+    8-byte bitmap per 8 x 8 tile, one 4-byte offset per 64 x 64 group plus
+    the end offset."""
+    return 2 * nnz + 8 * (M * K // 64) + 4 * (M * K // 4096 + 1)
+
+
+def sweep_nominal_bytes(M, K, s):
+    """The same closed form at the nominal count of kept values, M*K -
+    round(s*M*K); a few N(0, 0.02) draws round to an fp16 zero, which the
+    format does not store, so the measured storage is a little lower."""
+    return sweep_closed_form(M, K, M * K - round(s * M * K))
 
 
 def run_sweep_leg(bsp, torch, dev, stream, ws, steps=20):
@@ -669,7 +816,7 @@ def run_sweep_leg(bsp, torch, dev, stream, ws, steps=20):
     M, K = SWEEP_SHAPE
     out = {"shape": f"{M}x{K} fp16", "unit": "GB/s", "peak": peak, "peak_kind": peak_kind, "points": {}}
     for s in SWEEP_SPARSITY:
-        W = synth.weights_f16(M, K, s, "uniform", synth.seed_for(2, round(s * 10)))
+        W = sweep_weights(s)
         nnz = int(np.count_nonzero(W))
         Wd = torch.from_numpy(W.view(np.float16)).to(dev)
         del W
@@ -679,10 +826,14 @@ def run_sweep_leg(bsp, torch, dev, stream, ws, steps=20):
         mats = [first] + [bsp.BitmapMatrix(Wd) for _ in range(copies - 1)]
         del Wd
         torch.cuda.synchronize()
-        row = {"nnz": nnz, "storage_bytes": stor, "closed_form_bytes": sweep_closed_form(M, K, s),
+        closed = sweep_closed_form(M, K, nnz)
+        if stor != closed:
+            raise RuntimeError(f"storage {stor} != closed form {closed} at s={s}")
+        row = {"nnz": nnz, "storage_bytes": stor, "closed_form_bytes": closed,
+               "nominal_closed_form_bytes": sweep_nominal_bytes(M, K, s),
                "compression_ratio": round(2 * M * K / stor, 4), "copies": copies}
         for N in SWEEP_NS:
-            X = torch.from_numpy(synth.activations_f16(N, K, synth.seed_for(2, N)).view(np.float16)).to(dev)
+            X = torch.from_numpy(sweep_acts(N).view(np.float16)).to(dev)
             Y = torch.empty((N, M), dtype=torch.float16, device=dev)
 
             def rnd():
@@ -729,6 +880,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-union", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-int8", action="store_true")
     ap.add_argument("--case", default=None,
                     help="LAYER:N, one configuration only (N=0: spMspV), for profiler captures")
     args = ap.parse_args()

@@ -23,9 +23,25 @@ import bench  # noqa: E402
 def test_sweep_closed_form_matches_the_oracle(M, K, s):
     W = synth.weights_f16(M, K, s, "uniform", 7 + M + K)
     enc = oracle.encode(W)
-    # every kept N(0, 0.02) draw is a nonzero fp16 at these sizes
-    assert int(np.count_nonzero(W)) == M * K - round(s * M * K)
-    assert bench.sweep_closed_form(M, K, s) == oracle.storage_bytes(enc)
+    nnz = int(np.count_nonzero(W))
+    assert bench.sweep_closed_form(M, K, nnz) == oracle.storage_bytes(enc)
+    # every kept N(0, 0.02) draw is a nonzero fp16 at these sizes, so the
+    # nominal count gives the same bytes
+    assert nnz == M * K - round(s * M * K)
+    assert bench.sweep_nominal_bytes(M, K, s) == oracle.storage_bytes(enc)
+
+
+def test_sweep_closed_form_counts_the_stored_values():
+    """Where some draws round to an fp16 zero (not stored), the closed form
+    from the measured count still equals the oracle's bytes exactly, and the
+    nominal estimate is above it by 2 bytes per such zero."""
+    M, K, s = 512, 512, 0.5
+    W = synth.weights_f16(M, K, s, "uniform", 11)
+    W[np.nonzero(W)[0][:5], np.nonzero(W)[1][:5]] = 0  # five kept values become zeros
+    nnz = int(np.count_nonzero(W))
+    enc = oracle.encode(W)
+    assert bench.sweep_closed_form(M, K, nnz) == oracle.storage_bytes(enc)
+    assert bench.sweep_nominal_bytes(M, K, s) - oracle.storage_bytes(enc) == 2 * 5
 
 
 def test_decode_step_bytes_count_weight_x_and_y():

@@ -345,18 +345,6 @@ def test_opt13b_layers_sampled_rows(layer):
         assert_within_bound(y[rows], yref[0], s[0], "fc2 spmspv")
 
 
-def test_int8_full_size_sampled():
-    M, K = 4096, 11008
-    W = synth.weights_i8(M, K, 0.5, synth.seed_for(5, 0))
-    X = synth.activations_i8(16, K, synth.seed_for(5, 5))
-    rows = sample_rows(M, 4, seed=3)
-    Yref = oracle.spmm_i8(W[rows], X)
-    A = _encode(W)
-    for N in (1, 8, 16):
-        Y = A.spmm(to_dev(X[:N].copy(), DEV)).cpu().numpy()
-        np.testing.assert_array_equal(Y[:, rows].astype(np.int64), Yref[:N])
-
-
 # ------------------------------------------------------------------ bounded waits
 
 def test_check_ok_after_normal_calls():

@@ -108,15 +108,3 @@ def test_prefill_all_zero_weight():
     W = np.zeros((128, 256), dtype=np.uint16)
     X = synth.activations_f16(33, 256, 331)
     assert np.all(_run(W, X) == 0)
-
-
-@pytest.mark.parametrize("M,K", [(28672, 8192), (8192, 28672)])
-def test_prefill_llama70b_ffn_sampled_rows(M, K):
-    """Llama-2-70B FFN shapes at 50%, N = 256, the oracle on 2 sampled rows
-    of every 64-row strip."""
-    W = synth.weights_f16(M, K, 0.5, "uniform", synth.seed_for(4, 0 if M > K else 1))
-    X = synth.activations_f16(256, K, synth.seed_for(4, 2))
-    Y = _run(W, X)
-    rows = sample_rows(M, 2, seed=M)
-    Yref, S = oracle.spmm_f16(W[rows], X)
-    assert_within_bound(Y[:, rows], Yref, S, f"llama {M}x{K}")

@@ -394,3 +394,21 @@ def test_pmr_of_dense_and_half_dense_grouptiles():
     two = np.zeros((64, 128), dtype=np.uint16)
     two[3, 70] = dense[0, 0]               # one value, two GroupTiles: 128 bitmaps + 3 offsets
     assert oracle.payload_to_metadata(oracle.encode(two)) == 2 / (1024 + 12)
+
+
+def test_csr_bytes_hand_counted():
+    """The CSR comparator counted by hand: a 3 x 5 matrix with 4 nonzeros
+    holds 4 values (2 B each in fp16, 1 B in int8), 4 column indices of 4 B
+    and 3 + 1 row pointers of 4 B: 8 + 16 + 16 = 40 B in fp16, 36 B in int8.
+    A dropped row-pointer array, a 2-byte index or an M-entry pointer array
+    each changes the count."""
+    W16 = np.zeros((3, 5), dtype=np.uint16)
+    W16[0, 1] = 0x3C00
+    W16[0, 4] = 0xBC00
+    W16[2, 0] = 0x4000
+    W16[2, 3] = 0x3800
+    assert oracle.csr_bytes(W16) == 4 * 2 + 4 * 4 + (3 + 1) * 4 == 40
+    W8 = np.zeros((3, 5), dtype=np.int8)
+    W8[W16 != 0] = 7
+    assert oracle.csr_bytes(W8) == 4 * 1 + 4 * 4 + (3 + 1) * 4 == 36
+    assert oracle.csr_bytes(np.zeros((6, 5), dtype=np.uint16)) == (6 + 1) * 4
