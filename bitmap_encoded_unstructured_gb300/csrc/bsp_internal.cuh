@@ -114,20 +114,20 @@ int bsp_decode_split_cap(const bsp_decode_problem& p);
 bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                   cudaStream_t s);
 
-// ---- tcgen05 narrow kernel (spmm_prefill.cu), fp16, 1 <= N <= 16 ----
-// One 16-column MMA tile per CTA, split-K over the workspace, counters and
-// deterministic slots of the decode problem (same invariants as the decode
-// kernels: the workspace and counters are zero between calls).
+// ---- tcgen05 narrow kernel (spmm_narrow.cu), fp16, 1 <= N <= 16 ----
+// Persistent, balanced over the SM slots; tiles split between CTAs meet in
+// the decode problem's workspace (zero between calls, fp32 [M][16] here) or,
+// in deterministic mode, in its slots ([slots][M][16]), and a second kernel
+// converts them.
 bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                  cudaStream_t s);
-// Its split count (BSP_NARROW_SPLITK overrides; clamped to the deterministic
-// slots when those are in use), and the automatic choice alone.
-int bsp_narrow_splits(const bsp_decode_problem& p);
-int bsp_narrow_splits_auto(const bsp_decode_problem& p);
+// Slots the deterministic mode needs for the automatic CTA count: the
+// largest number of CTAs that share one tile.
+int bsp_narrow_det_slots(const bsp_decode_problem& p);
 
 // ---- process-wide tuning (bsp_tuning.cu) ----
 // Tuning knobs of the dispatch, read once per process from the environment
-// (BSP_SPLITK, BSP_NARROW_SPLITK, BSP_UNION_SPLITK, BSP_NARROW_MIN_N,
+// (BSP_SPLITK, BSP_NARROW_CTAS, BSP_UNION_SPLITK, BSP_NARROW_MIN_N,
 // BSP_PF_KSPLIT, BSP_PF_SC) on first use and changed afterwards only by
 // bsp_set_tuning.  0 means "automatic" for the split counts and the C ring
 // depth; BSP_TUNE_PREFILL_KSPLIT is -1 (automatic), 0 or 1.

@@ -33,7 +33,7 @@ struct Range {
 
 constexpr Range kRange[kKnobs] = {
     {"BSP_SPLITK", 0, 4096, 0},
-    {"BSP_NARROW_SPLITK", 0, 4096, 0},
+    {"BSP_NARROW_CTAS", 0, 1 << 20, 0},
     {"BSP_UNION_SPLITK", 0, 4096, 0},
     {"BSP_NARROW_MIN_N", 1, 1024, BSP_NARROW_MIN_N_DEFAULT},
     {"BSP_PF_KSPLIT", -1, 1, -1},

@@ -1418,7 +1418,7 @@ int bsp_decode_split_cap(const bsp_decode_problem& p)
     const int64_t strips = p.Mp / 64, KT = p.Kp / 64;
     int cap = team_splits(p, false);
     for (int nt = 1; nt <= 2; ++nt) cap = std::max(cap, gtw_splits_auto(strips, KT, gtw_slots(p, nt)));
-    cap = std::max(cap, bsp_narrow_splits_auto(p));
+    cap = std::max(cap, bsp_narrow_det_slots(p));
     // cap >= the team kernel's floor (runs of at most kMaxRun GTs), so a
     // count clamped to it still satisfies that floor
     return cap;

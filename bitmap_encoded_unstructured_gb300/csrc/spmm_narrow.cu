@@ -1,33 +1,52 @@
 // Narrow product Y = W * X for fp16 and 1 <= N <= 16 on the 5th-generation
-// tensor cores: the decode-then-multiply scheme of the prefill kernel
-// (spmm_prefill.cu) with one MMA of N = 16 per K = 16.
+// tensor cores, the decoded weight tile held in tensor memory.
 //
 // Method: "load as sparse, compute as dense" ("Unified Static-Dynamic
 // Pruning for Efficient LLM Inference", section 4.3; "SpInfer: How bitmaps
 // make sparse LLMs actually fast", sections "Shared Memory Bitmap Decoding
-// (SMBD)" and "The async pipeline").  At N <= 16 the CUDA-core decode path
-// spends one FMA per nonzero and column (and the same again for the zero
-// positions, which are predicated, not skipped): at N = 16 that is more
-// instruction issue than the HBM budget of a GroupTile allows.  Decoded
-// into a dense A tile, the same GroupTile costs four tcgen05.mma
-// instructions at any N <= 16; the decode (about one shared-memory load
-// per position, no conversion, no FMA) then sets the pace.
+// (SMBD)" and "The async pipeline").  The compressed GroupTiles stream into
+// shared memory; decoder warps expand them into a dense fp16 tile and one
+// MMA of N = 16 per K = 16 multiplies it by the X tile.  At N <= 16 the
+// MMAs are almost free: the decode (one predicated shared-memory load per
+// position) sets the pace, so everything here serves the decoders.
 //
-// CTA tile: 128 rows of W (two GT row strips) x 16 columns of Y; one GT
-// column (K = 64) per pipeline step; `splits` CTAs share a tile's GT
-// columns (split-K) and meet in the handle's split-K workspace.  Rings:
-//   C  compressed data  bitmaps + value spans of the two GTs (bulk copies),
-//                       the rest of shared memory in stages sized for the
-//                       densest GT (up to SC_MAX), producer -> decoders
-//   A  decoded W tile   128 x 64 fp16, K-major, SWIZZLE_128B (16 KB),
-//                       2 stages, decoders -> MMA
-//   B  X sub-tiles      16 x 64 fp16, K-major, SWIZZLE_128B (TMA, rows
-//                       past N read as zeros), 8 stages, producer -> MMA
-// Warp roles (21 warps): warp 0 C producer; warp 1 TMEM allocation and the
-// MMA issuer (tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 16, K = 16);
-// warps 2-3 scanners (row starts of every BT row); warps 4-19 decoders
-// (whole row-bytes into the swizzled A tile); warp 20 B producer; warps 4-7
-// then the epilogue (tcgen05.ld of their TMEM lane quadrant).
+// The decoded tile goes to tensor memory (tcgen05.st), not to shared
+// memory: tcgen05.mma reads its A operand from there, so the A tile costs
+// no shared-memory bandwidth at all (neither the decoders' stores nor the
+// MMA's operand reads), leaving the shared-memory pipes to the value loads.
+// tcgen05.st lets warp w write only TMEM lanes 32 (w % 4) .. + 31, and A's
+// lane is the row, so a decoder warp owns 32 consecutive rows: lane l row
+// 32 (w % 4) + l of the 128-row tile, all eight octets (row-bytes) of the
+// step's GT column, 8 x 8 positions per lane per step.
+//
+// Work: a 128-row tile of W (two GT row strips) times the 16 columns of Y
+// takes KT steps, one GT column (K = 64) each.  The kernel is persistent and
+// balanced (stream-K): CTA c of P takes the steps [c T / P, (c + 1) T / P)
+// of the T = tiles x KT steps in tile-major order, so every CTA has the same
+// work and the pipeline stays full across tile boundaries.  A CTA
+// accumulates each tile it touches (a segment) in one of two TMEM
+// accumulators, alternating, so the epilogue of one segment overlaps the
+// MMAs of the next.  A tile covered by one segment is written to Y directly;
+// the segments of a tile split between CTAs add their fp32 partial sums into
+// the workspace (vector reductions, fire and forget), or store them to
+// per-segment slots in deterministic mode, and a small second kernel,
+// launched as a programmatic dependent of the first, converts those tiles
+// to fp16 (and clears the workspace).  Warps:
+//   0       C producer: bitmaps + value spans of the step's two GTs (bulk
+//           copies) into the C ring (the rest of shared memory, stages
+//           sized for the densest GT)
+//   1       TMEM allocation; MMA issuer (tcgen05.mma.cta_group::1.kind::f16,
+//           A from tensor memory, B = the X tile in shared memory, M = 128,
+//           N = 16, K = 16, four per step)
+//   2       B producer: the 16 x 64 X tile of each step by TMA (rows past N
+//           read as zeros)
+//   3 ..    decoders, NG groups of four warps (one per TMEM lane quadrant);
+//           group g takes the CTA's steps g, g + NG, ... and owns A stage g
+//           in tensor memory.  Per step a warp scans the popcounts of its 32
+//           BitmapTiles (its half of a GT), writes their row starts to a
+//           private table, then decodes its 256 row-bytes.  The group that
+//           decodes the last step of a segment is also its epilogue
+//           (tcgen05.ld of the accumulator, then Y or the workspace).
 // Every wait is bounded; a wait that gives up stores BSP_ERR_TIMEOUT in the
 // error word, and the CTA still drains its copies, waits for its MMAs and
 // frees its tensor memory before it exits.
@@ -43,71 +62,75 @@
 #include <cstdlib>
 #include <mutex>
 
-// Self-checks (off by default): bounds of every global access and of the
-// data-derived shared-memory addresses, recorded in the error word as
-// 100 + site, the access skipped.
-#ifndef BSP_NW_CHECKS
-#define BSP_NW_CHECKS 0
-#endif
 // split model: fixed cost of a CTA in GT-column steps
 #ifndef BSP_NARROW_CTA_COST
 #define BSP_NARROW_CTA_COST 6
 #endif
-// resident CTAs per SM: 1 gives a CTA the whole shared memory (the deepest
-// C ring); 2 halves it and caps the registers at 48 per thread, so that a
-// second CTA's 21 warps hide the decoders' latency
+// resident CTAs per SM (1 or 2): shared memory and registers are split
+// between them
 #ifndef BSP_NARROW_MINB
 #define BSP_NARROW_MINB 2
+#endif
+// decoder groups of four warps (steps in flight, A stages in tensor memory)
+#ifndef BSP_NARROW_GROUPS
+#define BSP_NARROW_GROUPS 3
 #endif
 
 namespace {
 
 constexpr int BM = 128, BN = 16, BK = 64;  // tile rows, MMA columns, GT columns per step
-constexpr int A_BYTES = BM * BK * 2;       // 16384
-constexpr int DEC_WARPS = 16;              // eight per GroupTile
-constexpr int WPG = DEC_WARPS / 2;         // decoder warps per GroupTile
-constexpr int NR = 2;                      // row-bytes per decoder lane and step
-static_assert(WPG * 32 * NR == 512, "the decoder warps of a GT cover its 64 x 8 row-bytes");
-constexpr int DEC0 = 4;                    // first decoder warp (after producer, MMA, 2 scanners)
-constexpr int BPROD = DEC0 + DEC_WARPS;    // B (X tile) producer, the last warp
-constexpr int WARPS = BPROD + 1;
+constexpr int NG = BSP_NARROW_GROUPS;
+static_assert(NG >= 1 && NG <= 6, "decoder groups");
+constexpr int DEC_WARPS = 4 * NG;
+constexpr int CPROD = 0, MMAW = 1, BPROD = 2, DEC0 = 3;
+constexpr int WARPS = DEC0 + DEC_WARPS;
 constexpr int THREADS = WARPS * 32;
-constexpr int RS_BYTES = 64 * 8 * 2;       // row starts of one GT: [BT][row] u16
 constexpr uint32_t kSleepNs = 1000;        // suspend hint of the waiting polls
 
-constexpr int SB = 8;                      // X sub-tile stages
-constexpr int SA = 2;                      // decoded A tile stages
-constexpr int SC_MAX = 12;                 // barrier slots of the C ring
+constexpr int SB = 8;                      // X tile stages
+constexpr int SC_MAX = 16;                 // barrier slots of the C ring
 constexpr int MINB = BSP_NARROW_MINB;
 static_assert(MINB == 1 || MINB == 2, "one or two CTAs per SM");
 // shared memory of a CTA: all of it, or half of the SM's 228 KB less the
 // 1 KB the driver reserves per resident CTA
 constexpr int SMEM_MAX = MINB == 1 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
 constexpr int B_STAGE = BN * BK * 2;       // 2 KB
-constexpr int OFF_B = 0;                   // 1024-B aligned regions first
-constexpr int OFF_A = OFF_B + SB * B_STAGE;
-constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
-// barriers: c_full[SC_MAX] c_empty[SC_MAX] c_scan[SC_MAX] b_full[SB] b_empty[SB] a_full[SA] a_empty[SA] acc
-constexpr int NBAR = 3 * SC_MAX + 2 * SB + 2 * SA + 1;
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // TMEM address (4 B), last-CTA flag (4 B)
+constexpr int RS_WARP = 32 * 8 * 2;        // a decoder warp's row-start table: [BT][row] u16
+constexpr int OFF_B = 0;                   // 1024-B aligned (the X tiles' 128-B swizzle)
+constexpr int OFF_RS = OFF_B + SB * B_STAGE;
+constexpr int OFF_BAR = OFF_RS + DEC_WARPS * RS_WARP;
+// barriers: c_full[SC_MAX] c_empty[SC_MAX] b_full[SB] b_empty[SB] a_full[NG] a_empty[NG]
+// acc_full[2] acc_empty[2] drain
+constexpr int NBAR = 2 * SC_MAX + 2 * SB + 2 * NG + 5;
+constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // TMEM address (4 B)
 constexpr int OFF_C = (OFF_TMEM + 16 + 127) & ~127;
 constexpr int C_BYTES = SMEM_MAX - 1024 - OFF_C;  // 1024: slack to align the base to 1024 B
-constexpr uint32_t TMEM_COLS = 32;                // the allocation minimum; the accumulator uses 16
+// tensor memory: two accumulators (16 fp32 columns each, 32 apart), then NG
+// decoded A tiles of 128 lanes x 64 fp16 = 32 columns each
+constexpr uint32_t D_COLS = 32;
+constexpr uint32_t A_OFF = 2 * D_COLS;
+constexpr uint32_t A_COLS = BK / 2;
+constexpr uint32_t tmem_cols_for(uint32_t need)
+{
+    uint32_t c = 32;
+    while (c < need) c <<= 1;
+    return c;
+}
+constexpr uint32_t TMEM_COLS = tmem_cols_for(A_OFF + NG * A_COLS);
+static_assert(TMEM_COLS * MINB <= 512, "tensor memory of the resident CTAs");
 
 // One C stage: two GT slots (512 B of bitmaps, then the 16-B chunks that
-// hold the GT's value span), a 16-B header (the value shifts) and the row
-// starts of the two GTs.  The slot is sized for the densest GT of the
-// matrix, so the number of stages that fit follows the density.
+// hold the GT's value span) and a 16-B header (the value shifts).  The slot
+// is sized for the densest GT of the matrix, so the number of stages that
+// fit follows the density.
 constexpr uint32_t c_slot_bytes(uint32_t max_gt_nnz)
 {
     return (512u + 16u * ((max_gt_nnz + 7u) / 8u + 1u) + 127u) & ~127u;
 }
-constexpr uint32_t c_stage_bytes(uint32_t slot)
-{
-    return (2u * slot + 16u + 2u * (uint32_t)RS_BYTES + 127u) & ~127u;
-}
-static_assert(C_BYTES >= 2 * (int)c_stage_bytes(c_slot_bytes(4096)), "two dense C stages");
-static_assert((B_STAGE % 1024) == 0 && (A_BYTES % 1024) == 0, "swizzle atoms need 1024-B alignment");
+constexpr uint32_t c_stage_bytes(uint32_t slot) { return (2u * slot + 16u + 127u) & ~127u; }
+static_assert(C_BYTES >= NG * (int)c_stage_bytes(c_slot_bytes(4096)) && NG <= SC_MAX,
+              "a dense C stage per decoder group");
+static_assert((B_STAGE % 1024) == 0 && (OFF_RS % 16) == 0, "alignment of the X tiles and tables");
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
 // M = 128, N = 16.
@@ -120,21 +143,26 @@ struct NarrowArgs {
     __half* Y;
     int64_t M, N, K;           // logical: Y rows, columns, X row length
     int64_t Mp, KT;            // padded grid: rows (a multiple of 64), GT columns
+    int64_t T;                 // steps of the whole product: tiles x KT
+    int64_t P;                 // CTAs (1 <= P <= T)
     uint32_t c_slot, c_stage;  // C ring geometry (bytes): GT slot, stage
-    int sc;                    // C stages in use, 2..SC_MAX
-    // split-K over `splits` CTAs per tile: partial sums into the workspace
-    // [N][M] fp32 (zero between calls) by atomic adds, or into the
-    // deterministic slots [splits][N][M]; one arrival counter per tile (at
-    // its first 64-row strip); the last CTA of a tile writes Y
-    int splits;
+    int sc;                    // C stages in use, NG..SC_MAX
+    // partial sums of the tiles split between CTAs: fp32 [M][16], zero
+    // between calls (vector reductions; the finishing kernel clears it), or
+    // in deterministic mode the slots [slots][M][16], one per segment
     float* ws;
     float* ws_det;
-    uint32_t* counters;
-    int64_t ngt;            // GTs of the grid (self-checks)
-    uint64_t values_bytes;  // bytes allocated for values, 0: unknown (self-checks)
     int* err;
     uint32_t spin_cap;
 };
+
+// The balanced partition: CTA c owns steps [c T / P, (c + 1) T / P), so the
+// owner of step x is the largest c whose range starts at or before x.
+__host__ __device__ __forceinline__ int64_t part_begin(int64_t c, int64_t T, int64_t P) { return c * T / P; }
+__host__ __device__ __forceinline__ int64_t step_owner(int64_t x, int64_t T, int64_t P)
+{
+    return ((x + 1) * P - 1) / T;
+}
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzled canonical layout: rows of 128 B, 8-row atoms of 1 KB (stride
@@ -150,30 +178,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
     return d;
 }
 
-__device__ __forceinline__ int bt_local(int br, int bc)
-{
-    return (((br >> 1) * 4 + (bc >> 1)) << 2) + (br & 1) + ((bc & 1) << 1);
-}
-
-// One position of a row-byte, without a branch: if rbyte & bit, the next
-// packed fp16 value (shared-memory byte address `addr`) zero-extended, and
-// addr advances by one value; else 0.  Volatile: it reads shared memory,
-// so it is neither duplicated nor moved across the ring-barrier waits.
-__device__ __forceinline__ uint32_t take_f16(uint32_t& addr, uint32_t rbyte, uint32_t bit)
-{
-    uint32_t v;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
-        "and.b32 t, %2, %3;\n\t"
-        "setp.ne.b32 p, t, 0;\n\t"
-        "mov.b32 %0, 0;\n\t"
-        "@p ld.shared.u16 %0, [%1];\n\t"
-        "@p add.u32 %1, %1, 2;\n\t}"
-        : "=r"(v), "+r"(addr)
-        : "r"(rbyte), "r"(bit));
-    return v;
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
 {
     asm volatile(
@@ -183,13 +187,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum)
+// D (tensor memory) += A (tensor memory, 128 lanes x 8 columns = 16 fp16
+// per row) * B (shared-memory descriptor), or D = A * B when accum is 0.
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accum)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(kIdesc), "r"(accum)
         : "memory");
 }
 
@@ -202,6 +208,13 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// ws[0..3] += v[0..3], one vector reduction without a return value
+__device__ __forceinline__ void red_add_v4(float* ws, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ws), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
 
 // 16 consecutive TMEM columns of this thread's lane (32x32b shape, x16).
 // Whole warps only: the .aligned form runs on a reconverged warp.
@@ -218,14 +231,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Grid: tiles x splits CTAs, split fastest; CTA (tile, part) takes the
-// balanced share [part * KT / splits, (part + 1) * KT / splits) of the GT
-// columns (at least one: the host keeps splits <= KT).
+// 16 consecutive TMEM columns of this thread's lane from registers (32x32b
+// shape, x16).  Whole warps only.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r)
+{
+    __syncwarp();
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// The eight positions of one BT row-byte as four words of two fp16 each
+// (position 2k in the low half of word k): a set bit takes the next packed
+// value (shared memory, in order), a clear bit gives 0.  The loads are plain
+// predicated loads the compiler schedules; they stay after the ring-barrier
+// wait, whose inline assembly clobbers memory.
+__device__ __forceinline__ void decode_rowbyte(const uint16_t* vp, uint32_t byte, uint32_t* w)
+{
+    uint32_t h[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        h[c] = 0u;
+        if (byte & (1u << c)) {
+            h[c] = *vp;
+            ++vp;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __byte_perm(h[2 * k], h[2 * k + 1], 0x5410);
+}
+
+// Grid: P CTAs, persistent: CTA c takes the steps [c T / P, (c + 1) T / P)
+// (step x is GT column x % KT of tile x / KT).
 __global__ void __launch_bounds__(THREADS, MINB)
 spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
 {
-    const int SC = a.sc;
-    const uint32_t SLOT = a.c_slot, C_HDR = 2 * SLOT, C_RS = C_HDR + 16;
+    const uint32_t SC = (uint32_t)a.sc;
+    const uint32_t SLOT = a.c_slot, C_HDR = 2 * SLOT;
     const uint32_t vchunks = (SLOT - 512) / 16;  // value chunks a slot holds
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-B alignment of the shared-window offset (the 128-B swizzle atoms)
@@ -236,29 +281,27 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     const int warp = threadIdx.x >> 5;
     uint64_t* c_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* c_empty = c_full + SC_MAX;
-    uint64_t* c_scan = c_empty + SC_MAX;
-    uint64_t* b_full = c_scan + SC_MAX;
+    uint64_t* b_full = c_empty + SC_MAX;
     uint64_t* b_empty = b_full + SB;
     uint64_t* a_full = b_empty + SB;
-    uint64_t* a_empty = a_full + SA;
-    uint64_t* acc_bar = a_empty + SA;
+    uint64_t* a_empty = a_full + NG;
+    uint64_t* acc_full = a_empty + NG;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
-    int* s_last = reinterpret_cast<int*>(smem + OFF_TMEM + 4);
-    auto b_stage = [&](int s) { return smem + OFF_B + s * B_STAGE; };
-    auto a_stage = [&](int s) { return smem + OFF_A + s * A_BYTES; };
-    auto c_stage = [&](int s) { return smem + OFF_C + s * a.c_stage; };
+    auto b_stage = [&](uint32_t s) { return smem + OFF_B + s * B_STAGE; };
+    auto c_stage = [&](uint32_t s) { return smem + OFF_C + s * a.c_stage; };
 
-    const int64_t M = a.M, N = a.N;
-    const uint32_t KTA = (uint32_t)a.KT;  // GT columns of the grid (row pitch)
-    const uint32_t part = blockIdx.x % (uint32_t)a.splits, nparts = (uint32_t)a.splits;
-    const uint32_t k0 = (uint32_t)((uint64_t)part * KTA / nparts);             // first GT column
-    const uint32_t KT = (uint32_t)((uint64_t)(part + 1) * KTA / nparts) - k0;  // GT columns of this CTA
-    const int64_t mt = (int64_t)(blockIdx.x / (uint32_t)a.splits);              // tile
-    const int64_t strip0 = 2 * mt, strip1 = 2 * mt + 1;
-    const bool has_b = strip1 * 64 < a.Mp;  // second GT row strip of the tile exists
+    const int64_t M = a.M, N = a.N, T = a.T, P = a.P;
+    const uint32_t KTA = (uint32_t)a.KT;  // GT columns of the grid (row pitch, steps per tile)
+    const int64_t cta = blockIdx.x;
+    const int64_t g0 = part_begin(cta, T, P);
+    const uint32_t S = (uint32_t)(part_begin(cta + 1, T, P) - g0);  // steps of this CTA (>= 1: P <= T)
+    const int64_t t0 = g0 / KTA;                                    // first tile
+    const uint32_t kk0 = (uint32_t)(g0 - t0 * KTA);                 // its first GT column
     const uint32_t cap = a.spin_cap;
 
-    if (warp == 1) {  // 32 TMEM columns (the minimum) for the 128 x 16 accumulator
+    if (warp == MMAW) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          bspx::smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
@@ -266,20 +309,23 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SC; ++s) {
+        for (uint32_t s = 0; s < SC; ++s) {
             bspx::mbar_init(c_full + s, 1);
-            bspx::mbar_init(c_empty + s, DEC_WARPS);
-            bspx::mbar_init(c_scan + s, 2 * 32);  // every scanner lane
+            bspx::mbar_init(c_empty + s, 4);  // the four warps of the step's decoder group
         }
         for (int s = 0; s < SB; ++s) {
             bspx::mbar_init(b_full + s, 1);
             bspx::mbar_init(b_empty + s, 1);
         }
-        for (int s = 0; s < SA; ++s) {
-            bspx::mbar_init(a_full + s, DEC_WARPS);
-            bspx::mbar_init(a_empty + s, 1);
+        for (int g = 0; g < NG; ++g) {
+            bspx::mbar_init(a_full + g, 4);
+            bspx::mbar_init(a_empty + g, 1);
         }
-        bspx::mbar_init(acc_bar, 1);
+        for (int d = 0; d < 2; ++d) {
+            bspx::mbar_init(acc_full + d, 1);
+            bspx::mbar_init(acc_empty + d, 4);  // the four warps of an epilogue
+        }
+        bspx::mbar_init(drain, 1);
         bspx::fence_mbar_init();
     }
     tc_fence_before();
@@ -288,34 +334,29 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     const uint32_t tmem_base = *tmem_slot;
     bool failed = false;
 
-    if (warp == 0) {
+    if (warp == CPROD) {
         // ---------------- C producer: the two GTs of each step, up to SC steps ahead
-        const int64_t ta = strip0 * KTA + k0, tb = strip1 * KTA + k0;
+        int64_t t = t0;
+        uint32_t k = kk0;
         uint32_t offa = 0, offb = 0;
         uint32_t wbase = 0;
         uint32_t s = 0, ph = 0;  // stage and its phase parity
-        uint32_t kc = 0;         // steps issued
-        for (; kc < KT; ++kc) {
-            if (kc >= (uint32_t)SC &&
-                !__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph ^ 1u, cap, kSleepNs))) {
+        uint32_t i = 0;          // steps issued
+        for (; i < S; ++i) {
+            if (i >= SC && !__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph ^ 1u, cap, kSleepNs))) {
                 failed = true;
                 break;
             }
-            if (kc == 0 || kc - wbase >= 31) {  // window of offsets: lane i holds offsets[t + wbase + i]
-                wbase = kc;
-                const uint32_t i = wbase + lane;
-                offa = offb = 0;
-#if BSP_NW_CHECKS
-                if ((i <= KT && ta + i > a.ngt) || (has_b && i <= KT && tb + i > a.ngt))
-                    atomicCAS(a.err, 0, 101);
-                else
-#endif
-                {
-                    if (i <= KT) offa = __ldg(a.offsets + ta + i);
-                    if (has_b && i <= KT) offb = __ldg(a.offsets + tb + i);
-                }
+            const int64_t ta = 2 * t * KTA, tb = ta + KTA;  // the tile's two GT rows
+            const bool has_b = (2 * t + 1) * 64 < a.Mp;
+            if (i == 0 || k == 0 || k - wbase >= 31) {
+                // window of offsets: lane j holds offsets[row + wbase + j] (j <= KT: the row's end)
+                wbase = k;
+                const uint32_t j = wbase + lane;
+                offa = (j <= KTA) ? __ldg(a.offsets + ta + j) : 0u;
+                offb = (has_b && j <= KTA) ? __ldg(a.offsets + tb + j) : 0u;
             }
-            const int w = (int)(kc - wbase);
+            const int w = (int)(k - wbase);
             const uint32_t oa0 = __shfl_sync(FULL, offa, w), oa1 = __shfl_sync(FULL, offa, w + 1);
             const uint32_t ob0 = __shfl_sync(FULL, offb, w), ob1 = __shfl_sync(FULL, offb, w + 1);
             if (lane == 0) {
@@ -328,35 +369,30 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                     nca = min(nca, vchunks);
                     ncb = min(ncb, vchunks);
                 }
-#if BSP_NW_CHECKS
-                if (a.values_bytes && ((uint64_t)(cha + nca) * 16 > a.values_bytes ||
-                                       (uint64_t)(chb + ncb) * 16 > a.values_bytes)) {
-                    atomicCAS(a.err, 0, 102);
-                    nca = ncb = 0;
-                }
-#endif
                 hdr[0] = oa0 - cha * 8;
                 hdr[1] = ob0 - chb * 8;
                 uint32_t bytes = 512 + nca * 16;
                 if (has_b) bytes += 512 + ncb * 16;
                 bspx::mbar_arrive_expect_tx(c_full + s, bytes);
-                bspx::bulk_g2s(st, a.bitmaps + (ta + kc) * 64, 512, c_full + s);
+                bspx::bulk_g2s(st, a.bitmaps + (ta + k) * 64, 512, c_full + s);
                 if (nca) bspx::bulk_g2s(st + 512, a.values + (int64_t)cha * 16, nca * 16, c_full + s);
                 if (has_b) {
-                    bspx::bulk_g2s(st + SLOT, a.bitmaps + (tb + kc) * 64, 512, c_full + s);
+                    bspx::bulk_g2s(st + SLOT, a.bitmaps + (tb + k) * 64, 512, c_full + s);
                     if (ncb) bspx::bulk_g2s(st + SLOT + 512, a.values + (int64_t)chb * 16, ncb * 16, c_full + s);
                 }
             }
-            if (++s == (uint32_t)SC) { s = 0; ph ^= 1u; }
+            if (++s == SC) { s = 0; ph ^= 1u; }
+            if (++k == KTA) { k = 0; ++t; }
         }
         // let the last copies land before the CTA can exit (bounded)
-        for (uint32_t k = (kc > (uint32_t)SC ? kc - SC : 0); k < kc; ++k)
-            bspx::mbar_wait_bounded(c_full + (k % SC), (k / SC) & 1u, cap);
+        for (uint32_t j = (i > SC ? i - SC : 0); j < i; ++j)
+            bspx::mbar_wait_bounded(c_full + (j % SC), (j / SC) & 1u, cap);
     } else if (warp == BPROD) {
-        // ---------------- B producer: one 16 x 64 X sub-tile per step by TMA
+        // ---------------- B producer: one 16 x 64 X tile per step by TMA
         uint32_t s = 0, ph = 0;
+        uint32_t k = kk0;
         uint32_t i = 0;
-        for (; i < KT; ++i) {
+        for (; i < S; ++i) {
             if (i >= (uint32_t)SB &&
                 !__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph ^ 1u, cap, kSleepNs))) {
                 failed = true;
@@ -364,196 +400,207 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             }
             if (lane == 0) {
                 bspx::mbar_arrive_expect_tx(b_full + s, (uint32_t)B_STAGE);
-                tma_load_2d(b_stage(s), &tmX, (int)((k0 + i) * BK), 0, b_full + s);
+                tma_load_2d(b_stage(s), &tmX, (int)(k * BK), 0, b_full + s);
             }
             if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
+            if (++k == KTA) k = 0;
         }
-        for (uint32_t k = (i > (uint32_t)SB ? i - SB : 0); k < i; ++k)
-            bspx::mbar_wait_bounded(b_full + (k % SB), (k / SB) & 1u, cap);
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
-        uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
-        for (uint32_t kb = 0; kb < KT && !failed; ++kb) {
-            bool ok = bspx::mbar_wait_sleep(a_full + sa, pa, cap, kSleepNs);
+        for (uint32_t j = (i > (uint32_t)SB ? i - SB : 0); j < i; ++j)
+            bspx::mbar_wait_bounded(b_full + (j % SB), (j / SB) & 1u, cap);
+    } else if (warp == MMAW) {
+        // ---------------- MMA issuer: step i reads A stage i % NG and
+        // accumulates into buffer (segment & 1); the first MMA of a segment
+        // overwrites the buffer, which the epilogue two segments back must
+        // have read
+        uint32_t sb = 0, pb = 0;
+        uint32_t k = kk0, seg = 0;
+        for (uint32_t i = 0; i < S && !failed; ++i) {
+            const uint32_t g = i % NG;
+            const bool first = i == 0 || k == 0, last = i + 1 == S || k + 1 == KTA;
+            const uint32_t buf = seg & 1u;
+            bool ok = bspx::mbar_wait_sleep(a_full + g, (i / NG) & 1u, cap, kSleepNs);
             ok = ok && bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
+            if (first && seg >= 2) ok = ok && bspx::mbar_wait_sleep(acc_empty + buf, ((seg - 2) >> 1) & 1u, cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint64_t ad = smem_desc_sw128(bspx::smem_u32(a_stage(sa)));
+                const uint32_t ta = tmem_base + A_OFF + g * A_COLS;
+                const uint32_t td = tmem_base + buf * D_COLS;
                 const uint64_t bd = smem_desc_sw128(bspx::smem_u32(b_stage(sb)));
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 32 B along the swizzled row
-                    umma_f16(tmem_base, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), (kb | j) ? 1u : 0u);
+                for (int j = 0; j < BK / 16; ++j)  // K = 16 per MMA: 8 A columns, 32 B along the swizzled X row
+                    umma_f16_ts(td, ta + (uint32_t)(8 * j), bd + (uint64_t)(2 * j), (first && j == 0) ? 0u : 1u);
                 umma_commit(b_empty + sb);  // fire once the MMAs above are done
-                umma_commit(a_empty + sa);
+                umma_commit(a_empty + g);
+                if (last) umma_commit(acc_full + buf);
             }
             __syncwarp();
             if (++sb == (uint32_t)SB) { sb = 0; pb ^= 1u; }
-            if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
+            if (last) ++seg;
+            if (++k == KTA) k = 0;
         }
-        if (lane == 0) umma_commit(acc_bar);  // fires once every MMA issued above is done
+        // every MMA issued above is done before the CTA frees tensor memory
+        if (lane == 0) umma_commit(drain);
         __syncwarp();
-        bspx::mbar_wait_bounded(acc_bar, 0, cap);
+        bspx::mbar_wait_bounded(drain, 0, cap);
         __syncwarp();
-    } else if (warp < DEC0) {
-        // ---------------- scanners: row starts of GT (warp - 2)
-        const int gsel = warp - 2;
-        const bool active = gsel == 0 || has_b;
-        uint32_t sc = 0, pc = 0;
-        for (uint32_t kb = 0; kb < KT; ++kb) {
-            const bool ok = bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
+    } else {
+        // ---------------- decoders.  Warp: group G (its steps), TMEM lane
+        // quadrant q = rows 32 q .. 32 q + 31 of the tile = half h of GT
+        // gsel.  Lane l: row 32 h + l of the GT, which lies in BT row
+        // (l / 8) & 1 of TCTile row l / 16 of the half; its row-byte of
+        // octet o is row l % 8 of the half's BT (4 (l / 16) + o / 2) * 4 +
+        // 2 (o % 2) + (l / 8) % 2 (BTs in GT order).
+        const int dw = warp - DEC0;
+        const uint32_t G = (uint32_t)(dw >> 2);
+        const int q = warp & 3;
+        const int gsel = q >> 1, h = q & 1;
+        const uint32_t tq = (uint32_t)(32 * q) << 16;  // TMEM lane field of the quadrant
+        const uint32_t tA = tmem_base + A_OFF + G * A_COLS + tq;
+        uint16_t* rs = reinterpret_cast<uint16_t*>(smem + OFF_RS + dw * RS_WARP);
+        const int ri = lane & 7;
+        const int bt0 = 16 * (lane >> 4) + ((lane >> 3) & 1);  // the lane's BT of octet 0 (half-local)
+        // step i = G, G + NG, ...: its tile, GT column, C stage and parity
+        int64_t t = t0;
+        uint32_t k = kk0 + G;
+        while (k >= KTA) { k -= KTA; ++t; }
+        uint32_t sc = G, pc = 0;
+        uint32_t it = 0;
+        for (uint32_t i = G; i < S; i += NG, ++it) {
+            bool ok = bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
+            // the MMAs of this group's previous step read A stage G: done
+            if (it > 0) ok = ok && bspx::mbar_wait_sleep(a_empty + G, (it - 1) & 1u, cap, kSleepNs);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
-            uint8_t* st = c_stage(sc);
+            tc_fence_after();
+            const bool active = gsel == 0 || (2 * t + 1) * 64 < a.Mp;  // a missing second strip: zeros
+            uint32_t w[16];
             if (active) {
-                // lane: BTs 2 lane and 2 lane + 1 (GT order = value order)
-                const ulonglong2 bb = reinterpret_cast<const ulonglong2*>(st + gsel * SLOT)[lane];
-                const uint32_t shift = reinterpret_cast<const uint32_t*>(st + C_HDR)[gsel];
-                const uint32_t c0 = __popcll(bb.x), c1 = __popcll(bb.y);
-                uint32_t incl = c0 + c1;
+                const uint8_t* slot = c_stage(sc) + gsel * SLOT;
+                // BT value bases: lane l owns BT 32 h + l (GT order = value order)
+                const uint64_t* bms = reinterpret_cast<const uint64_t*>(slot);
+                const uint64_t bm = bms[32 * h + lane];
+                const uint32_t cnt = (uint32_t)__popcll(bm);
+                uint32_t incl = cnt;
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
                     const uint32_t o = __shfl_up_sync(FULL, incl, d);
                     if (lane >= d) incl += o;
                 }
-                const uint32_t base0 = incl - (c0 + c1) + shift;
-                uint4* rs = reinterpret_cast<uint4*>(st + C_RS + gsel * RS_BYTES) + 2 * lane;
-                rs[0] = bspx::row_starts(bb.x, base0);
-                rs[1] = bspx::row_starts(bb.y, base0 + c0);
-            }
-            __syncwarp();
-            bspx::mbar_arrive(c_scan + sc);  // release: the row starts above
-            if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
-        }
-    } else if (warp < BPROD) {
-        // ---------------- decoders.  Row-byte j of a lane: row 16q + lane % 16
-        // of the GT, octet bc = 2 p0 + 2 (lane / 16) + j; its eight positions
-        // become one whole 16-B chunk of the A tile.  Each quarter-warp
-        // writes the chunks of eight consecutive rows of one octet, which the
-        // swizzle puts in distinct banks.
-        const int dw = warp - DEC0;
-        const int gsel = dw / WPG, wq = dw % WPG;
-        const int q = wq / 2;         // TCTile row of the warp (16 GT rows)
-        const int p0 = (wq % 2) * 2;  // first TCTile column (octet pair) of the warp
-        const int row = 16 * q + (lane & 15);  // row inside the GT
-        const int trow = 64 * gsel + row;      // row inside the 128-row tile
-        int ent[NR];       // BT row entry: 8 g + row % 8 (bitmap byte / row start)
-        uint32_t dst[NR];  // byte offset of the row-byte's 16-B chunk in A (128-B swizzle)
+                uint32_t base = incl - cnt + reinterpret_cast<const uint32_t*>(c_stage(sc) + C_HDR)[gsel];
+                if (h) base += __reduce_add_sync(FULL, (uint32_t)__popcll(bms[lane]));  // the first half's values
+                *reinterpret_cast<uint4*>(rs + 8 * lane) = bspx::row_starts(bm, base);
+                __syncwarp();
+                const uint8_t* bytes = slot + 256 * h;  // byte 8 bt + r: row r of the half's BT bt
+                const uint16_t* vals = reinterpret_cast<const uint16_t*>(slot + 512);
 #pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int bc = 2 * p0 + 2 * (lane >> 4) + j;
-            ent[j] = 8 * bt_local(row >> 3, bc) + (row & 7);
-            dst[j] = (uint32_t)((trow >> 3) * 1024 + (trow & 7) * 128 + ((bc ^ (trow & 7)) << 4));
-        }
-        const bool active = gsel == 0 || has_b;
-        uint32_t sc = 0, pc = 0, sa = 0, pa = 0;
-        for (uint32_t kb = 0; kb < KT; ++kb) {
-            // c_scan implies c_full: the scanners arrive only after they saw it
-            bool ok = bspx::mbar_wait_sleep(c_scan + sc, pc, cap, kSleepNs);
-            if (kb >= (uint32_t)SA) ok = ok && bspx::mbar_wait_sleep(a_empty + sa, pa ^ 1u, cap, kSleepNs);
-            if (!__all_sync(FULL, ok)) { failed = true; break; }
-            const uint8_t* st = c_stage(sc);
-            uint8_t* at = a_stage(sa);
-            if (active) {
-                const uint8_t* bmb = st + gsel * SLOT;  // bitmap bytes: byte 8 g + r = row r of BT g
-                const uint16_t* rst = reinterpret_cast<const uint16_t*>(st + C_RS + gsel * RS_BYTES);
-                const uint32_t vbase = bspx::smem_u32(st + gsel * SLOT + 512);
+                for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                for (int j = 0; j < NR; ++j) {
-                    const uint32_t byte = bmb[ent[j]];
-                    uint32_t start = (uint32_t)rst[ent[j]];
-#if BSP_NW_CHECKS
-                    if (2u * (start + 8u) > SLOT - 512u) { atomicCAS(a.err, 0, 110); start = 0; }
-#endif
-                    uint32_t addr = vbase + 2u * start;
-                    uint32_t h[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) h[c] = take_f16(addr, byte, 1u << c);
-                    *reinterpret_cast<uint4*>(at + dst[j]) =
-                        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                    for (int oo = 0; oo < 4; ++oo) {
+                        const int o = 4 * half + oo;
+                        const int bt = bt0 + 4 * (o >> 1) + 2 * (o & 1);
+                        const uint32_t byte = bytes[8 * bt + ri];
+                        decode_rowbyte(vals + rs[8 * bt + ri], byte, w + 4 * oo);
+                    }
+                    tmem_st16(tA + (uint32_t)(16 * half), w);
                 }
             } else {
                 // rows of a missing second strip: zeros, so that the MMA
                 // reads defined values (their Y rows are not written)
 #pragma unroll
-                for (int j = 0; j < NR; ++j) *reinterpret_cast<uint4*>(at + dst[j]) = make_uint4(0u, 0u, 0u, 0u);
+                for (int j = 0; j < 16; ++j) w[j] = 0u;
+                tmem_st16(tA, w);
+                tmem_st16(tA + 16u, w);
             }
-            // make the generic-proxy writes of A visible to the tensor cores
-            bspx::fence_proxy_async_smem();
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                bspx::mbar_arrive(a_full + sa);
+                bspx::mbar_arrive(a_full + G);
                 bspx::mbar_arrive(c_empty + sc);
             }
-            if (++sc == (uint32_t)SC) { sc = 0; pc ^= 1u; }
-            if (++sa == (uint32_t)SA) { sa = 0; pa ^= 1u; }
-        }
-    }
-
-    // ---------------- epilogue: warps 4-7, one per TMEM lane quadrant, each
-    // thread one row of the 16 columns; then split-K through the workspace
-    const bool epi = warp >= DEC0 && warp < DEC0 + 4;
-    const int trow = 32 * (warp & 3) + lane;
-    const int64_t m = mt * BM + trow;
-    float v[BN];
-    bool ok = true;
-    if (epi) {
-        ok = __all_sync(FULL, bspx::mbar_wait_sleep(acc_bar, 0, cap, kSleepNs));
-        if (!ok || failed) {
-            failed = true;
-            ok = false;
-        } else {
-            tc_fence_after();
-            uint32_t r[16];
-            tmem_ld16(tmem_base + ((uint32_t)(32 * (warp & 3)) << 16), r);
-#pragma unroll
-            for (int j = 0; j < BN; ++j) v[j] = __uint_as_float(r[j]);
-        }
-    }
-    const bool mine = epi && ok && m < M;
-    if (a.splits == 1) {
-        if (mine)
-#pragma unroll
-            for (int j = 0; j < BN; ++j)
-                if (j < N) a.Y[j * M + m] = __float2half_rn(v[j]);
-    } else {
-        // this split's partial sums: its own slot (deterministic) or an
-        // atomic add; the last CTA of the tile to arrive writes Y
-        float* det = a.ws_det ? a.ws_det + (int64_t)part * N * M : nullptr;
-        if (mine)
-#pragma unroll
-            for (int j = 0; j < BN; ++j)
-                if (j < N) {
-                    if (det) det[j * M + m] = v[j];
-                    else atomicAdd(a.ws + j * M + m, v[j]);
+            if (i + 1 == S || k + 1 == KTA) {
+                // ---------------- epilogue of the segment this step ends:
+                // one row of 16 columns per thread
+                const uint32_t seg = (uint32_t)(t - t0), buf = seg & 1u;
+                if (!__all_sync(FULL, bspx::mbar_wait_sleep(acc_full + buf, (seg >> 1) & 1u, cap, kSleepNs))) {
+                    failed = true;
+                    break;
                 }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) *s_last = atomicAdd(a.counters + strip0, 1u) == (uint32_t)(a.splits - 1);
-        __syncthreads();
-        if (*s_last) {
-            __threadfence();
-            if (epi && m < M)
-                for (int j = 0; j < BN && j < N; ++j) {
-                    float t = 0.f;
-                    if (a.ws_det) {
-                        for (int sp = 0; sp < a.splits; ++sp) t += __ldcg(a.ws_det + ((int64_t)sp * N + j) * M + m);
+                tc_fence_after();
+                uint32_t r[16];
+                tmem_ld16(tmem_base + buf * D_COLS + tq, r);
+                const int64_t m = t * BM + 32 * q + lane;
+                if (m < M) {
+                    const int64_t first = step_owner(t * KTA, T, P);
+                    const int64_t nseg = step_owner((t + 1) * KTA - 1, T, P) - first + 1;
+                    if (nseg == 1) {
+#pragma unroll
+                        for (int j = 0; j < BN; ++j)
+                            if (j < N) a.Y[j * M + m] = __float2half_rn(__uint_as_float(r[j]));
+                    } else if (a.ws_det) {
+                        float4* d = reinterpret_cast<float4*>(a.ws_det + ((cta - first) * M + m) * 16);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                     } else {
-                        t = atomicExch(a.ws + j * M + m, 0.0f);
+                        // columns at or past N are exact zeros (X rows past N read as zeros)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (4 * j < N)
+                                red_add_v4(a.ws + m * 16 + 4 * j, __uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                     }
-                    a.Y[j * M + m] = __float2half_rn(t);
                 }
-            if (threadIdx.x == 0) a.counters[strip0] = 0u;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bspx::mbar_arrive(acc_empty + buf);
+            }
+            sc += NG;
+            if (sc >= SC) { sc -= SC; pc ^= 1u; }
+            k += NG;
+            while (k >= KTA) { k -= KTA; ++t; }
         }
     }
 
+    // the finishing kernel may start launching (it waits for this grid's
+    // completion and memory before it reads the workspace)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (failed && lane == 0) atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == MMAW) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                      : "memory");
+    }
+}
+
+// Finishing kernel: Y of the tiles whose steps are split between CTAs, from
+// the workspace (which it clears) or, deterministically, from the segments'
+// slots added in segment order.  One thread per (row, column < N).
+__global__ void __launch_bounds__(256)
+spmm_narrow_finish_kernel(__half* __restrict__ Y, float* __restrict__ ws, const float* __restrict__ ws_det,
+                          int64_t M, int64_t N, int64_t KT, int64_t T, int64_t P)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t total = M * N;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = e / N, n = e - m * N;
+        const int64_t t = m / BM;
+        const int64_t first = step_owner(t * KT, T, P);
+        const int64_t nseg = step_owner((t + 1) * KT - 1, T, P) - first + 1;
+        if (nseg == 1) continue;  // written by the product kernel
+        float v;
+        if (ws_det) {
+            v = 0.f;
+            for (int64_t sgi = 0; sgi < nseg; ++sgi) v += ws_det[(sgi * M + m) * 16 + n];
+        } else {
+            v = ws[m * 16 + n];
+            ws[m * 16 + n] = 0.f;
+        }
+        Y[n * M + m] = __float2half_rn(v);
     }
 }
 
@@ -574,32 +621,33 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 
 }  // namespace
 
-int bsp_narrow_splits_auto(const bsp_decode_problem& p)
+namespace {
+
+// CTAs of the narrow kernel: every resident slot (MINB per SM), at most one
+// per step; BSP_TUNE_NARROW_CTAS overrides.
+int64_t narrow_ctas_auto(const bsp_decode_problem& p, int64_t T)
 {
-    // the critical path: CTA waves (MINB CTAs per SM) times the GT columns
-    // of a CTA plus a fixed cost per CTA (start, epilogue)
-    const int64_t tiles = (p.Mp + BM - 1) / BM, KT = p.Kp / 64;
-    const int64_t slots = (p.num_sms > 0 ? p.num_sms : 1) * MINB;
-    int64_t best = 1, best_cost = INT64_MAX;
-    for (int64_t sp = 1; sp <= KT && sp <= 64; ++sp) {
-        const int64_t cost = ((tiles * sp + slots - 1) / slots) * ((KT + sp - 1) / sp + BSP_NARROW_CTA_COST);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = sp;
-        }
-    }
-    return (int)best;
+    const int64_t slots = (int64_t)(p.num_sms > 0 ? p.num_sms : 1) * MINB;
+    return std::max<int64_t>(1, std::min(slots, T));
 }
 
-int bsp_narrow_splits(const bsp_decode_problem& p)
+// Largest number of CTAs sharing one tile under the balanced partition.
+int64_t max_segments(int64_t tiles, int64_t KT, int64_t T, int64_t P)
 {
-    const int64_t KT = p.Kp / 64;
-    int64_t best = bsp_narrow_splits_auto(p);
-    if (const int64_t v = bsp_tune(BSP_TUNE_NARROW_SPLITK)) best = v;  // tests, tuning
-    if (best > KT) best = KT;
-    if (best < 1) best = 1;
-    if (p.ws_det && best > p.det_slots) best = p.det_slots;
-    return (int)best;
+    int64_t mx = 1;
+    for (int64_t t = 0; t < tiles; ++t)
+        mx = std::max(mx, step_owner((t + 1) * KT - 1, T, P) - step_owner(t * KT, T, P) + 1);
+    return mx;
+}
+
+bool any_split(int64_t tiles, int64_t KT, int64_t T, int64_t P) { return max_segments(tiles, KT, T, P) > 1; }
+
+}  // namespace
+
+int bsp_narrow_det_slots(const bsp_decode_problem& p)
+{
+    const int64_t tiles = (p.Mp + BM - 1) / BM, KT = p.Kp / 64, T = tiles * KT;
+    return (int)max_segments(tiles, KT, T, narrow_ctas_auto(p, T));
 }
 
 bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
@@ -626,6 +674,13 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
             return cudaFuncSetAttribute(spmm_narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
         }))
         return BSP_ERR_CUDA;
+    const int64_t tiles = (p.Mp + BM - 1) / BM, KT = p.Kp / 64, T = tiles * KT;
+    int64_t P = narrow_ctas_auto(p, T);
+    if (const int64_t v = bsp_tune(BSP_TUNE_NARROW_CTAS)) P = std::min(v, T);  // tests, tuning
+    // deterministic slots: one per CTA sharing a tile; fewer CTAs share less
+    if (p.ws_det)
+        while (P > 1 && max_segments(tiles, KT, T, P) > p.det_slots) --P;
+    if (P < 1 || P > 0x7FFFFFFF) return BSP_ERR_INTERNAL;
     NarrowArgs a = {};
     a.bitmaps = p.bitmaps;
     a.offsets = p.offsets;
@@ -635,24 +690,36 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     a.N = N;
     a.K = p.K;
     a.Mp = p.Mp;
-    a.KT = p.Kp / 64;
-    a.splits = bsp_narrow_splits(p);
-    if (a.splits < 1 || a.splits > a.KT) return BSP_ERR_INTERNAL;  // a split without GT columns
+    a.KT = KT;
+    a.T = T;
+    a.P = P;
     a.ws = (float*)p.ws;
-    a.ws_det = a.splits > 1 ? p.ws_det : nullptr;
-    a.counters = p.counters;
-    a.ngt = (p.Mp / 64) * (p.Kp / 64);
-    a.values_bytes = p.values_bytes;
+    a.ws_det = p.ws_det;
     a.err = p.err;
     a.spin_cap = bsp_spin_cap();
     // C ring: as many stages as fit, each sized for the densest GT
     a.c_slot = c_slot_bytes(std::min<uint32_t>(p.max_gt_nnz, 4096u));
     a.c_stage = c_stage_bytes(a.c_slot);
     a.sc = std::min<int>(SC_MAX, C_BYTES / (int)a.c_stage);
+    if (a.sc < NG) return BSP_ERR_INTERNAL;  // each decoder group needs a stage of its own in flight
     const int smem = OFF_C + a.sc * (int)a.c_stage + 1024;
-    const int64_t tiles = (p.Mp + BM - 1) / BM;
-    const int64_t ctas = tiles * a.splits;
-    if (ctas > 0x7FFFFFFF) return BSP_ERR_INVALID_ARG;
-    spmm_narrow_kernel<<<(unsigned)ctas, THREADS, smem, s>>>(map, a);
-    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    spmm_narrow_kernel<<<(unsigned)P, THREADS, smem, s>>>(map, a);
+    if (cudaGetLastError() != cudaSuccess) return BSP_ERR_CUDA;
+    if (!any_split(tiles, KT, T, P)) return BSP_OK;
+    // the tiles split between CTAs: converted by a programmatic dependent
+    // kernel (launched while the product kernel drains; it waits for it)
+    cudaLaunchConfig_t cfg = {};
+    const int64_t elems = p.M * N;
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>((elems + 255) / 256, (int64_t)p.num_sms * 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, spmm_narrow_finish_kernel, (__half*)Y, (float*)p.ws, (const float*)p.ws_det,
+                              p.M, (int64_t)N, KT, T, P) == cudaSuccess
+               ? BSP_OK
+               : BSP_ERR_CUDA;
 }

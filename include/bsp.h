@@ -159,8 +159,9 @@ bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
  * returns; it is not synchronised with calls other threads make meanwhile.
  *   BSP_TUNE_SPLITK          (BSP_SPLITK)        split-K count of the
  *                            CUDA-core decode kernels; 0 = automatic
- *   BSP_TUNE_NARROW_SPLITK   (BSP_NARROW_SPLITK) split-K count of the
- *                            tcgen05 decode kernel; 0 = automatic
+ *   BSP_TUNE_NARROW_CTAS     (BSP_NARROW_CTAS)   CTAs the tcgen05 decode
+ *                            kernel's steps are balanced over; 0 = automatic
+ *                            (every resident slot)
  *   BSP_TUNE_UNION_SPLITK    (BSP_UNION_SPLITK)  split-K count of the IE-BME
  *                            product; 0 = automatic
  *   BSP_TUNE_NARROW_MIN_N    (BSP_NARROW_MIN_N)  smallest fp16 N <= 16 that
@@ -172,11 +173,12 @@ bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
  *                            prefill kernel; 0 = as many as fit
  * Split counts are clamped to the problem (at most one per GroupTile
  * column).  BSP_ERR_INVALID_ARG for an unknown knob or a value out of range
- * (split counts and stages 0..4096, NARROW_MIN_N 1..1024, KSPLIT -1..1).
+ * (split counts and stages 0..4096, NARROW_CTAS 0..2^20, NARROW_MIN_N
+ * 1..1024, KSPLIT -1..1).
  */
 typedef enum {
     BSP_TUNE_SPLITK = 0,
-    BSP_TUNE_NARROW_SPLITK = 1,
+    BSP_TUNE_NARROW_CTAS = 1,
     BSP_TUNE_UNION_SPLITK = 2,
     BSP_TUNE_NARROW_MIN_N = 3,
     BSP_TUNE_PREFILL_KSPLIT = 4,

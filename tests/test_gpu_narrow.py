@@ -22,7 +22,7 @@ def _narrow(monkeypatch):
     tune("narrow_min_n", "1")
     yield
     tune("narrow_min_n")
-    tune("narrow_splitk")
+    tune("narrow_ctas")
 
 
 def _run(W, X):
@@ -52,7 +52,7 @@ def test_narrow_forced_splits(splits, monkeypatch):
     W = synth.weights_f16(M, K, 0.6, "uniform", 510)
     X = synth.activations_f16(N, K, 511)
     Yref, S = oracle.spmm_f16(W, X)
-    tune("narrow_splitk", str(splits))
+    tune("narrow_ctas", str(splits))
     A = bsp.BitmapMatrix(to_dev_f16(W, DEV))
     Xd = to_dev_f16(X, DEV)
     for _ in range(3):  # the workspace and counters are clean after each call
@@ -61,7 +61,7 @@ def test_narrow_forced_splits(splits, monkeypatch):
 
 
 def test_narrow_small_integers_exact(monkeypatch):
-    tune("narrow_splitk", "3")
+    tune("narrow_ctas", "3")
     W = synth.small_int_f16((256, 256), -8, 8, seed=521, sparsity=0.5)
     X = synth.small_int_f16((9, 256), -8, 8, seed=522)
     Yref, _ = oracle.spmm_f16(W, X)

@@ -34,13 +34,13 @@ def splitk(monkeypatch):
     def set_(v):
         if v is None:
             tune("splitk")
-            tune("narrow_splitk")
+            tune("narrow_ctas")
         else:
             tune("splitk", str(v))
-            tune("narrow_splitk", str(v))
+            tune("narrow_ctas", str(v))
     yield set_
     tune("splitk")
-    tune("narrow_splitk")
+    tune("narrow_ctas")
 
 
 @pytest.fixture(params=["cuda_cores", "tcgen05_narrow"])

@@ -25,13 +25,13 @@ def splitk(monkeypatch):
     def set_(s):
         if s is None:
             tune("splitk")
-            tune("narrow_splitk")
+            tune("narrow_ctas")
         else:
             tune("splitk", str(s))
-            tune("narrow_splitk", str(s))
+            tune("narrow_ctas", str(s))
     yield set_
     tune("splitk")
-    tune("narrow_splitk")
+    tune("narrow_ctas")
 
 
 def _encode(W):
