@@ -31,7 +31,12 @@
 // the workspace (vector reductions, fire and forget), or store them to
 // per-segment slots in deterministic mode, and a small second kernel,
 // launched as a programmatic dependent of the first, converts those tiles
-// to fp16 (and clears the workspace).  Warps:
+// to fp16 (and clears the workspace).  The product kernel is itself
+// launched as a programmatic dependent of whatever precedes it on the
+// stream: its prologue (tensor memory, barriers, the encoded weight's
+// copies, which no kernel writes after encoding) overlaps the tail of the
+// previous kernel, and it waits for that kernel only before it reads X or
+// writes Y or the workspace.  Warps:
 //   0       C producer: bitmaps + value spans of the step's two GTs (bulk
 //           copies) into the C ring (the rest of shared memory, stages
 //           sized for the densest GT)
@@ -205,6 +210,10 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
                      bspx::smem_u32(bar))
                  : "memory");
 }
+
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; returns at once otherwise.
+__device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -389,6 +398,8 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             bspx::mbar_wait_bounded(c_full + (j % SC), (j / SC) & 1u, cap);
     } else if (warp == BPROD) {
         // ---------------- B producer: one 16 x 64 X tile per step by TMA
+        // (X may be written by the previous kernel on the stream)
+        wait_prior_grids();
         uint32_t s = 0, ph = 0;
         uint32_t k = kk0;
         uint32_t i = 0;
@@ -527,6 +538,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                     break;
                 }
                 tc_fence_after();
+                wait_prior_grids();  // Y and the workspace: the previous kernel is done with them
                 uint32_t r[16];
                 tmem_ld16(tmem_base + buf * D_COLS + tq, r);
                 const int64_t m = t * BM + 32 * q + lane;
@@ -566,7 +578,10 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     // the finishing kernel may start launching (it waits for this grid's
     // completion and memory before it reads the workspace)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (failed && lane == 0) atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
+    if (failed && lane == 0) {
+        wait_prior_grids();
+        atomicExch(a.err, (int)BSP_ERR_TIMEOUT);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == MMAW) {
@@ -584,6 +599,9 @@ __global__ void __launch_bounds__(256)
 spmm_narrow_finish_kernel(__half* __restrict__ Y, float* __restrict__ ws, const float* __restrict__ ws_det,
                           int64_t M, int64_t N, int64_t KT, int64_t T, int64_t P)
 {
+    // the next product kernel may start its prologue now (it waits for this
+    // grid before it touches Y or the workspace)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = M * N;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
@@ -703,8 +721,19 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     a.sc = std::min<int>(SC_MAX, C_BYTES / (int)a.c_stage);
     if (a.sc < NG) return BSP_ERR_INTERNAL;  // each decoder group needs a stage of its own in flight
     const int smem = OFF_C + a.sc * (int)a.c_stage + 1024;
-    spmm_narrow_kernel<<<(unsigned)P, THREADS, smem, s>>>(map, a);
-    if (cudaGetLastError() != cudaSuccess) return BSP_ERR_CUDA;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)P);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, spmm_narrow_kernel, map, a) != cudaSuccess) return BSP_ERR_CUDA;
+    }
     if (!any_split(tiles, KT, T, P)) return BSP_OK;
     // the tiles split between CTAs: converted by a programmatic dependent
     // kernel (launched while the product kernel drains; it waits for it)
@@ -713,9 +742,6 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     cfg.gridDim = dim3((unsigned)std::min<int64_t>((elems + 255) / 256, (int64_t)p.num_sms * 8));
     cfg.blockDim = dim3(256);
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, spmm_narrow_finish_kernel, (__half*)Y, (float*)p.ws, (const float*)p.ws_det,
