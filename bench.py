@@ -47,11 +47,12 @@ INT8_LAYERS = [("int8_11008x4096", 11008, 4096), ("int8_4096x11008", 4096, 11008
 INT8_SPARSITY = (0.5, 0.6)
 INT8_NS = (1, 8, 16)
 # kernels of the decode step and their sources (with the dispatch): fp16
-# N <= 2 and spMspV on the GT-per-warp kernel, N = 3, 4 on the team kernel,
-# N >= 5 on the narrow tcgen05 kernel
+# N <= 2 and spMspV on the GT-per-warp kernel, N >= 3 on the narrow tcgen05
+# kernel (its finishing kernel, which converts the tiles split between
+# CTAs, is part of the same call)
 STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_narrow_kernel (N=8, 16)"
-STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu")
-NARROW_MIN_N_DEFAULT = 5  # BSP_NARROW_MIN_N_DEFAULT of bsp_api.cu (a CPU test holds them equal)
+STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu", "bsp_tuning.cu")
+NARROW_MIN_N_DEFAULT = 3  # BSP_NARROW_MIN_N_DEFAULT of bsp_tuning.cu (a CPU test holds them equal)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
 

@@ -17,9 +17,11 @@
 
 // Smallest fp16 N (up to BSP_DECODE_MAX_N) that runs the tcgen05 narrow
 // kernel instead of the CUDA-core decode kernels, chosen from measurements
-// on the OPT-13B projections (the crossover of the two kernels' GB/s).
+// on the OPT-13B projections: at N = 1 and 2 the GT-per-warp CUDA-core
+// kernel is as fast or faster (QKV 29 / 33 us against 33 / 33 us); from
+// N = 3 the narrow kernel is (2.6 TB/s against 1.7 for the team kernel).
 #ifndef BSP_NARROW_MIN_N_DEFAULT
-#define BSP_NARROW_MIN_N_DEFAULT 5
+#define BSP_NARROW_MIN_N_DEFAULT 3
 #endif
 
 namespace {

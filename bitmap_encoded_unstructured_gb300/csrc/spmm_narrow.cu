@@ -91,6 +91,16 @@ constexpr int CPROD = 0, MMAW = 1, BPROD = 2, DEC0 = 3;
 constexpr int WARPS = DEC0 + DEC_WARPS;
 constexpr int THREADS = WARPS * 32;
 constexpr uint32_t kSleepNs = 1000;        // suspend hint of the waiting polls
+// longest sleep between the polls of a waiting producer, MMA issuer, decoder
+#ifndef BSP_NARROW_SLEEP_PROD
+#define BSP_NARROW_SLEEP_PROD 256
+#endif
+#ifndef BSP_NARROW_SLEEP_MMA
+#define BSP_NARROW_SLEEP_MMA 64
+#endif
+#ifndef BSP_NARROW_SLEEP_DEC
+#define BSP_NARROW_SLEEP_DEC 256
+#endif
 
 constexpr int SB = 8;                      // X tile stages
 constexpr int SC_MAX = 16;                 // barrier slots of the C ring
@@ -211,6 +221,28 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
                  : "memory");
 }
 
+// Bounded wait for phase `parity` of `bar` (at most `cap` polls).  Between
+// polls a waiting thread sleeps, starting at 32 ns and doubling up to
+// `max_ns`, so warps that wait (for data, for the MMAs, for a free stage)
+// leave the issue slots to the decoders.
+#ifndef BSP_NARROW_WAIT
+#define BSP_NARROW_WAIT 1
+#endif
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint32_t cap, uint32_t max_ns)
+{
+#if BSP_NARROW_WAIT == 0
+    return bspx::mbar_wait_sleep(bar, parity, cap, kSleepNs);
+#else
+    uint32_t ns = 32;
+    for (uint32_t i = 0; i < cap; ++i) {
+        if (bspx::mbar_try_wait(bar, parity)) return true;
+        __nanosleep(ns);
+        if (ns < max_ns) ns <<= 1;
+    }
+    return false;
+#endif
+}
+
 // Wait until the grids this one depends on (programmatic dependent launch)
 // have completed and their memory is visible; returns at once otherwise.
 __device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -240,17 +272,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 16 consecutive TMEM columns of this thread's lane from registers (32x32b
-// shape, x16).  Whole warps only.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r)
+// 4 consecutive TMEM columns of this thread's lane from registers (32x32b
+// shape, x4): one decoded row-byte.  Whole warps only (the callers run
+// converged: the decode has no divergent branch).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r)
 {
-    __syncwarp();
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
 }
 
 // The eight positions of one BT row-byte as four words of two fp16 each
@@ -352,7 +381,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         uint32_t s = 0, ph = 0;  // stage and its phase parity
         uint32_t i = 0;          // steps issued
         for (; i < S; ++i) {
-            if (i >= SC && !__all_sync(FULL, bspx::mbar_wait_sleep(c_empty + s, ph ^ 1u, cap, kSleepNs))) {
+            if (i >= SC && !__all_sync(FULL, wait_bar(c_empty + s, ph ^ 1u, cap, BSP_NARROW_SLEEP_PROD))) {
                 failed = true;
                 break;
             }
@@ -405,7 +434,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         uint32_t i = 0;
         for (; i < S; ++i) {
             if (i >= (uint32_t)SB &&
-                !__all_sync(FULL, bspx::mbar_wait_sleep(b_empty + s, ph ^ 1u, cap, kSleepNs))) {
+                !__all_sync(FULL, wait_bar(b_empty + s, ph ^ 1u, cap, BSP_NARROW_SLEEP_PROD))) {
                 failed = true;
                 break;
             }
@@ -429,9 +458,9 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             const uint32_t g = i % NG;
             const bool first = i == 0 || k == 0, last = i + 1 == S || k + 1 == KTA;
             const uint32_t buf = seg & 1u;
-            bool ok = bspx::mbar_wait_sleep(a_full + g, (i / NG) & 1u, cap, kSleepNs);
-            ok = ok && bspx::mbar_wait_sleep(b_full + sb, pb, cap, kSleepNs);
-            if (first && seg >= 2) ok = ok && bspx::mbar_wait_sleep(acc_empty + buf, ((seg - 2) >> 1) & 1u, cap, kSleepNs);
+            bool ok = wait_bar(a_full + g, (i / NG) & 1u, cap, BSP_NARROW_SLEEP_MMA);
+            ok = ok && wait_bar(b_full + sb, pb, cap, BSP_NARROW_SLEEP_MMA);
+            if (first && seg >= 2) ok = ok && wait_bar(acc_empty + buf, ((seg - 2) >> 1) & 1u, cap, BSP_NARROW_SLEEP_MMA);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
             if (lane == 0) {
@@ -472,19 +501,20 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         const int ri = lane & 7;
         const int bt0 = 16 * (lane >> 4) + ((lane >> 3) & 1);  // the lane's BT of octet 0 (half-local)
         // step i = G, G + NG, ...: its tile, GT column, C stage and parity
-        int64_t t = t0;
+        const uint32_t Mp32 = (uint32_t)a.Mp;
+        uint32_t t = (uint32_t)t0;
         uint32_t k = kk0 + G;
         while (k >= KTA) { k -= KTA; ++t; }
         uint32_t sc = G, pc = 0;
         uint32_t it = 0;
         for (uint32_t i = G; i < S; i += NG, ++it) {
-            bool ok = bspx::mbar_wait_sleep(c_full + sc, pc, cap, kSleepNs);
+            bool ok = wait_bar(c_full + sc, pc, cap, BSP_NARROW_SLEEP_DEC);
             // the MMAs of this group's previous step read A stage G: done
-            if (it > 0) ok = ok && bspx::mbar_wait_sleep(a_empty + G, (it - 1) & 1u, cap, kSleepNs);
+            if (it > 0) ok = ok && wait_bar(a_empty + G, (it - 1) & 1u, cap, BSP_NARROW_SLEEP_DEC);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
-            const bool active = gsel == 0 || (2 * t + 1) * 64 < a.Mp;  // a missing second strip: zeros
-            uint32_t w[16];
+            const bool active = gsel == 0 || (2 * t + 1) * 64 < Mp32;  // a missing second strip: zeros
+            __syncwarp();
             if (active) {
                 const uint8_t* slot = c_stage(sc) + gsel * SLOT;
                 // BT value bases: lane l owns BT 32 h + l (GT order = value order)
@@ -504,23 +534,19 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 const uint8_t* bytes = slot + 256 * h;  // byte 8 bt + r: row r of the half's BT bt
                 const uint16_t* vals = reinterpret_cast<const uint16_t*>(slot + 512);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int oo = 0; oo < 4; ++oo) {
-                        const int o = 4 * half + oo;
-                        const int bt = bt0 + 4 * (o >> 1) + 2 * (o & 1);
-                        const uint32_t byte = bytes[8 * bt + ri];
-                        decode_rowbyte(vals + rs[8 * bt + ri], byte, w + 4 * oo);
-                    }
-                    tmem_st16(tA + (uint32_t)(16 * half), w);
+                for (int o = 0; o < 8; ++o) {
+                    const int bt = bt0 + 4 * (o >> 1) + 2 * (o & 1);
+                    const uint32_t byte = bytes[8 * bt + ri];
+                    uint32_t w[4];
+                    decode_rowbyte(vals + rs[8 * bt + ri], byte, w);
+                    tmem_st4(tA + (uint32_t)(4 * o), w);  // octet o: columns 4 o .. 4 o + 3
                 }
             } else {
                 // rows of a missing second strip: zeros, so that the MMA
                 // reads defined values (their Y rows are not written)
+                const uint32_t z[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = 0u;
-                tmem_st16(tA, w);
-                tmem_st16(tA + 16u, w);
+                for (int o = 0; o < 8; ++o) tmem_st4(tA + (uint32_t)(4 * o), z);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
@@ -532,8 +558,8 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             if (i + 1 == S || k + 1 == KTA) {
                 // ---------------- epilogue of the segment this step ends:
                 // one row of 16 columns per thread
-                const uint32_t seg = (uint32_t)(t - t0), buf = seg & 1u;
-                if (!__all_sync(FULL, bspx::mbar_wait_sleep(acc_full + buf, (seg >> 1) & 1u, cap, kSleepNs))) {
+                const uint32_t seg = t - (uint32_t)t0, buf = seg & 1u;
+                if (!__all_sync(FULL, wait_bar(acc_full + buf, (seg >> 1) & 1u, cap, BSP_NARROW_SLEEP_DEC))) {
                     failed = true;
                     break;
                 }
@@ -541,10 +567,10 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 wait_prior_grids();  // Y and the workspace: the previous kernel is done with them
                 uint32_t r[16];
                 tmem_ld16(tmem_base + buf * D_COLS + tq, r);
-                const int64_t m = t * BM + 32 * q + lane;
+                const int64_t m = (int64_t)t * BM + 32 * q + lane;
                 if (m < M) {
-                    const int64_t first = step_owner(t * KTA, T, P);
-                    const int64_t nseg = step_owner((t + 1) * KTA - 1, T, P) - first + 1;
+                    const int64_t first = step_owner((int64_t)t * KTA, T, P);
+                    const int64_t nseg = step_owner(((int64_t)t + 1) * KTA - 1, T, P) - first + 1;
                     if (nseg == 1) {
 #pragma unroll
                         for (int j = 0; j < BN; ++j)

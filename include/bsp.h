@@ -166,7 +166,7 @@ bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
  *                            product; 0 = automatic
  *   BSP_TUNE_NARROW_MIN_N    (BSP_NARROW_MIN_N)  smallest fp16 N <= 16 that
  *                            runs the tcgen05 decode kernel; larger than 16:
- *                            never; default 5
+ *                            never; default 3
  *   BSP_TUNE_PREFILL_KSPLIT  (BSP_PF_KSPLIT)     prefill split-K over a CTA
  *                            pair: -1 automatic, 0 off, 1 on (N <= 256)
  *   BSP_TUNE_PREFILL_CSTAGES (BSP_PF_SC)         compressed-ring depth of the

@@ -57,8 +57,8 @@ def test_decode_step_bytes_count_weight_x_and_y():
 def test_step_kernel_follows_the_dispatch(monkeypatch):
     monkeypatch.delenv("BSP_NARROW_MIN_N", raising=False)
     got = {N: bench.step_kernel(("qkv", N)) for N in (1, 2, 3, 4, 5, 8, 16)}
-    assert got == {1: "spmm_decode_gtw_kernel", 2: "spmm_decode_gtw_kernel", 3: "spmm_decode_kernel",
-                   4: "spmm_decode_kernel", 5: "spmm_narrow_kernel", 8: "spmm_narrow_kernel",
+    assert got == {1: "spmm_decode_gtw_kernel", 2: "spmm_decode_gtw_kernel", 3: "spmm_narrow_kernel",
+                   4: "spmm_narrow_kernel", 5: "spmm_narrow_kernel", 8: "spmm_narrow_kernel",
                    16: "spmm_narrow_kernel"}
     assert bench.step_kernel(("fc2", "spmspv")) == "spmm_decode_gtw_kernel"
     monkeypatch.setenv("BSP_NARROW_MIN_N", "17")
