@@ -60,6 +60,9 @@ SIGNATURES = {
     "bsp_spmm_noalloc": (C.c_int, [_P, _P, _P, C.c_int, _I64, _I64, _P, _I64, _P, _P]),
     "bsp_set_deterministic": (C.c_int, [_P, C.c_int]),
     "bsp_set_tuning": (C.c_int, [C.c_int, _I64]),
+    "bsp_build_column_index": (C.c_int, [_P, _P]),
+    "bsp_column_index_bytes": (C.c_int, [_P, C.POINTER(C.c_uint64)]),
+    "bsp_column_index_export": (C.c_int, [_P, _P, _P, _P, _P, _P]),
     "bsp_get_tuning": (C.c_int, [C.c_int, C.POINTER(_I64)]),
     "bsp_union_encode": (C.c_int, [_P, C.c_int, _I64, _I64, _P, C.POINTER(_P)]),
     "bsp_union_destroy": (C.c_int, [_P]),
@@ -441,6 +444,33 @@ class BitmapMatrix:
     def check(self, stream=None):
         """Synchronise and raise if a kernel on this handle gave up a wait."""
         bsp_check(self.h, _stream(stream))
+
+    # -- Tiled-CBC column index (column-skipping spMspV)
+    def build_column_index(self, stream=None):
+        _check("bsp_build_column_index", lib().bsp_build_column_index(self.h, _stream(stream)))
+
+    def column_index_bytes(self) -> int:
+        v = C.c_uint64()
+        _check("bsp_column_index_bytes", lib().bsp_column_index_bytes(self.h, C.byref(v)))
+        return v.value
+
+    def column_index_arrays(self, stream=None):
+        """Copies of (TileOffset int32 [NGT+1], ColInfo int32 [NGT*64], bitmaps
+        int64 [NGT*64*4], values [NNZ]) of the column index."""
+        import torch
+        tr = -(-self.M // 256)
+        tc = -(-self.K // 64)
+        ngt = tr * tc
+        dev = self.device
+        off = torch.empty(ngt + 1, dtype=torch.int32, device=dev)
+        ci = torch.empty(ngt * 64, dtype=torch.int32, device=dev)
+        bm = torch.empty(ngt * 64 * 4, dtype=torch.int64, device=dev)
+        nnz = self.nnz
+        vals = torch.empty(nnz, dtype=self.torch_dtype, device=dev)
+        _check("bsp_column_index_export", lib().bsp_column_index_export(
+            self.h, off.data_ptr(), ci.data_ptr(), bm.data_ptr(), vals.data_ptr() if nnz else None,
+            _stream(stream)))
+        return off, ci, bm, vals
 
     def set_deterministic(self, on: bool = True):
         """Split-K partial sums added in a fixed order (bit-identical fp16

@@ -40,6 +40,10 @@ void free_handle(bsp_handle* h)
     cudaFree(h->err);
     cudaFree(h->stage_x);
     cudaFree(h->stage_y);
+    cudaFree(h->cbc_offsets);
+    cudaFree(h->cbc_colinfo);
+    cudaFree(h->cbc_bitmaps);
+    cudaFree(h->cbc_values);
     h->magic = 0;
     delete h;
 }
@@ -196,6 +200,7 @@ bsp_status_t bsp_spmspv(bsp_handle_t h, const void* x, void* y, bsp_stream_t str
     if (!aligned16(x) || !aligned16(y)) return BSP_ERR_ALIGN;
     DeviceGuard g(h->device);
     if (!g.ok) return BSP_ERR_CUDA;
+    if (h->cbc_values) return bsp_run_spmspv_cbc(h, x, y, 0.0f, (cudaStream_t)stream);
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     return bsp_run_spmm_decode(bsp_problem_of(h), x, 1, y, mode, nullptr, true, (cudaStream_t)stream);
 }
@@ -206,8 +211,48 @@ bsp_status_t bsp_spmspv_threshold(bsp_handle_t h, const void* x, float threshold
     if (!aligned16(x) || !aligned16(y)) return BSP_ERR_ALIGN;
     DeviceGuard g(h->device);
     if (!g.ok) return BSP_ERR_CUDA;
+    if (h->cbc_values) return bsp_run_spmspv_cbc(h, x, y, threshold, (cudaStream_t)stream);
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     return bsp_run_spmm_decode(bsp_problem_of(h), x, 1, y, mode, nullptr, true, (cudaStream_t)stream, threshold);
+}
+
+bsp_status_t bsp_build_column_index(bsp_handle_t h, bsp_stream_t stream)
+{
+    if (!valid(h)) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    return bsp_run_build_cbc(h, (cudaStream_t)stream);
+}
+
+bsp_status_t bsp_column_index_bytes(bsp_handle_t h, uint64_t* bytes)
+{
+    if (!valid(h) || !bytes) return BSP_ERR_INVALID_ARG;
+    if (!h->cbc_values) return BSP_ERR_INVALID_ARG;
+    const uint64_t ngt = (uint64_t)(h->cbc_tr * h->cbc_tc);
+    const uint64_t nbm = ngt * 256 * 64 / 64;
+    *bytes = 4ull * (ngt + 1) + 4ull * ngt * 64 + 8ull * nbm + (uint64_t)bsp_elem_bytes(h->dtype) * h->NNZ;
+    return BSP_OK;
+}
+
+bsp_status_t bsp_column_index_export(bsp_handle_t h, uint32_t* offsets, uint32_t* colinfo, uint64_t* bitmaps,
+                                     void* values, bsp_stream_t stream)
+{
+    if (!valid(h) || !h->cbc_values) return BSP_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return BSP_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t ngt = (size_t)(h->cbc_tr * h->cbc_tc);
+    if (offsets && cudaMemcpyAsync(offsets, h->cbc_offsets, (ngt + 1) * 4, cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (colinfo && cudaMemcpyAsync(colinfo, h->cbc_colinfo, ngt * 64 * 4, cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (bitmaps && cudaMemcpyAsync(bitmaps, h->cbc_bitmaps, ngt * 64 * 4 * 8, cudaMemcpyDefault, s) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (values && h->NNZ &&
+        cudaMemcpyAsync(values, h->cbc_values, (size_t)h->NNZ * bsp_elem_bytes(h->dtype), cudaMemcpyDefault, s) !=
+            cudaSuccess)
+        return BSP_ERR_CUDA;
+    return BSP_OK;
 }
 
 bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,

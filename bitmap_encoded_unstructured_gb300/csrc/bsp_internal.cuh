@@ -38,6 +38,14 @@ struct bsp_handle {
     // BSP_ERR_TIMEOUT here; bsp_check reads and clears it
     int* err;
     int num_sms;
+    // Tiled-CBC column index (bsp_build_column_index), or null: GTiles of
+    // 256 x 64, TileOffset u32 [NGT + 1], ColInfo u32 [NGT * 64], bitmaps
+    // u64 [NGT * 64 * 4], values [NNZ] (+16 B slack); cbc_tr x cbc_tc GTiles
+    uint32_t* cbc_offsets;
+    uint32_t* cbc_colinfo;
+    uint64_t* cbc_bitmaps;
+    void* cbc_values;
+    int64_t cbc_tr, cbc_tc;
     // staging for bsp_spmm_host, grown on demand
     void* stage_x;
     size_t stage_x_bytes;
@@ -124,6 +132,13 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
 // Slots the deterministic mode needs for the automatic CTA count: the
 // largest number of CTAs that share one tile.
 int bsp_narrow_det_slots(const bsp_decode_problem& p);
+
+// ---- Tiled-CBC column index and its spMspV (tiled_cbc.cu) ----
+// Build the index from the handle's arrays (allocates; synchronises s).
+bsp_status_t bsp_run_build_cbc(bsp_handle* h, cudaStream_t s);
+// y = W x' over the index, columns with |x| <= tau skipped (tau = 0: exact
+// zeros); fp16 -> fp16 y, int8 -> int32 y.
+bsp_status_t bsp_run_spmspv_cbc(const bsp_handle* h, const void* x, void* y, float tau, cudaStream_t s);
 
 // ---- process-wide tuning (bsp_tuning.cu) ----
 // Tuning knobs of the dispatch, read once per process from the environment

@@ -224,6 +224,37 @@ bsp_status_t bsp_spmspv_threshold(bsp_handle_t h, const void *x, float threshold
                                   void *y, bsp_stream_t stream);
 
 /*
+ * Tiled-CBC column index ("Unified Static-Dynamic Pruning for Efficient LLM
+ * Inference", section 4.1, "Tiled-CBC: Unified Compression Format"): a
+ * column-major copy of the encoded weight that lets bsp_spmspv and
+ * bsp_spmspv_threshold fetch only the columns whose activation survives
+ * (section 4.2, step (3)).  GTiles of 256 x 64 elements tile W row-major (M
+ * and K zero-padded to multiples of 256 and 64); each 256 x 1 column tile
+ * has four uint64 bitmaps (rows 0-63, 64-127, 128-191, 192-255; bit r % 64
+ * of word r / 64 <=> element r is nonzero); the GTile's nonzeros follow in
+ * column order, top to bottom.  Arrays: TileOffset u32 [NGT + 1] (values
+ * before each GTile), ColInfo u32 [NGT * 64] (column's first value inside
+ * its GTile << 16 | its nonzero count), bitmaps u64 [NGT * 64 * 4], values
+ * [NNZ].  Storage, the page's closed form with TILE_K = 64:
+ *   4 (NGT + 1) + 4 NGT 64 + 8 NBM + B_v NNZ,  NBM = (M, K padded) / 64.
+ *
+ * bsp_build_column_index builds it on the handle's device from the handle's
+ * arrays (allocates the index and a dense scratch copy of W, synchronises
+ * `stream`); from then on the handle's spMspV calls use it (and allocate
+ * nothing).  Building again replaces it.  BSP_ERR_OOM if it does not fit.
+ */
+bsp_status_t bsp_build_column_index(bsp_handle_t h, bsp_stream_t stream);
+
+/* Bytes of the column index (the closed form above); BSP_ERR_INVALID_ARG
+ * when the handle has none. */
+bsp_status_t bsp_column_index_bytes(bsp_handle_t h, uint64_t *bytes);
+
+/* Copies of the index arrays (device or host memory, any pointer may be
+ * NULL), ordered on `stream`; BSP_ERR_INVALID_ARG without an index. */
+bsp_status_t bsp_column_index_export(bsp_handle_t h, uint32_t *offsets, uint32_t *colinfo,
+                                     uint64_t *bitmaps, void *values, bsp_stream_t stream);
+
+/*
  * Same product as bsp_spmm, from and to HOST memory: copies X in, runs the
  * product and copies Y out on `stream`, then synchronises `stream`.  Uses a
  * device staging buffer owned by the handle (grown on demand, so this call
