@@ -4,14 +4,14 @@ Workload: the four projections of an OPT-13B decoder layer (QKV 15360x5120,
 out 5120x5120, FC1 20480x5120, FC2 5120x20480), fp16, 50% magnitude-style
 unstructured mask, synthetic N(0, 0.02) weights (no checkpoints needed).
 One step = bsp_spmm on every layer at N = 1, 2, 8, 16, plus bsp_spmspv on
-FC2 with a post-ReLU activation (~85% zeros): 17 launches of the decode
-kernels.  The step's working set (354 MB of encoded weights) is larger than
+FC2 with a post-ReLU activation (~85% zeros) over FC2's Tiled-CBC column
+index: 17 calls of the decode kernels.  The step's working set (354 MB of encoded weights) is larger than
 L2 (129 MB), and each layer is re-read only after the three others have
 passed through L2.
 
 GB/s counts algorithmic bytes: the encoded weight (Stor) + X + Y for each
-spmm, and bitmaps + offsets + the values of active K-octets + x + y for the
-spMspV.
+spmm; for the spMspV the column index's TileOffset and ColInfo rows, the
+bitmaps and values of the active columns, x and y.
 
 ``--impl reference`` times the CPU oracle instead, on a bounded row sample
 of the same workload, and prints the same metric.
@@ -47,11 +47,12 @@ INT8_LAYERS = [("int8_11008x4096", 11008, 4096), ("int8_4096x11008", 4096, 11008
 INT8_SPARSITY = (0.5, 0.6)
 INT8_NS = (1, 8, 16)
 # kernels of the decode step and their sources (with the dispatch): fp16
-# N <= 2 and spMspV on the GT-per-warp kernel, N >= 3 on the narrow tcgen05
-# kernel (its finishing kernel, which converts the tiles split between
-# CTAs, is part of the same call)
-STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2, spMspV) + spmm_narrow_kernel (N=8, 16)"
-STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "bsp_api.cu", "bsp_tuning.cu")
+# N <= 2 on the GT-per-warp kernel, N >= 3 on the narrow tcgen05 kernel, the
+# spMspV on the column-skipping kernel over the Tiled-CBC index (a narrow or
+# spMspV call's finishing kernel, which converts split partial sums, is part
+# of the same call)
+STEP_KERNELS = "spmm_decode_gtw_kernel (N<=2) + spmm_narrow_kernel (N=8, 16) + spmspv_cbc_kernel (spMspV)"
+STEP_SOURCES = ("spmm_decode.cu", "spmm_narrow.cu", "tiled_cbc.cu", "bsp_api.cu", "bsp_tuning.cu")
 NARROW_MIN_N_DEFAULT = 3  # BSP_NARROW_MIN_N_DEFAULT of bsp_tuning.cu (a CPU test holds them equal)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
@@ -61,7 +62,9 @@ def step_kernel(key):
     """The kernel a call of the step launches, by the library's fp16
     dispatch (BSP_NARROW_MIN_N, else the library's default)."""
     _, N = key
-    if N == "spmspv" or N <= 2:
+    if N == "spmspv":
+        return "spmspv_cbc_kernel"
+    if N <= 2:
         return "spmm_decode_gtw_kernel"
     min_n = int(os.environ.get("BSP_NARROW_MIN_N", str(NARROW_MIN_N_DEFAULT)))
     return "spmm_narrow_kernel" if N >= min_n else "spmm_decode_kernel"
@@ -131,6 +134,24 @@ def make_workload(only=None):
     return Ws, xs, relu
 
 
+def cbc_spmspv_bytes(W, x):
+    """Algorithmic bytes of the column-skipping spMspV over the Tiled-CBC
+    index (256 x 64 GTiles): the TileOffset and the whole ColInfo row of
+    every GTile with an active column, the four bitmap words (32 B) and the
+    values of every active column tile, x and y."""
+    M, K = W.shape
+    tr, tc = -(-M // 256), -(-K // 64)
+    act = np.zeros(tc * 64, dtype=bool)
+    act[:K] = (x.view(np.uint16) & 0x7FFF) != 0
+    nz = np.zeros((tr * 256, tc * 64), dtype=bool)
+    nz[:M, :K] = W.view(np.uint16) != 0
+    col_nnz = nz.reshape(tr, 256, tc * 64).sum(axis=1)           # [tr][columns]
+    act_tiles = act.reshape(tc, 64).any(axis=1)                  # GTile columns with an active column
+    n_gt = tr * int(act_tiles.sum())
+    vals = int(col_nnz[:, act].sum())
+    return 4 * (n_gt + 1) + 4 * 64 * n_gt + 32 * tr * int(act.sum()) + 2 * vals + 2 * K + 2 * M
+
+
 def algorithmic_bytes(Ws, relu):
     """Per-call algorithmic bytes for each (layer, N) and for the spMspV."""
     out = {}
@@ -147,10 +168,9 @@ def algorithmic_bytes(Ws, relu):
     if name not in Ws:
         return out, stor, 0.0
     W = Ws[name]
-    act = (relu.reshape(-1, 8).view(np.float16) != 0).any(axis=1)  # active K-octets
-    nnz_active = int(np.count_nonzero(W.reshape(M, -1, 8)[:, act, :]))
-    ngt, nbt = (M // 64) * (K // 64), M * K // 64
-    out[("fc2", "spmspv")] = 4 * (ngt + 1) + 8 * nbt + 2 * nnz_active + 2 * K + 2 * M
+    # the spMspV runs over the FC2 handle's Tiled-CBC column index
+    out[("fc2", "spmspv")] = cbc_spmspv_bytes(W, relu)
+    act = (relu.view(np.uint16) & 0x7FFF) != 0
     return out, stor, float(act.mean())
 
 
@@ -382,6 +402,7 @@ def run_case(args):
     if N == 0:
         x = torch.from_numpy(relu.view(np.float16)).to(dev) if name == "fc2" else \
             torch.from_numpy(xs[name][0].view(np.float16).copy()).to(dev)
+        A.build_column_index()
         y = torch.empty(M, dtype=torch.float16, device=dev)
         fn = lambda: A.spmspv(x, out=y)
     else:
@@ -427,6 +448,7 @@ def run_gpu(args):
         assert mats[name].storage_bytes() == stor[name]
         Xd[name] = torch.from_numpy(xs[name].view(np.float16)).to(dev)
         Yd[name] = torch.empty((16, M), dtype=torch.float16, device=dev)
+    mats["fc2"].build_column_index()  # the step's spMspV skips inactive columns
     xr = torch.from_numpy(relu.view(np.float16)).to(dev)
     yr = torch.empty(LAYERS[3][1], dtype=torch.float16, device=dev)
     Xn = {(name, N): Xd[name][:N].contiguous() for name, _, _ in LAYERS for N in NS}
@@ -503,7 +525,8 @@ def run_gpu(args):
             "us_per_layer": {n: round(statistics.median(per_call[(n, N)]) * 1e3, 2) for n, _, _ in LAYERS}}
     t_sp = statistics.median(per_call[("fc2", "spmspv")])
     breakdown["spmspv_fc2"] = {"GBps": round(bpc[("fc2", "spmspv")] / (t_sp * 1e-3) / 1e9, 1),
-                               "us": round(t_sp * 1e3, 2), "active_octets": round(act_frac, 4),
+                               "us": round(t_sp * 1e3, 2), "active_columns": round(act_frac, 4),
+                               "column_index_bytes": mats["fc2"].column_index_bytes(),
                                "speedup_vs_spmm_n1": round(statistics.median(per_call[("fc2", 1)]) / t_sp, 3)}
 
     traffic = None

@@ -60,7 +60,7 @@ def test_step_kernel_follows_the_dispatch(monkeypatch):
     assert got == {1: "spmm_decode_gtw_kernel", 2: "spmm_decode_gtw_kernel", 3: "spmm_narrow_kernel",
                    4: "spmm_narrow_kernel", 5: "spmm_narrow_kernel", 8: "spmm_narrow_kernel",
                    16: "spmm_narrow_kernel"}
-    assert bench.step_kernel(("fc2", "spmspv")) == "spmm_decode_gtw_kernel"
+    assert bench.step_kernel(("fc2", "spmspv")) == "spmspv_cbc_kernel"
     monkeypatch.setenv("BSP_NARROW_MIN_N", "17")
     assert bench.step_kernel(("qkv", 16)) == "spmm_decode_kernel"
 
@@ -72,3 +72,18 @@ def test_step_kernel_default_is_the_librarys():
     src = open(os.path.join(ROOT, "bitmap_encoded_unstructured_gb300", "csrc", "bsp_tuning.cu")).read()
     m = re.search(r"#define\s+BSP_NARROW_MIN_N_DEFAULT\s+(\d+)", src)
     assert m and int(m.group(1)) == bench.NARROW_MIN_N_DEFAULT
+
+
+def test_spmspv_bytes_follow_the_oracle_fetch_accounting():
+    """The bench's algorithmic bytes of the column-skipping spMspV are the
+    oracle's fetched index bytes (ColInfo of every GTile, bitmaps and values
+    of the active columns; here every GTile has an active column) plus the
+    TileOffset, x and y."""
+    from oracle import tiled_cbc
+    M, K = 512, 1024
+    W = synth.weights_f16(M, K, 0.5, "uniform", 21)
+    x = synth.activations_relu_f16(K, 22)
+    e = tiled_cbc.encode(W)
+    act = (x & 0x7FFF) != 0
+    expect = 4 * (e["NGT"] + 1) + tiled_cbc.fetched_bytes(e, act) + 2 * K + 2 * M
+    assert bench.cbc_spmspv_bytes(W, x) == expect
