@@ -83,12 +83,13 @@ extern "C" bsp_status_t bsp_spmm_noalloc(const uint64_t* bitmaps, const uint32_t
 
     cudaStream_t s = (cudaStream_t)stream;
     // The scratch keeps whatever the previous call left: clear the parts
-    // this call relies on starting at zero (its workspace slice, the strip
-    // counters, the error word).
+    // this call relies on starting at zero (its workspace slice: 16 M
+    // entries, which covers both the CUDA-core kernels' [N][M] layout and
+    // the narrow kernel's [M][16]; the strip counters; the error word).
     unsigned char* ws = d->ptr;
     unsigned char* counters = d->ptr + kWsBytes;
     int* err = reinterpret_cast<int*>(d->ptr + kWsBytes + kCounterBytes);
-    if (cudaMemsetAsync(ws, 0, (size_t)N * (size_t)M * 4, s) != cudaSuccess ||
+    if (cudaMemsetAsync(ws, 0, (size_t)BSP_DECODE_MAX_N * (size_t)M * 4, s) != cudaSuccess ||
         cudaMemsetAsync(counters, 0, (size_t)(M / 64) * 4, s) != cudaSuccess ||
         cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
         return BSP_ERR_CUDA;
@@ -105,11 +106,14 @@ extern "C" bsp_status_t bsp_spmm_noalloc(const uint64_t* bitmaps, const uint32_t
     p.max_gt_nnz = 4096;  // the arrays are not inspected: any GT may be dense
     p.device = dev;
     p.num_sms = d->num_sms;
-    // the kernel indexes the workspace as [n][M]: the same layout as the
-    // handle's, with M as the row pitch
+    // the CUDA-core kernels index the workspace as [n][M] and the narrow
+    // kernel as [M][16]: both within the 16 M entries cleared above, the
+    // handle's layouts with M as the pitch
     p.ws = ws;
     p.counters = reinterpret_cast<uint32_t*>(counters);
     p.err = err;
+    // the dispatch of bsp_spmm
+    if (dtype == BSP_FP16 && N >= bsp_tune(BSP_TUNE_NARROW_MIN_N)) return bsp_run_spmm_narrow(p, X, N, Y, s);
     const bsp_out_mode mode = dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     return bsp_run_spmm_decode(p, X, (int)N, Y, mode, nullptr, false, s);
 }

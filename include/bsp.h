@@ -74,7 +74,9 @@ typedef enum {
     BSP_INT8 = 1  /* int8 values, int32 accumulation (exact)             */
 } bsp_dtype_t;
 
-/* Largest N taken by the CUDA-core decode path; larger N use tensor cores. */
+/* Largest N of the decode path (the skinny product, N <= 16): split-K
+ * workspaces are sized for it.  Larger N run the prefill kernel (fp16) or
+ * the decode kernels over blocks of 16 columns (int8). */
 #define BSP_DECODE_MAX_N 16
 
 typedef struct {
@@ -120,11 +122,17 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  * Inference", section 3.1: W in R^{MxK}, X in R^{KxN}.)
  *   X  device [N][K], fp16 (BSP_FP16 handle) or int8 (BSP_INT8), 16-B aligned.
  *   Y  device [N][M], fp16 (BSP_FP16) or int32 (BSP_INT8), 16-B aligned.
- *   N  >= 1.  N <= BSP_DECODE_MAX_N runs the CUDA-core decode kernel
- *      (split-K over GroupTiles, fp32 / int32 accumulation).  Larger N:
- *      fp16 runs the tcgen05 tensor-core prefill kernel (decoded tiles, fp32
- *      accumulation in tensor memory); int8 runs the decode kernel over
- *      blocks of 16 columns (there is no int8 tensor-core path).
+ *   N  >= 1.  Kernels, by dtype and N (the fp16 crossover is the tuning
+ *      knob BSP_TUNE_NARROW_MIN_N, default 3):
+ *        fp16, N <= 2: the GT-per-warp CUDA-core decode kernel (split-K
+ *          over GroupTiles, fp32 accumulation);
+ *        fp16, 3 <= N <= 16: the narrow tcgen05 kernel (decoded tiles in
+ *          tensor memory, MMAs of N = 16, fp32 accumulation, persistent
+ *          CTAs; tiles split between CTAs are finished by a second kernel);
+ *        fp16, N > 16: the tcgen05 prefill kernel (decoded tiles in shared
+ *          memory, fp32 accumulation in tensor memory);
+ *        int8, any N: the CUDA-core team decode kernel (dp4a, exact int32),
+ *          over blocks of 16 columns when N > 16 (no int8 tensor-core path).
  * fp16: Y = fp16(round-to-nearest of an fp32 sum in unspecified order).
  * int8: Y is the exact int32 sum.
  */
@@ -200,12 +208,18 @@ bsp_status_t bsp_spmm_scaled(bsp_handle_t h, const int8_t *X, int64_t N,
 
 /*
  * Sparse-matrix times sparse-vector: y = W * x for one activation vector,
- * skipping the weight tiles whose activations are all zero ("Unified
+ * skipping the weight columns whose activation is exactly zero ("Unified
  * Static-Dynamic Pruning for Efficient LLM Inference", sections 4.2-4.2.1:
- * inactive columns are neither loaded nor decoded).  The skip unit is an
- * 8-column BitmapTile column (a K-octet): its values are not read when
- * x[8j .. 8j+7] are all exactly zero.  The result equals bsp_spmm with N=1.
+ * inactive columns are neither loaded nor decoded).  The result equals
+ * bsp_spmm with N = 1.
  *   x device [K] (fp16 or int8), y device [M] (fp16 or int32), 16-B aligned.
+ * With a column index (bsp_build_column_index) the skip unit is the column
+ * for both the fetch and the arithmetic: only the active columns' bitmaps
+ * and values are read.  Without one it runs on the row-wise format: fp16
+ * skips the multiply-adds per column and the fetch per K-octet (a BT column
+ * of 8 activations, fetched only when one of them survives, and fetched by
+ * the octet only in GroupTiles where at most two of the eight octets
+ * survive); int8 skips per K-octet.
  */
 bsp_status_t bsp_spmspv(bsp_handle_t h, const void *x, void *y,
                         bsp_stream_t stream);
@@ -215,8 +229,8 @@ bsp_status_t bsp_spmspv(bsp_handle_t h, const void *x, void *y,
  * "Unified Static-Dynamic Pruning for Efficient LLM Inference" (section
  * 3.2 and 4.2, a TEAL-style magnitude criterion):
  *   y = W * x',  x'_k = 0 if |x_k| <= threshold, else x_k.
- * K-octets whose eight activations are all pruned are skipped as in
- * bsp_spmspv; threshold = 0 is exactly bsp_spmspv.  NaN activations are
+ * Pruned columns are skipped as in bsp_spmspv (with a column index, per
+ * column; without, per K-octet); threshold = 0 is exactly bsp_spmspv.  NaN activations are
  * never pruned.  threshold must be >= 0 (BSP_ERR_INVALID_ARG otherwise).
  * The comparison is |x| <= threshold with x widened exactly to fp32.
  */
@@ -279,7 +293,10 @@ bsp_status_t bsp_storage_bytes(bsp_handle_t h, uint64_t *bytes);
  */
 bsp_status_t bsp_cr(bsp_handle_t h, double *cr);
 
-/* Shapes, counts and device pointers of the encoded arrays (read only). */
+/* Shapes, counts and device pointers of the encoded arrays (read only):
+ * the bitmaps, offsets and values of the format of "SpInfer: How bitmaps
+ * make sparse LLMs actually fast", section "How TCA-BME addresses the
+ * indexing overhead". */
 bsp_status_t bsp_info(bsp_handle_t h, bsp_info_t *out);
 
 /*
@@ -320,7 +337,11 @@ bsp_status_t bsp_check(bsp_handle_t h, bsp_stream_t stream);
 
 /*
  * Decode back to dense: W_out device row-major [M][K] (fp16 or int8 bits),
- * 16-B aligned.  decode(encode(W)) == W bit for bit.
+ * 16-B aligned.  Each element is the value at offsets[t] + (values of the
+ * earlier BTs of its GT) + the masked popcount of its BT's bitmap, or 0
+ * when its bit is clear ("SpInfer: How bitmaps make sparse LLMs actually
+ * fast", sections "How TCA-BME addresses the indexing overhead" and "Shared
+ * Memory Bitmap Decoding (SMBD)").  decode(encode(W)) == W bit for bit.
  */
 bsp_status_t bsp_decode(bsp_handle_t h, void *W_out, bsp_stream_t stream);
 
@@ -356,9 +377,15 @@ bsp_status_t bsp_decode(bsp_handle_t h, void *W_out, bsp_stream_t stream);
  * `stream`), so calls that overlap on the GPU (different streams, or other
  * threads) race and must not be issued.  The first call on a device, with
  * that device current, looks up the array's device address and zeroes it
- * synchronously: make that first call before any stream capture.  Results
- * match bsp_spmm.  A device-side wait that gives up leaves Y incomplete and
- * is not reported here (bsp_spmm with bsp_check reports it).
+ * synchronously: make that first call before any stream capture.  The call
+ * runs the kernels bsp_spmm runs for the same dtype and N (fp16 N <= 2:
+ * GT-per-warp CUDA-core kernel; fp16 N >= BSP_TUNE_NARROW_MIN_N: the narrow
+ * tcgen05 kernel and its finishing kernel; int8 and the N between: the
+ * CUDA-core team kernel), with GroupTile stages sized for dense GroupTiles
+ * (it does not inspect the arrays), so the results equal bsp_spmm's within
+ * the fp16 rounding bound (int8: exactly).  A device-side wait that gives
+ * up leaves Y incomplete and is not reported here (bsp_spmm with bsp_check
+ * reports it).
  */
 bsp_status_t bsp_spmm_noalloc(const uint64_t *bitmaps, const uint32_t *offsets,
                               const void *values, bsp_dtype_t dtype, int64_t M,
@@ -462,6 +489,10 @@ bsp_status_t bsp_union_destroy(bsp_union_t h);
  * Y = W * X, exact int32 accumulation ("UnionSparse" W8A8 / W4A4: the int4
  * activations are int8 values in -8..7).  X device int8 [N][K], Y device
  * int32 [N][M], both 16-B aligned; N >= 1 (runs in blocks of 16 columns).
+ * For a 4-bit handle X must hold values in -8..7: the product accumulates
+ * 16 w x in int32 and divides once at the end, which is exact only for
+ * int4 activations; X is not checked, and other values give undefined
+ * results.
  * The decode-path kernel on CUDA cores (dp4a); calls on one handle must be
  * serialised on one stream.  A device-side wait that gives up leaves Y
  * incomplete and is reported by bsp_union_check.

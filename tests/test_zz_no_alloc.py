@@ -50,7 +50,7 @@ def _noalloc(A, arrays, X, N, Y):
                               X.data_ptr(), N, Y.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("N", [1, 5, 16])
+@pytest.mark.parametrize("N", [1, 3, 5, 16])
 def test_noalloc_matches_spmm_fp16(N):
     M, K = 384, 2048
     W = synth.weights_f16(M, K, 0.5, "uniform", 201)
