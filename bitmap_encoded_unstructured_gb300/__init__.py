@@ -85,7 +85,7 @@ TESTING_SIGNATURES = {
 
 # bsp_tune_t of include/bsp.h
 TUNE = {"splitk": 0, "narrow_ctas": 1, "union_splitk": 2, "narrow_min_n": 3,
-        "prefill_ksplit": 4, "prefill_cstages": 5}
+        "prefill_ksplit": 4, "prefill_cstages": 5, "narrow_min_n_i8": 6}
 
 
 class bsp_info_t(C.Structure):

@@ -163,8 +163,7 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void* X, int64_t N, void* Y, bsp_str
     cudaStream_t s = (cudaStream_t)stream;
     const bsp_out_mode mode = h->dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     if (N <= BSP_DECODE_MAX_N) {
-        if (h->dtype == BSP_FP16 && N >= bsp_tune(BSP_TUNE_NARROW_MIN_N))
-            return bsp_run_spmm_narrow(bsp_problem_of(h), X, N, Y, s);
+        if (N >= bsp_narrow_min_n(h->dtype)) return bsp_run_spmm_narrow(bsp_problem_of(h), X, N, Y, s);
         return bsp_run_spmm_decode(bsp_problem_of(h), X, (int)N, Y, mode, nullptr, false, s);
     }
     // Larger N, fp16: the tcgen05 prefill kernel.

@@ -122,11 +122,12 @@ int bsp_decode_split_cap(const bsp_decode_problem& p);
 bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                   cudaStream_t s);
 
-// ---- tcgen05 narrow kernel (spmm_narrow.cu), fp16, 1 <= N <= 16 ----
+// ---- tcgen05 narrow kernel (spmm_narrow.cu), fp16 or int8, 1 <= N <= 16 ----
 // Persistent, balanced over the SM slots; tiles split between CTAs meet in
-// the decode problem's workspace (zero between calls, fp32 [M][16] here) or,
-// in deterministic mode, in its slots ([slots][M][16]), and a second kernel
-// converts them.
+// the decode problem's workspace (zero between calls, fp32 [M][16] here;
+// int32 for int8, whose tiles of more than 16 GT columns meet there too)
+// or, fp16 in deterministic mode, in its slots ([slots][M][16]), and a
+// second kernel converts them.  int8: X int8 [N][K], Y int32 [N][M], exact.
 bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                  cudaStream_t s);
 // Slots the deterministic mode needs for the automatic CTA count: the
@@ -147,6 +148,9 @@ bsp_status_t bsp_run_spmspv_cbc(const bsp_handle* h, const void* x, void* y, flo
 // bsp_set_tuning.  0 means "automatic" for the split counts and the C ring
 // depth; BSP_TUNE_PREFILL_KSPLIT is -1 (automatic), 0 or 1.
 int64_t bsp_tune(bsp_tune_t knob);
+// Smallest N (<= BSP_DECODE_MAX_N) that runs the tcgen05 narrow kernel for
+// weights of this dtype (BSP_TUNE_NARROW_MIN_N, BSP_TUNE_NARROW_MIN_N_I8).
+int64_t bsp_narrow_min_n(bsp_dtype_t dtype);
 // Spin cap of the kernels' bounded waits, and whether producers skip their
 // first copies (a wait that runs out, for the timeout tests).  Both are
 // fixed (bspx::kSpinCap, no skipping) unless the library was built with

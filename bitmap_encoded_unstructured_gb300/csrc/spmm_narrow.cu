@@ -66,6 +66,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 // split model: fixed cost of a CTA in GT-column steps
 #ifndef BSP_NARROW_CTA_COST
@@ -111,15 +112,27 @@ static_assert(MINB == 1 || MINB == 2, "one or two CTAs per SM");
 constexpr int SMEM_MAX = MINB == 1 ? 227 * 1024 : 228 * 1024 / 2 - 1024;
 constexpr int B_STAGE = BN * BK * 2;       // 2 KB
 constexpr int RS_WARP = 32 * 8 * 2;        // a decoder warp's row-start table: [BT][row] u16
+constexpr int XS_STAGE = BN * BK;          // an int8 X tile as it arrives (1 KB)
 constexpr int OFF_B = 0;                   // 1024-B aligned (the X tiles' 128-B swizzle)
 constexpr int OFF_RS = OFF_B + SB * B_STAGE;
-constexpr int OFF_BAR = OFF_RS + DEC_WARPS * RS_WARP;
+constexpr int OFF_XS = OFF_RS + DEC_WARPS * RS_WARP;
 // barriers: c_full[SC_MAX] c_empty[SC_MAX] b_full[SB] b_empty[SB] a_full[NG] a_empty[NG]
-// acc_full[2] acc_empty[2] drain
-constexpr int NBAR = 2 * SC_MAX + 2 * SB + 2 * NG + 5;
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // TMEM address (4 B)
-constexpr int OFF_C = (OFF_TMEM + 16 + 127) & ~127;
-constexpr int C_BYTES = SMEM_MAX - 1024 - OFF_C;  // 1024: slack to align the base to 1024 B
+// acc_full[2] acc_empty[2] drain xs_full[2]
+constexpr int NBAR = 2 * SC_MAX + 2 * SB + 2 * NG + 7;
+// The rest of the layout: after two int8 X staging tiles for int8 weights.
+template <bool I8>
+struct Layout {
+    static constexpr int OFF_BAR = OFF_XS + (I8 ? 2 * XS_STAGE : 0);
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // TMEM address (4 B)
+    static constexpr int OFF_C = (OFF_TMEM + 16 + 127) & ~127;
+    static constexpr int C_BYTES = SMEM_MAX - 1024 - OFF_C;  // 1024: slack to align the base to 1024 B
+};
+// int8 weights: the tensor cores multiply fp16 copies of the int8 values
+// (exact), accumulating in fp32; a run of at most RUN_I8 steps sums at most
+// 64 RUN_I8 products of magnitude <= 127 * 128, below 2^24, so every fp32
+// partial sum is an exact integer.  Each run leaves the accumulator as int32.
+constexpr uint32_t RUN_I8 = 16;
+static_assert(64u * RUN_I8 * 127u * 128u < (1u << 24), "exact fp32 runs");
 // tensor memory: two accumulators (16 fp32 columns each, 32 apart), then NG
 // decoded A tiles of 128 lanes x 64 fp16 = 32 columns each
 constexpr uint32_t D_COLS = 32;
@@ -135,15 +148,15 @@ constexpr uint32_t TMEM_COLS = tmem_cols_for(A_OFF + NG * A_COLS);
 static_assert(TMEM_COLS * MINB <= 512, "tensor memory of the resident CTAs");
 
 // One C stage: two GT slots (512 B of bitmaps, then the 16-B chunks that
-// hold the GT's value span) and a 16-B header (the value shifts).  The slot
-// is sized for the densest GT of the matrix, so the number of stages that
-// fit follows the density.
-constexpr uint32_t c_slot_bytes(uint32_t max_gt_nnz)
+// hold the GT's value span, `vpc` values per chunk) and a 16-B header (the
+// value shifts).  The slot is sized for the densest GT of the matrix, so the
+// number of stages that fit follows the density.
+constexpr uint32_t c_slot_bytes(uint32_t max_gt_nnz, uint32_t vpc)
 {
-    return (512u + 16u * ((max_gt_nnz + 7u) / 8u + 1u) + 127u) & ~127u;
+    return (512u + 16u * ((max_gt_nnz + vpc - 1u) / vpc + 1u) + 127u) & ~127u;
 }
 constexpr uint32_t c_stage_bytes(uint32_t slot) { return (2u * slot + 16u + 127u) & ~127u; }
-static_assert(C_BYTES >= NG * (int)c_stage_bytes(c_slot_bytes(4096)) && NG <= SC_MAX,
+static_assert(Layout<true>::C_BYTES >= NG * (int)c_stage_bytes(c_slot_bytes(4096, 8)) && NG <= SC_MAX,
               "a dense C stage per decoder group");
 static_assert((B_STAGE % 1024) == 0 && (OFF_RS % 16) == 0, "alignment of the X tiles and tables");
 
@@ -155,16 +168,17 @@ struct NarrowArgs {
     const uint64_t* bitmaps;
     const uint32_t* offsets;
     const uint8_t* values;
-    __half* Y;
+    void* Y;                   // fp16 or (int8 weights) int32, [N][M]
     int64_t M, N, K;           // logical: Y rows, columns, X row length
     int64_t Mp, KT;            // padded grid: rows (a multiple of 64), GT columns
     int64_t T;                 // steps of the whole product: tiles x KT
     int64_t P;                 // CTAs (1 <= P <= T)
     uint32_t c_slot, c_stage;  // C ring geometry (bytes): GT slot, stage
     int sc;                    // C stages in use, NG..SC_MAX
-    // partial sums of the tiles split between CTAs: fp32 [M][16], zero
-    // between calls (vector reductions; the finishing kernel clears it), or
-    // in deterministic mode the slots [slots][M][16], one per segment
+    // partial sums of the tiles split between CTAs: fp32 [M][16] (int32 for
+    // int8 weights), zero between calls (reductions; the finishing kernel
+    // clears it), or in deterministic mode (fp16) the slots [slots][M][16],
+    // one per segment
     float* ws;
     float* ws_det;
     int* err;
@@ -302,11 +316,58 @@ __device__ __forceinline__ void decode_rowbyte(const uint16_t* vp, uint32_t byte
     for (int k = 0; k < 4; ++k) w[k] = __byte_perm(h[2 * k], h[2 * k + 1], 0x5410);
 }
 
+// The same for int8 values: each stored value becomes its fp16 copy (exact:
+// |v| <= 128).
+__device__ __forceinline__ void decode_rowbyte(const int8_t* vp, uint32_t byte, uint32_t* w)
+{
+    uint32_t h[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        h[c] = 0u;
+        if (byte & (1u << c)) {
+            h[c] = __half_as_ushort(__short2half_rn((short)*vp));
+            ++vp;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __byte_perm(h[2 * k], h[2 * k + 1], 0x5410);
+}
+
+__device__ __forceinline__ void red_add_s32(int* p, int v)
+{
+    asm volatile("red.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 16 int8 values (one 16-B load) as fp16 in two 16-B chunks
+__device__ __forceinline__ void i8x16_to_f16(const uint4 v, uint4& lo, uint4& hi)
+{
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t x = wv[q];
+        const uint32_t b0 = __half_as_ushort(__short2half_rn((short)(int8_t)(x & 0xFFu)));
+        const uint32_t b1 = __half_as_ushort(__short2half_rn((short)(int8_t)((x >> 8) & 0xFFu)));
+        const uint32_t b2 = __half_as_ushort(__short2half_rn((short)(int8_t)((x >> 16) & 0xFFu)));
+        const uint32_t b3 = __half_as_ushort(__short2half_rn((short)(int8_t)(x >> 24)));
+        o[2 * q] = b0 | (b1 << 16);
+        o[2 * q + 1] = b2 | (b3 << 16);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Grid: P CTAs, persistent: CTA c takes the steps [c T / P, (c + 1) T / P)
-// (step x is GT column x % KT of tile x / KT).
+// (step x is GT column x % KT of tile x / KT).  I8: int8 weights and X
+// (the B producer converts each X tile to fp16), int32 Y, exact runs of at
+// most RUN_I8 steps.
+template <bool I8>
 __global__ void __launch_bounds__(THREADS, MINB)
 spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
 {
+    using L = Layout<I8>;
+    constexpr uint32_t VPC = I8 ? 16u : 8u;        // values per 16-B chunk
+    constexpr uint32_t RUN = I8 ? RUN_I8 : 1u;     // steps per exact run (int8 only; fp16 runs are segments)
     const uint32_t SC = (uint32_t)a.sc;
     const uint32_t SLOT = a.c_slot, C_HDR = 2 * SLOT;
     const uint32_t vchunks = (SLOT - 512) / 16;  // value chunks a slot holds
@@ -317,7 +378,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    uint64_t* c_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* c_full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
     uint64_t* c_empty = c_full + SC_MAX;
     uint64_t* b_full = c_empty + SC_MAX;
     uint64_t* b_empty = b_full + SB;
@@ -326,9 +387,10 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     uint64_t* acc_full = a_empty + NG;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    uint64_t* xs_full = drain + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
     auto b_stage = [&](uint32_t s) { return smem + OFF_B + s * B_STAGE; };
-    auto c_stage = [&](uint32_t s) { return smem + OFF_C + s * a.c_stage; };
+    auto c_stage = [&](uint32_t s) { return smem + L::OFF_C + s * a.c_stage; };
 
     const int64_t M = a.M, N = a.N, T = a.T, P = a.P;
     const uint32_t KTA = (uint32_t)a.KT;  // GT columns of the grid (row pitch, steps per tile)
@@ -338,6 +400,12 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     const int64_t t0 = g0 / KTA;                                    // first tile
     const uint32_t kk0 = (uint32_t)(g0 - t0 * KTA);                 // its first GT column
     const uint32_t cap = a.spin_cap;
+    // exact runs (int8): a run restarts the accumulator every RUN steps of a
+    // segment.  L0: steps of the CTA's first segment; R0, RT: runs of the
+    // first segment and of a whole tile
+    const uint32_t L0 = min(S, KTA - kk0);
+    const uint32_t R0 = I8 ? (L0 + RUN - 1) / RUN : 1u;
+    const uint32_t RT = I8 ? (KTA + RUN - 1) / RUN : 1u;
 
     if (warp == MMAW) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -364,6 +432,8 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             bspx::mbar_init(acc_empty + d, 4);  // the four warps of an epilogue
         }
         bspx::mbar_init(drain, 1);
+        bspx::mbar_init(xs_full, 1);
+        bspx::mbar_init(xs_full + 1, 1);
         bspx::fence_mbar_init();
     }
     tc_fence_before();
@@ -400,15 +470,15 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
             if (lane == 0) {
                 uint8_t* st = c_stage(s);
                 uint32_t* hdr = reinterpret_cast<uint32_t*>(st + C_HDR);
-                const uint32_t cha = oa0 / 8, chb = ob0 / 8;
-                uint32_t nca = (oa1 + 7) / 8 - cha, ncb = has_b ? (ob1 + 7) / 8 - chb : 0u;
+                const uint32_t cha = oa0 / VPC, chb = ob0 / VPC;
+                uint32_t nca = (oa1 + VPC - 1) / VPC - cha, ncb = has_b ? (ob1 + VPC - 1) / VPC - chb : 0u;
                 if (nca > vchunks || ncb > vchunks) {  // a GT denser than the handle recorded
                     atomicExch(a.err, (int)BSP_ERR_INTERNAL);
                     nca = min(nca, vchunks);
                     ncb = min(ncb, vchunks);
                 }
-                hdr[0] = oa0 - cha * 8;
-                hdr[1] = ob0 - chb * 8;
+                hdr[0] = oa0 - cha * VPC;
+                hdr[1] = ob0 - chb * VPC;
                 uint32_t bytes = 512 + nca * 16;
                 if (has_b) bytes += 512 + ncb * 16;
                 bspx::mbar_arrive_expect_tx(c_full + s, bytes);
@@ -425,6 +495,56 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         // let the last copies land before the CTA can exit (bounded)
         for (uint32_t j = (i > SC ? i - SC : 0); j < i; ++j)
             bspx::mbar_wait_bounded(c_full + (j % SC), (j / SC) & 1u, cap);
+    } else if (warp == BPROD && I8) {
+        // ---------------- B producer, int8 X: the 16 x 64 int8 tile of step i
+        // arrives by TMA in staging buffer i % 2 (the next one is in flight
+        // meanwhile); lane l converts row l / 2, half l % 2 (32 values) to
+        // fp16 into the 128-B-swizzled X stage (16-B chunk c of row r at
+        // chunk position c ^ (r % 8)), then the stage is handed to the MMAs
+        // (X may be written by the previous kernel on the stream)
+        wait_prior_grids();
+        uint8_t* xs = smem + OFF_XS;
+        auto x_issue = [&](uint32_t i, uint32_t kx) {
+            if (lane == 0) {
+                bspx::mbar_arrive_expect_tx(xs_full + (i & 1u), (uint32_t)XS_STAGE);
+                tma_load_2d(xs + (i & 1u) * XS_STAGE, &tmX, (int)(kx * BK), 0, xs_full + (i & 1u));
+            }
+        };
+        uint32_t s = 0, ph = 0;
+        uint32_t k = kk0;
+        uint32_t i = 0;
+        x_issue(0, kk0);
+        const int r = lane >> 1, hh = lane & 1;
+        for (; i < S; ++i) {
+            if (i + 1 < S) x_issue(i + 1, k + 1 == KTA ? 0u : k + 1);  // its buffer was converted at step i - 1
+            bool ok = wait_bar(xs_full + (i & 1u), (i >> 1) & 1u, cap, BSP_NARROW_SLEEP_PROD);
+            if (i >= (uint32_t)SB) ok = ok && wait_bar(b_empty + s, ph ^ 1u, cap, BSP_NARROW_SLEEP_PROD);
+            if (!__all_sync(FULL, ok)) {
+                failed = true;
+                break;
+            }
+            const uint4* src = reinterpret_cast<const uint4*>(xs + (i & 1u) * XS_STAGE + r * BK + hh * 32);
+            uint8_t* dst = b_stage(s) + r * 128;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint4 lo, hi;
+                i8x16_to_f16(src[h2], lo, hi);
+                const int c0 = 4 * hh + 2 * h2;  // fp16 chunk of the row
+                *reinterpret_cast<uint4*>(dst + ((c0 ^ (r & 7)) * 16)) = lo;
+                *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (r & 7)) * 16)) = hi;
+            }
+            // the writes are seen by the tensor cores (async proxy), and the
+            // staging buffer may be refilled by TMA
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) bspx::mbar_arrive(b_full + s);
+            if (++s == (uint32_t)SB) { s = 0; ph ^= 1u; }
+            if (++k == KTA) k = 0;
+        }
+        // staging copies still in flight (a wait gave up) land before the
+        // CTA can exit (bounded)
+        for (uint32_t q = i; q < S && q <= i + 1; ++q)
+            bspx::mbar_wait_bounded(xs_full + (q & 1u), (q >> 1) & 1u, cap);
     } else if (warp == BPROD) {
         // ---------------- B producer: one 16 x 64 X tile per step by TMA
         // (X may be written by the previous kernel on the stream)
@@ -456,7 +576,9 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         uint32_t k = kk0, seg = 0;
         for (uint32_t i = 0; i < S && !failed; ++i) {
             const uint32_t g = i % NG;
-            const bool first = i == 0 || k == 0, last = i + 1 == S || k + 1 == KTA;
+            const uint32_t pos = i < L0 ? i : k;  // step within the segment
+            const bool first = I8 ? pos % RUN == 0 : (i == 0 || k == 0);
+            const bool last = i + 1 == S || k + 1 == KTA || (I8 && (pos + 1) % RUN == 0);
             const uint32_t buf = seg & 1u;
             bool ok = wait_bar(a_full + g, (i / NG) & 1u, cap, BSP_NARROW_SLEEP_MMA);
             ok = ok && wait_bar(b_full + sb, pb, cap, BSP_NARROW_SLEEP_MMA);
@@ -532,7 +654,8 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 *reinterpret_cast<uint4*>(rs + 8 * lane) = bspx::row_starts(bm, base);
                 __syncwarp();
                 const uint8_t* bytes = slot + 256 * h;  // byte 8 bt + r: row r of the half's BT bt
-                const uint16_t* vals = reinterpret_cast<const uint16_t*>(slot + 512);
+                using VT = typename std::conditional<I8, int8_t, uint16_t>::type;
+                const VT* vals = reinterpret_cast<const VT*>(slot + 512);
 #pragma unroll
                 for (int o = 0; o < 8; ++o) {
                     const int bt = bt0 + 4 * (o >> 1) + 2 * (o & 1);
@@ -555,10 +678,14 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 bspx::mbar_arrive(a_full + G);
                 bspx::mbar_arrive(c_empty + sc);
             }
-            if (i + 1 == S || k + 1 == KTA) {
-                // ---------------- epilogue of the segment this step ends:
-                // one row of 16 columns per thread
-                const uint32_t seg = t - (uint32_t)t0, buf = seg & 1u;
+            const uint32_t pos = t == (uint32_t)t0 ? i : k;  // step within the segment
+            if (i + 1 == S || k + 1 == KTA || (I8 && (pos + 1) % RUN == 0)) {
+                // ---------------- epilogue of the segment (int8: the run) this
+                // step ends: one row of 16 columns per thread.  Its number
+                // among the CTA's accumulator uses picks the buffer.
+                const uint32_t seg = !I8 ? t - (uint32_t)t0
+                                         : (t == (uint32_t)t0 ? pos / RUN : R0 + (t - (uint32_t)t0 - 1) * RT + k / RUN);
+                const uint32_t buf = seg & 1u;
                 if (!__all_sync(FULL, wait_bar(acc_full + buf, (seg >> 1) & 1u, cap, BSP_NARROW_SLEEP_DEC))) {
                     failed = true;
                     break;
@@ -571,10 +698,25 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 if (m < M) {
                     const int64_t first = step_owner((int64_t)t * KTA, T, P);
                     const int64_t nseg = step_owner(((int64_t)t + 1) * KTA - 1, T, P) - first + 1;
-                    if (nseg == 1) {
+                    if (I8) {
+                        // exact integers: straight to Y when the tile is one
+                        // run of one CTA, else added into the int32 workspace
+                        int* Yi = static_cast<int*>(a.Y);
+                        int* wsi = reinterpret_cast<int*>(a.ws);
+                        if (nseg == 1 && RT == 1) {
+#pragma unroll
+                            for (int j = 0; j < BN; ++j)
+                                if (j < N) Yi[j * M + m] = __float2int_rn(__uint_as_float(r[j]));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN; ++j)
+                                if (j < N) red_add_s32(wsi + m * 16 + j, __float2int_rn(__uint_as_float(r[j])));
+                        }
+                    } else if (nseg == 1) {
+                        __half* Yh = static_cast<__half*>(a.Y);
 #pragma unroll
                         for (int j = 0; j < BN; ++j)
-                            if (j < N) a.Y[j * M + m] = __float2half_rn(__uint_as_float(r[j]));
+                            if (j < N) Yh[j * M + m] = __float2half_rn(__uint_as_float(r[j]));
                     } else if (a.ws_det) {
                         float4* d = reinterpret_cast<float4*>(a.ws_det + ((cta - first) * M + m) * 16);
 #pragma unroll
@@ -618,11 +760,13 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     }
 }
 
-// Finishing kernel: Y of the tiles whose steps are split between CTAs, from
-// the workspace (which it clears) or, deterministically, from the segments'
-// slots added in segment order.  One thread per (row, column < N).
+// Finishing kernel: Y of the tiles whose steps are split between CTAs (and,
+// int8, of the tiles of several runs), from the workspace (which it clears)
+// or, deterministically, from the segments' slots added in segment order.
+// One thread per (row, column < N).
+template <bool I8>
 __global__ void __launch_bounds__(256)
-spmm_narrow_finish_kernel(__half* __restrict__ Y, float* __restrict__ ws, const float* __restrict__ ws_det,
+spmm_narrow_finish_kernel(void* __restrict__ Y, float* __restrict__ ws, const float* __restrict__ ws_det,
                           int64_t M, int64_t N, int64_t KT, int64_t T, int64_t P)
 {
     // the next product kernel may start its prologue now (it waits for this
@@ -635,7 +779,13 @@ spmm_narrow_finish_kernel(__half* __restrict__ Y, float* __restrict__ ws, const 
         const int64_t t = m / BM;
         const int64_t first = step_owner(t * KT, T, P);
         const int64_t nseg = step_owner((t + 1) * KT - 1, T, P) - first + 1;
-        if (nseg == 1) continue;  // written by the product kernel
+        if (nseg == 1 && (!I8 || KT <= (int64_t)RUN_I8)) continue;  // written by the product kernel
+        if (I8) {
+            int* wsi = reinterpret_cast<int*>(ws);
+            static_cast<int*>(Y)[n * M + m] = wsi[m * 16 + n];
+            wsi[m * 16 + n] = 0;
+            continue;
+        }
         float v;
         if (ws_det) {
             v = 0.f;
@@ -644,7 +794,7 @@ spmm_narrow_finish_kernel(__half* __restrict__ Y, float* __restrict__ ws, const 
             v = ws[m * 16 + n];
             ws[m * 16 + n] = 0.f;
         }
-        Y[n * M + m] = __float2half_rn(v);
+        static_cast<__half*>(Y)[n * M + m] = __float2half_rn(v);
     }
 }
 
@@ -694,42 +844,45 @@ int bsp_narrow_det_slots(const bsp_decode_problem& p)
     return (int)max_segments(tiles, KT, T, narrow_ctas_auto(p, T));
 }
 
-bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
+namespace {
+
+template <bool I8>
+bsp_status_t launch_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
 {
-    if (p.dtype != BSP_FP16) return BSP_ERR_DTYPE;
-    if (N < 1 || N > BN || p.K > (int64_t)0x7FFFFFFF) return BSP_ERR_INVALID_ARG;
-    if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
+    using L = Layout<I8>;
     auto encode = get_encode_fn();
     if (!encode) return BSP_ERR_CUDA;
-    // X: [N][K] fp16, K contiguous; boxes of 64 (K) x 16 rows, 128-B
-    // swizzle; rows past N read as zeros
+    // X: [N][K], K contiguous; boxes of 64 (K) x 16 rows, rows past N read
+    // as zeros.  fp16: 128-B swizzle, straight into the MMA's X stage; int8:
+    // unswizzled 1 KB tiles that the B producer converts
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.K * (I8 ? 1 : 2)};
     const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&map, I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               I8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return BSP_ERR_INVALID_ARG;
 
     static bsp_attr_once attr;
     if (!attr.run(p.device, [] {
-            return cudaFuncSetAttribute(spmm_narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+            return cudaFuncSetAttribute(spmm_narrow_kernel<I8>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
         }))
         return BSP_ERR_CUDA;
     const int64_t tiles = (p.Mp + BM - 1) / BM, KT = p.Kp / 64, T = tiles * KT;
     int64_t P = narrow_ctas_auto(p, T);
     if (const int64_t v = bsp_tune(BSP_TUNE_NARROW_CTAS)) P = std::min(v, T);  // tests, tuning
     // deterministic slots: one per CTA sharing a tile; fewer CTAs share less
-    if (p.ws_det)
+    if (p.ws_det && !I8)  // int8 partial sums are exact integers: any order gives the same Y
         while (P > 1 && max_segments(tiles, KT, T, P) > p.det_slots) --P;
     if (P < 1 || P > 0x7FFFFFFF) return BSP_ERR_INTERNAL;
     NarrowArgs a = {};
     a.bitmaps = p.bitmaps;
     a.offsets = p.offsets;
     a.values = (const uint8_t*)p.values;
-    a.Y = (__half*)Y;
+    a.Y = Y;
     a.M = p.M;
     a.N = N;
     a.K = p.K;
@@ -738,15 +891,15 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     a.T = T;
     a.P = P;
     a.ws = (float*)p.ws;
-    a.ws_det = p.ws_det;
+    a.ws_det = I8 ? nullptr : p.ws_det;
     a.err = p.err;
     a.spin_cap = bsp_spin_cap();
     // C ring: as many stages as fit, each sized for the densest GT
-    a.c_slot = c_slot_bytes(std::min<uint32_t>(p.max_gt_nnz, 4096u));
+    a.c_slot = c_slot_bytes(std::min<uint32_t>(p.max_gt_nnz, 4096u), I8 ? 16u : 8u);
     a.c_stage = c_stage_bytes(a.c_slot);
-    a.sc = std::min<int>(SC_MAX, C_BYTES / (int)a.c_stage);
+    a.sc = std::min<int>(SC_MAX, L::C_BYTES / (int)a.c_stage);
     if (a.sc < NG) return BSP_ERR_INTERNAL;  // each decoder group needs a stage of its own in flight
-    const int smem = OFF_C + a.sc * (int)a.c_stage + 1024;
+    const int smem = L::OFF_C + a.sc * (int)a.c_stage + 1024;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
@@ -758,9 +911,10 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
         cfg.stream = s;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, spmm_narrow_kernel, map, a) != cudaSuccess) return BSP_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, spmm_narrow_kernel<I8>, map, a) != cudaSuccess) return BSP_ERR_CUDA;
     }
-    if (!any_split(tiles, KT, T, P)) return BSP_OK;
+    // int8 tiles of more than one run go through the workspace too
+    if (!any_split(tiles, KT, T, P) && !(I8 && KT > (int64_t)RUN_I8)) return BSP_OK;
     // the tiles split between CTAs: converted by a programmatic dependent
     // kernel (launched while the product kernel drains; it waits for it)
     cudaLaunchConfig_t cfg = {};
@@ -770,8 +924,18 @@ bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, spmm_narrow_finish_kernel, (__half*)Y, (float*)p.ws, (const float*)p.ws_det,
-                              p.M, (int64_t)N, KT, T, P) == cudaSuccess
+    return cudaLaunchKernelEx(&cfg, spmm_narrow_finish_kernel<I8>, Y, (float*)p.ws, (const float*)a.ws_det, p.M,
+                              (int64_t)N, KT, T, P) == cudaSuccess
                ? BSP_OK
                : BSP_ERR_CUDA;
+}
+
+}  // namespace
+
+bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y, cudaStream_t s)
+{
+    if (p.dtype != BSP_FP16 && p.dtype != BSP_INT8) return BSP_ERR_DTYPE;
+    if (N < 1 || N > BN || p.K > (int64_t)0x7FFFFFFF) return BSP_ERR_INVALID_ARG;
+    if (p.device < 0 || p.device >= 64) return BSP_ERR_INVALID_ARG;
+    return p.dtype == BSP_INT8 ? launch_narrow<true>(p, X, N, Y, s) : launch_narrow<false>(p, X, N, Y, s);
 }

@@ -107,13 +107,13 @@ extern "C" bsp_status_t bsp_spmm_noalloc(const uint64_t* bitmaps, const uint32_t
     p.device = dev;
     p.num_sms = d->num_sms;
     // the CUDA-core kernels index the workspace as [n][M] and the narrow
-    // kernel as [M][16]: both within the 16 M entries cleared above, the
-    // handle's layouts with M as the pitch
+    // kernel as [M][16] (fp32, or int32 for int8): all within the 16 M
+    // entries cleared above, the handle's layouts with M as the pitch
     p.ws = ws;
     p.counters = reinterpret_cast<uint32_t*>(counters);
     p.err = err;
     // the dispatch of bsp_spmm
-    if (dtype == BSP_FP16 && N >= bsp_tune(BSP_TUNE_NARROW_MIN_N)) return bsp_run_spmm_narrow(p, X, N, Y, s);
+    if (N >= bsp_narrow_min_n(dtype)) return bsp_run_spmm_narrow(p, X, N, Y, s);
     const bsp_out_mode mode = dtype == BSP_INT8 ? BSP_OUT_I32 : BSP_OUT_F16;
     return bsp_run_spmm_decode(p, X, (int)N, Y, mode, nullptr, false, s);
 }

@@ -122,8 +122,9 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  * Inference", section 3.1: W in R^{MxK}, X in R^{KxN}.)
  *   X  device [N][K], fp16 (BSP_FP16 handle) or int8 (BSP_INT8), 16-B aligned.
  *   Y  device [N][M], fp16 (BSP_FP16) or int32 (BSP_INT8), 16-B aligned.
- *   N  >= 1.  Kernels, by dtype and N (the fp16 crossover is the tuning
- *      knob BSP_TUNE_NARROW_MIN_N, default 3):
+ *   N  >= 1.  Kernels, by dtype and N (the crossovers are the tuning
+ *      knobs BSP_TUNE_NARROW_MIN_N, default 3, and BSP_TUNE_NARROW_MIN_N_I8,
+ *      default 1):
  *        fp16, N <= 2: the GT-per-warp CUDA-core decode kernel (split-K
  *          over GroupTiles, fp32 accumulation);
  *        fp16, 3 <= N <= 16: the narrow tcgen05 kernel (decoded tiles in
@@ -131,8 +132,12 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  *          CTAs; tiles split between CTAs are finished by a second kernel);
  *        fp16, N > 16: the tcgen05 prefill kernel (decoded tiles in shared
  *          memory, fp32 accumulation in tensor memory);
- *        int8, any N: the CUDA-core team decode kernel (dp4a, exact int32),
- *          over blocks of 16 columns when N > 16 (no int8 tensor-core path).
+ *        int8, N <= 16: the same narrow tcgen05 kernel on exact fp16 copies
+ *          of the int8 weights and activations (fp32 accumulation in runs
+ *          of at most 16 GroupTile columns, each an exact integer below
+ *          2^24, added as int32); below the crossover the CUDA-core team
+ *          decode kernel (dp4a);
+ *        int8, N > 16: the team decode kernel over blocks of 16 columns.
  * fp16: Y = fp16(round-to-nearest of an fp32 sum in unspecified order).
  * int8: Y is the exact int32 sum.
  */
@@ -179,10 +184,13 @@ bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
  *                            pair: -1 automatic, 0 off, 1 on (N <= 256)
  *   BSP_TUNE_PREFILL_CSTAGES (BSP_PF_SC)         compressed-ring depth of the
  *                            prefill kernel; 0 = as many as fit
+ *   BSP_TUNE_NARROW_MIN_N_I8 (BSP_NARROW_MIN_N_I8) smallest int8 N <= 16
+ *                            that runs the tcgen05 decode kernel; larger
+ *                            than 16: never; default 1
  * Split counts are clamped to the problem (at most one per GroupTile
  * column).  BSP_ERR_INVALID_ARG for an unknown knob or a value out of range
- * (split counts and stages 0..4096, NARROW_CTAS 0..2^20, NARROW_MIN_N
- * 1..1024, KSPLIT -1..1).
+ * (split counts and stages 0..4096, NARROW_CTAS 0..2^20, NARROW_MIN_N and
+ * NARROW_MIN_N_I8 1..1024, KSPLIT -1..1).
  */
 typedef enum {
     BSP_TUNE_SPLITK = 0,
@@ -190,7 +198,8 @@ typedef enum {
     BSP_TUNE_UNION_SPLITK = 2,
     BSP_TUNE_NARROW_MIN_N = 3,
     BSP_TUNE_PREFILL_KSPLIT = 4,
-    BSP_TUNE_PREFILL_CSTAGES = 5
+    BSP_TUNE_PREFILL_CSTAGES = 5,
+    BSP_TUNE_NARROW_MIN_N_I8 = 6
 } bsp_tune_t;
 
 bsp_status_t bsp_set_tuning(bsp_tune_t knob, int64_t value);
@@ -198,7 +207,8 @@ bsp_status_t bsp_get_tuning(bsp_tune_t knob, int64_t *value);
 
 /*
  * INT8 with per-row dequantisation: Y[n][m] = fp32(acc[n][m]) * row_scale[m],
- * one round-to-nearest int->float conversion and one fp32 multiply.
+ * one round-to-nearest int->float conversion and one fp32 multiply (on the
+ * CUDA-core team decode kernel at every N).
  *   X device int8 [N][K]; row_scale device fp32 [M]; Y device fp32 [N][M].
  *   1 <= N <= BSP_DECODE_MAX_N.  BSP_ERR_DTYPE on an fp16 handle.
  */
@@ -379,9 +389,10 @@ bsp_status_t bsp_decode(bsp_handle_t h, void *W_out, bsp_stream_t stream);
  * that device current, looks up the array's device address and zeroes it
  * synchronously: make that first call before any stream capture.  The call
  * runs the kernels bsp_spmm runs for the same dtype and N (fp16 N <= 2:
- * GT-per-warp CUDA-core kernel; fp16 N >= BSP_TUNE_NARROW_MIN_N: the narrow
- * tcgen05 kernel and its finishing kernel; int8 and the N between: the
- * CUDA-core team kernel), with GroupTile stages sized for dense GroupTiles
+ * GT-per-warp CUDA-core kernel; N >= BSP_TUNE_NARROW_MIN_N (fp16) or
+ * BSP_TUNE_NARROW_MIN_N_I8 (int8): the narrow tcgen05 kernel and its
+ * finishing kernel; the N between: the CUDA-core team kernel), with
+ * GroupTile stages sized for dense GroupTiles
  * (it does not inspect the arrays), so the results equal bsp_spmm's within
  * the fp16 rounding bound (int8: exactly).  A device-side wait that gives
  * up leaves Y incomplete and is not reported here (bsp_spmm with bsp_check
