@@ -58,6 +58,14 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
 
 
+# Kernels one call of the step launches: the narrow and column-index spMspV
+# products are followed by their finishing kernel whenever tiles are split
+# between CTAs, which holds for every layer of the step at the automatic
+# CTA / split counts (tests/test_bench_cpu.py checks the split counts).
+LAUNCHES_PER_CALL = {"spmm_decode_gtw_kernel": 1, "spmm_decode_kernel": 1, "spmm_narrow_kernel": 2,
+                     "spmspv_cbc_kernel": 2}
+
+
 def step_kernel(key):
     """The kernel a call of the step launches, by the library's fp16
     dispatch (BSP_NARROW_MIN_N, else the library's default)."""
@@ -639,7 +647,7 @@ def run_gpu(args):
                 "breakdown": breakdown, "prefill": prefill, "union_ie_bme": union,
                 "sparsity_sweep": sweep, "int8": int8,
                 "roofline": roofline,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * args.steps,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * sum(LAUNCHES_PER_CALL[step_kernel(k)] for k, _ in calls),
                 "clocks": clk}
         print(json.dumps(line))
     if ws > 1:
