@@ -50,6 +50,7 @@ SIGNATURES = {
     "bsp_spmspv": (C.c_int, [_P, _P, _P, _P]),
     "bsp_spmspv_threshold": (C.c_int, [_P, _P, C.c_float, _P, _P]),
     "bsp_spmm_host": (C.c_int, [_P, _P, _I64, _P, _P]),
+    "bsp_spmm_host_async": (C.c_int, [_P, _P, _I64, _P, _P]),
     "bsp_storage_bytes": (C.c_int, [_P, C.POINTER(C.c_uint64)]),
     "bsp_cr": (C.c_int, [_P, C.POINTER(C.c_double)]),
     "bsp_info": (C.c_int, [_P, _P]),
@@ -224,6 +225,10 @@ def bsp_spmspv_threshold(h: int, x_ptr: int, threshold: float, y_ptr: int, strea
 
 def bsp_spmm_host(h: int, X_host_ptr: int, N: int, Y_host_ptr: int, stream: int = 0) -> None:
     _check("bsp_spmm_host", lib().bsp_spmm_host(h, X_host_ptr, N, Y_host_ptr, stream))
+
+
+def bsp_spmm_host_async(h: int, X_host_ptr: int, N: int, Y_host_ptr: int, stream: int = 0) -> None:
+    _check("bsp_spmm_host_async", lib().bsp_spmm_host_async(h, X_host_ptr, N, Y_host_ptr, stream))
 
 
 def bsp_storage_bytes(h: int) -> int:
@@ -515,6 +520,11 @@ class BitmapMatrix:
 
     def spmm_host(self, X_host, Y_host, stream=None):
         bsp_spmm_host(self.h, X_host.data_ptr(), X_host.shape[0], Y_host.data_ptr(), _stream(stream))
+        return Y_host
+
+    def spmm_host_async(self, X_host, Y_host, stream=None):
+        """Enqueued only: Y_host is valid after `stream` is synchronised."""
+        bsp_spmm_host_async(self.h, X_host.data_ptr(), X_host.shape[0], Y_host.data_ptr(), _stream(stream))
         return Y_host
 
     def decode(self, out=None, stream=None):

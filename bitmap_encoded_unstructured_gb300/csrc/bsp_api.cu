@@ -254,8 +254,11 @@ bsp_status_t bsp_column_index_export(bsp_handle_t h, uint32_t* offsets, uint32_t
     return BSP_OK;
 }
 
-bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,
-                           bsp_stream_t stream)
+namespace {
+
+// H2D copy of X into the handle's staging buffer, the product, D2H copy of
+// Y, all on `stream`; `sync`: then wait for them.
+bsp_status_t spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host, bsp_stream_t stream, bool sync)
 {
     if (!valid(h) || !X_host || !Y_host || N < 1 || N > (int64_t)1 << 30) return BSP_ERR_INVALID_ARG;
     DeviceGuard g(h->device);
@@ -271,10 +274,22 @@ bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* 
         return BSP_ERR_CUDA;
     st = bsp_spmm(h, h->stage_x, N, h->stage_y, stream);
     if (st != BSP_OK) return st;
-    if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-        return BSP_ERR_CUDA;
+    if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BSP_ERR_CUDA;
+    if (sync && cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;
     return BSP_OK;
+}
+
+}  // namespace
+
+bsp_status_t bsp_spmm_host(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host, bsp_stream_t stream)
+{
+    return spmm_host(h, X_host, N, Y_host, stream, true);
+}
+
+bsp_status_t bsp_spmm_host_async(bsp_handle_t h, const void* X_host, int64_t N, void* Y_host,
+                                 bsp_stream_t stream)
+{
+    return spmm_host(h, X_host, N, Y_host, stream, false);
 }
 
 bsp_status_t bsp_storage_bytes(bsp_handle_t h, uint64_t* bytes)

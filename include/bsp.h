@@ -288,6 +288,22 @@ bsp_status_t bsp_spmm_host(bsp_handle_t h, const void *X_host, int64_t N,
                            void *Y_host, bsp_stream_t stream);
 
 /*
+ * bsp_spmm_host without the final synchronisation: the copies and the
+ * product are only enqueued on `stream`, so calls on several handles
+ * overlap their transfers and kernels.  Y_host holds the result once
+ * `stream` has been synchronised (or an event recorded after the call has
+ * completed); X_host and Y_host must stay valid until then and should be
+ * pinned (pageable memory makes the copies synchronous with the host).
+ * Successive calls on one handle reuse its staging buffers in stream order,
+ * so they must use the same stream; a call that needs larger staging
+ * buffers than the handle holds replaces them, which synchronises the
+ * device (cudaFree).  Errors as bsp_spmm_host; an error of the enqueued
+ * work is reported by the synchronisation or by bsp_check.
+ */
+bsp_status_t bsp_spmm_host_async(bsp_handle_t h, const void *X_host, int64_t N,
+                                 void *Y_host, bsp_stream_t stream);
+
+/*
  * Footprint of the encoded weight in bytes, exactly
  *   Stor = 4*(NGT+1) + 8*NBT + B_v*NNZ   (B_v = 2 fp16, 1 int8),
  * the closed form on the SpInfer page ("How TCA-BME addresses the indexing

@@ -301,6 +301,35 @@ def test_spmm_host_buffers():
     assert_within_bound(Yh.numpy(), Yref, S, "host")
 
 
+def test_spmm_host_async_enqueued_calls():
+    """bsp_spmm_host_async on three handles (fp16 at two N, int8), enqueued
+    back to back on one stream with a single synchronisation: every Y in
+    host memory is right afterwards, and the same handle called twice in a
+    row (staging buffers reused in stream order) gives both results."""
+    s = torch.cuda.Stream()
+    W1 = synth.weights_f16(384, 1024, 0.5, "uniform", 73)
+    W2 = synth.weights_i8(256, 512, 0.5, 74)
+    A1, A2 = _encode(W1), _encode(W2)
+    Xa = synth.activations_f16(3, 1024, 75)
+    Xb = synth.activations_f16(12, 1024, 76)
+    X8 = synth.activations_i8(16, 512, 77)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    Xah, Xbh, X8h = pin(Xa.view(np.float16)), pin(Xb.view(np.float16)), pin(X8)
+    Yah = torch.empty((3, 384), dtype=torch.float16).pin_memory()
+    Ybh = torch.empty((12, 384), dtype=torch.float16).pin_memory()
+    Y8h = torch.empty((16, 256), dtype=torch.int32).pin_memory()
+    A1.spmm_host_async(Xah, Yah, stream=s)
+    A1.spmm_host_async(Xbh, Ybh, stream=s)
+    A2.spmm_host_async(X8h, Y8h, stream=s)
+    s.synchronize()
+    A1.check(s)
+    A2.check(s)
+    for X, Yh in ((Xa, Yah), (Xb, Ybh)):
+        Yref, S = oracle.spmm_f16(W1, X)
+        assert_within_bound(Yh.numpy(), Yref, S, "host async")
+    np.testing.assert_array_equal(Y8h.numpy().astype(np.int64), oracle.spmm_i8(W2, X8))
+
+
 # ------------------------------------------------------------------ ABI errors
 
 def test_abi_error_paths():
