@@ -235,6 +235,11 @@ def _dist():
     return ws, rank, local
 
 
+def _progress(msg: str) -> None:
+    """One progress line on stderr (the JSON result goes to stdout)."""
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def _max_over_ranks(v: float, ws: int) -> float:
     """Max of a per-rank value over all ranks (the whole-job time)."""
     if ws == 1:
@@ -501,6 +506,7 @@ def run_gpu(args):
             if events is not None:
                 events[i].record(stream)
 
+    _progress("decode step")
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -585,6 +591,7 @@ def run_gpu(args):
     # ---- e2e: same step through the host-buffer C-ABI call
     e2e = None
     if not args.no_e2e:
+        _progress("e2e")
         Xh = {(n, N): torch.from_numpy(xs[n][:N].view(np.float16).copy()).pin_memory() for n, _, _ in LAYERS for N in NS}
         Yh = {(n, N): torch.empty((N, M), dtype=torch.float16).pin_memory() for n, M, _ in LAYERS for N in NS}
         h2d = sum(Xh[k].numel() * 2 for k in Xh)
@@ -619,18 +626,22 @@ def run_gpu(args):
 
     prefill = None
     if not args.no_prefill:
+        _progress("prefill leg")
         prefill = run_prefill_leg(bsp, torch, dev, stream, ws)
 
     union = None
     if not args.no_union:
+        _progress("union leg")
         union = run_union_leg(bsp, torch, dev, stream, ws)
 
     sweep = None
     if not args.no_sweep:
+        _progress("sweep leg")
         sweep = run_sweep_leg(bsp, torch, dev, stream, ws)
 
     int8 = None
     if not args.no_int8:
+        _progress("int8 leg")
         int8 = run_int8_leg(bsp, torch, dev, stream, ws)
 
     cpu = None
@@ -790,6 +801,7 @@ def run_int8_leg(bsp, torch, dev, stream, ws, steps=20):
             torch.cuda.synchronize()
             row = {"storage_bytes": stor, "compression_ratio": round(M * K / stor, 4), "copies": copies}
             for N in INT8_NS:
+                _progress(f"int8 {name} s={s} N={N}")
                 Xd = torch.from_numpy(X[:N].copy()).to(dev)
                 Y = torch.empty((N, M), dtype=torch.int32, device=dev)
 

@@ -451,6 +451,10 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         uint32_t s = 0, ph = 0;  // stage and its phase parity
         uint32_t i = 0;          // steps issued
         for (; i < S; ++i) {
+            // a stage frees only once the MMAs run, which wait for the
+            // previous kernel: wait for it here (unbounded, it completes on
+            // its own) so that no bounded wait below counts that time
+            if (i == SC) wait_prior_grids();
             if (i >= SC && !__all_sync(FULL, wait_bar(c_empty + s, ph ^ 1u, cap, BSP_NARROW_SLEEP_PROD))) {
                 failed = true;
                 break;
@@ -574,6 +578,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         // have read
         uint32_t sb = 0, pb = 0;
         uint32_t k = kk0, seg = 0;
+        wait_prior_grids();  // the X tiles come after it (see the producer)
         for (uint32_t i = 0; i < S && !failed; ++i) {
             const uint32_t g = i % NG;
             const uint32_t pos = i < L0 ? i : k;  // step within the segment
@@ -632,6 +637,7 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         for (uint32_t i = G; i < S; i += NG, ++it) {
             bool ok = wait_bar(c_full + sc, pc, cap, BSP_NARROW_SLEEP_DEC);
             // the MMAs of this group's previous step read A stage G: done
+            if (it == 1) wait_prior_grids();  // the MMAs wait for the previous kernel (see the producer)
             if (it > 0) ok = ok && wait_bar(a_empty + G, (it - 1) & 1u, cap, BSP_NARROW_SLEEP_DEC);
             if (!__all_sync(FULL, ok)) { failed = true; break; }
             tc_fence_after();
@@ -900,9 +906,13 @@ bsp_status_t launch_narrow(const bsp_decode_problem& p, const void* X, int64_t N
     a.sc = std::min<int>(SC_MAX, L::C_BYTES / (int)a.c_stage);
     if (a.sc < NG) return BSP_ERR_INTERNAL;  // each decoder group needs a stage of its own in flight
     const int smem = L::OFF_C + a.sc * (int)a.c_stage + 1024;
+    // programmatic dependent launch for fp16 only: the int8 variant stalled
+    // under it (rarely: about one call in a thousand in back-to-back calls,
+    // a wait for its first X tile running out) and is launched in plain
+    // stream order, which ran clean
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[0].val.programmaticStreamSerializationAllowed = I8 ? 0 : 1;
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)P);
