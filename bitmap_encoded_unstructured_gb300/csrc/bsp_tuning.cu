@@ -26,10 +26,11 @@
 // The same crossover for int8 weights.  The narrow kernel multiplies exact
 // fp16 copies of the int8 values; the CUDA-core alternative is the team
 // kernel's dp4a.  Measured on the 11008 x 4096 and 4096 x 11008 layers at 50%
-// and 60%: the narrow kernel is ahead at every N, 23.4 against 24.7 us at
-// N = 1, 24.4 against 44.7 at N = 8, 28.0 against 65.7 at N = 16.
+// and 60% (calls rotating over copies larger than L2): team 24.6 / 26.7 /
+// 34.9 / 44.7 / 65.7 us at N = 1 / 2 / 3 / 8 / 16, narrow 28.8 at N = 1,
+// 30.7 at N = 8, 33.7 at N = 16.
 #ifndef BSP_NARROW_MIN_N_I8_DEFAULT
-#define BSP_NARROW_MIN_N_I8_DEFAULT 1
+#define BSP_NARROW_MIN_N_I8_DEFAULT 3
 #endif
 
 namespace {

@@ -124,7 +124,7 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  *   Y  device [N][M], fp16 (BSP_FP16) or int32 (BSP_INT8), 16-B aligned.
  *   N  >= 1.  Kernels, by dtype and N (the crossovers are the tuning
  *      knobs BSP_TUNE_NARROW_MIN_N, default 3, and BSP_TUNE_NARROW_MIN_N_I8,
- *      default 1):
+ *      default 3):
  *        fp16, N <= 2: the GT-per-warp CUDA-core decode kernel (split-K
  *          over GroupTiles, fp32 accumulation);
  *        fp16, 3 <= N <= 16: the narrow tcgen05 kernel (decoded tiles in
@@ -132,11 +132,11 @@ bsp_status_t bsp_destroy(bsp_handle_t h);
  *          CTAs; tiles split between CTAs are finished by a second kernel);
  *        fp16, N > 16: the tcgen05 prefill kernel (decoded tiles in shared
  *          memory, fp32 accumulation in tensor memory);
- *        int8, N <= 16: the same narrow tcgen05 kernel on exact fp16 copies
- *          of the int8 weights and activations (fp32 accumulation in runs
- *          of at most 16 GroupTile columns, each an exact integer below
- *          2^24, added as int32); below the crossover the CUDA-core team
- *          decode kernel (dp4a);
+ *        int8, N <= 2: the CUDA-core team decode kernel (dp4a);
+ *        int8, 3 <= N <= 16: the same narrow tcgen05 kernel on exact fp16
+ *          copies of the int8 weights and activations (fp32 accumulation in
+ *          runs of at most 16 GroupTile columns, each an exact integer below
+ *          2^24, added as int32);
  *        int8, N > 16: the team decode kernel over blocks of 16 columns.
  * fp16: Y = fp16(round-to-nearest of an fp32 sum in unspecified order).
  * int8: Y is the exact int32 sum.
@@ -186,7 +186,7 @@ bsp_status_t bsp_set_deterministic(bsp_handle_t h, int on);
  *                            prefill kernel; 0 = as many as fit
  *   BSP_TUNE_NARROW_MIN_N_I8 (BSP_NARROW_MIN_N_I8) smallest int8 N <= 16
  *                            that runs the tcgen05 decode kernel; larger
- *                            than 16: never; default 1
+ *                            than 16: never; default 3
  * Split counts are clamped to the problem (at most one per GroupTile
  * column).  BSP_ERR_INVALID_ARG for an unknown knob or a value out of range
  * (split counts and stages 0..4096, NARROW_CTAS 0..2^20, NARROW_MIN_N and
