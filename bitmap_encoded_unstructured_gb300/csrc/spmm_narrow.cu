@@ -1,5 +1,6 @@
-// Narrow product Y = W * X for fp16 and 1 <= N <= 16 on the 5th-generation
-// tensor cores, the decoded weight tile held in tensor memory.
+// Narrow product Y = W * X for 1 <= N <= 16 on the 5th-generation tensor
+// cores, the decoded weight tile held in tensor memory: fp16 weights and X,
+// or int8 weights and X multiplied as their exact fp16 copies (int32 Y).
 //
 // Method: "load as sparse, compute as dense" ("Unified Static-Dynamic
 // Pruning for Efficient LLM Inference", section 4.3; "SpInfer: How bitmaps
@@ -31,12 +32,21 @@
 // the workspace (vector reductions, fire and forget), or store them to
 // per-segment slots in deterministic mode, and a small second kernel,
 // launched as a programmatic dependent of the first, converts those tiles
-// to fp16 (and clears the workspace).  The product kernel is itself
+// to fp16 (and clears the workspace).  The fp16 product kernel is itself
 // launched as a programmatic dependent of whatever precedes it on the
-// stream: its prologue (tensor memory, barriers, the encoded weight's
-// copies, which no kernel writes after encoding) overlaps the tail of the
-// previous kernel, and it waits for that kernel only before it reads X or
-// writes Y or the workspace.  Warps:
+// stream: its prologue (tensor memory, barriers, the first ring of the
+// encoded weight's copies, which no kernel writes after encoding) overlaps
+// the tail of the previous kernel.  Every warp waits for that kernel before
+// it reads X, writes Y or the workspace, or starts a bounded wait that
+// depends on it, so no poll cap counts the time the previous kernel takes.
+//
+// int8: values are 16 per 16-B chunk; each stored value is decoded into
+// its fp16 copy (exact), the B producer converts each int8 X tile (TMA into
+// a staging buffer) into the fp16 X stage, and the accumulator restarts
+// every RUN_I8 steps of a segment so that every fp32 partial sum stays an
+// exact integer; each run is added as int32 (the tile's rows straight to Y
+// when the tile is one run of one CTA, else into the int32 workspace).  The
+// int8 kernels are launched in plain stream order.  Warps:
 //   0       C producer: bitmaps + value spans of the step's two GTs (bulk
 //           copies) into the C ring (the rest of shared memory, stages
 //           sized for the densest GT)
@@ -44,7 +54,7 @@
 //           A from tensor memory, B = the X tile in shared memory, M = 128,
 //           N = 16, K = 16, four per step)
 //   2       B producer: the 16 x 64 X tile of each step by TMA (rows past N
-//           read as zeros)
+//           read as zeros); int8: converted to fp16 by this warp
 //   3 ..    decoders, NG groups of four warps (one per TMEM lane quadrant);
 //           group g takes the CTA's steps g, g + NG, ... and owns A stage g
 //           in tensor memory.  Per step a warp scans the popcounts of its 32

@@ -7,7 +7,9 @@ on them: fp16 within |y - y_ref| <= 4e-3 * sum_k |w_mk x_kn| + 1e-5, int8 bit
 for bit.  The shapes are the workloads of SpInfer's "Results" section and the
 SPDP kernel evaluation (section 5.3): Llama-2-70B FFN prefill at N = 1024 and
 4096 (two 256-column sub-tiles per CTA), the 8192 x 8192 sparsity sweep at 30%
-and 70%, and INT8 11008 x 4096 / 4096 x 11008 at 50% and 60%.
+and 70%, INT8 11008 x 4096 / 4096 x 11008 at 50% and 60%, and the IE-BME leg
+(UnionSparse's W8A8 / W4A4 product, plain and row-reordered) on the OPT-13B
+QKV and FC2 projections.
 """
 import numpy as np
 import pytest
@@ -92,4 +94,26 @@ def test_int8_full_size(li, s):
         A.check()
         np.testing.assert_array_equal(_rows_of(Y, rows).astype(np.int64), acc[:N])
         np.testing.assert_array_equal(_rows_of(Yf, rows).view(np.uint32), ref_scaled[:N].view(np.uint32))
+    A.close()
+
+
+@pytest.mark.parametrize("bits,reorder", [(8, False), (4, False), (4, True)])
+@pytest.mark.parametrize("li", [0, 3])
+def test_ie_bme_full_size(li, bits, reorder):
+    """The IE-BME leg's own configurations (UnionSparse): the OPT-13B QKV and
+    FC2 projections as b-bit integers with i.i.d. 50% masks, W8A8, W4A4 and
+    W4A4 with bitmap-aware row reordering, N = 1, 8, 16: the exact int32
+    product, bit for bit on 2 sampled rows of every 64-row strip."""
+    from bitmap_encoded_unstructured_gb300 import synth
+    from oracle import ie_bme
+    name, M, K = bench.LAYERS[li]
+    W = synth.weights_int(M, K, bits, 0.5, synth.seed_for(6, 10 * bits + li), exact=False)
+    A = bsp.UnionMatrix(to_dev(W, DEV), bits, reorder=reorder)
+    rows = sample_rows(M, 2, seed=11 * li + bits)
+    for N in bench.UNION_NS:
+        X = synth.activations_int(N, K, bits, synth.seed_for(6, N))
+        Y = A.spmm(to_dev(X, DEV))
+        A.check()
+        np.testing.assert_array_equal(_rows_of(Y, rows).astype(np.int64), ie_bme.union_spmm(W[rows], X),
+                                      err_msg=f"{name} W{bits}A{bits} reorder={reorder} N={N}")
     A.close()
