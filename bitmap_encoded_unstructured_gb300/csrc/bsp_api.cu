@@ -413,6 +413,14 @@ bsp_status_t bsp_check(bsp_handle_t h, bsp_stream_t stream)
         cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return BSP_ERR_CUDA;
+    if (e) {
+        // a call that gave up may have left partial sums and arrival counts
+        // behind: restore the zero state the next call relies on
+        if (cudaMemsetAsync(h->ws, 0, (size_t)BSP_DECODE_MAX_N * (size_t)h->M * 4, s) != cudaSuccess ||
+            cudaMemsetAsync(h->counters, 0, (size_t)(h->Mp / 64) * 4, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return BSP_ERR_CUDA;
+    }
     return e ? (bsp_status_t)e : BSP_OK;
 }
 
