@@ -58,11 +58,11 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
 
 
-# Kernels one call of the step launches: the column-index spMspV product is
-# followed by its finishing kernel whenever it splits the GTile columns,
-# which holds for FC2 (tests/test_bench_cpu.py checks it); the fp16 narrow
-# kernel converts its split tiles itself.
-LAUNCHES_PER_CALL = {"spmm_decode_gtw_kernel": 1, "spmm_decode_kernel": 1, "spmm_narrow_kernel": 1,
+# Kernels one call of the step launches: the narrow and column-index spMspV
+# products are followed by their finishing kernel whenever tiles are split
+# between CTAs, which holds for every layer of the step at the automatic
+# CTA / split counts (tests/test_bench_cpu.py checks the split counts).
+LAUNCHES_PER_CALL = {"spmm_decode_gtw_kernel": 1, "spmm_decode_kernel": 1, "spmm_narrow_kernel": 2,
                      "spmspv_cbc_kernel": 2}
 
 

@@ -124,12 +124,10 @@ bsp_status_t bsp_run_spmm_prefill(const bsp_decode_problem& p, const void* X, in
 
 // ---- tcgen05 narrow kernel (spmm_narrow.cu), fp16 or int8, 1 <= N <= 16 ----
 // Persistent, balanced over the SM slots; tiles split between CTAs meet in
-// the decode problem's workspace (zero between calls, fp32 [M][16] here)
-// or, fp16 in deterministic mode, in its slots ([slots][M][16]), and the
-// last arrival on the tile's counter (the counters, zero between calls)
-// converts them.  int8: X int8 [N][K], Y int32 [N][M], exact; tiles split
-// or of more than 16 GT columns meet in the int32 workspace and a second
-// kernel converts them.
+// the decode problem's workspace (zero between calls, fp32 [M][16] here;
+// int32 for int8, whose tiles of more than 16 GT columns meet there too)
+// or, fp16 in deterministic mode, in its slots ([slots][M][16]), and a
+// second kernel converts them.  int8: X int8 [N][K], Y int32 [N][M], exact.
 bsp_status_t bsp_run_spmm_narrow(const bsp_decode_problem& p, const void* X, int64_t N, void* Y,
                                  cudaStream_t s);
 // Slots the deterministic mode needs for the automatic CTA count: the

@@ -30,10 +30,9 @@
 // MMAs of the next.  A tile covered by one segment is written to Y directly;
 // the segments of a tile split between CTAs add their fp32 partial sums into
 // the workspace (vector reductions, fire and forget), or store them to
-// per-segment slots in deterministic mode, and count their arrivals on the
-// tile's counter; the last arrival converts the tile to fp16 (adding the
-// slots in segment order in deterministic mode) and clears the workspace
-// and the counter.  The fp16 product kernel is
+// per-segment slots in deterministic mode, and a small second kernel,
+// launched as a programmatic dependent of the first, converts those tiles
+// to fp16 (and clears the workspace).  The fp16 product kernel is itself
 // launched as a programmatic dependent of whatever precedes it on the
 // stream: its prologue (tensor memory, barriers, the first ring of the
 // encoded weight's copies, which no kernel writes after encoding) overlaps
@@ -192,7 +191,6 @@ struct NarrowArgs {
     // one per segment
     float* ws;
     float* ws_det;
-    uint32_t* counters;        // fp16: arrivals per tile split between CTAs, zero between calls
     int* err;
     uint32_t spin_cap;
 };
@@ -713,9 +711,9 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 uint32_t r[16];
                 tmem_ld16(tmem_base + buf * D_COLS + tq, r);
                 const int64_t m = (int64_t)t * BM + 32 * q + lane;
-                const int64_t first = step_owner((int64_t)t * KTA, T, P);
-                const int64_t nseg = step_owner(((int64_t)t + 1) * KTA - 1, T, P) - first + 1;
                 if (m < M) {
+                    const int64_t first = step_owner((int64_t)t * KTA, T, P);
+                    const int64_t nseg = step_owner(((int64_t)t + 1) * KTA - 1, T, P) - first + 1;
                     if (I8) {
                         // exact integers: straight to Y when the tile is one
                         // run of one CTA, else added into the int32 workspace
@@ -753,36 +751,6 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) bspx::mbar_arrive(acc_empty + buf);
-                if (!I8 && nseg > 1) {
-                    // fp16 tile split between CTAs: this warp's 32 rows are in
-                    // the workspace (or the segment's slot); the last of the
-                    // tile's 4 nseg arrivals (four quadrant warps a segment)
-                    // converts the whole tile, clears the workspace and the
-                    // counter (all zero between calls)
-                    __threadfence();
-                    __syncwarp();
-                    uint32_t last = 0;
-                    if (lane == 0) last = atomicAdd(a.counters + t, 1u) == 4u * (uint32_t)nseg - 1u ? 1u : 0u;
-                    if (__shfl_sync(FULL, last, 0)) {
-                        __threadfence();
-                        __half* Yh = static_cast<__half*>(a.Y);
-                        const int64_t r0 = (int64_t)t * BM;
-                        const int64_t rows = M - r0 < BM ? M - r0 : (int64_t)BM;
-                        for (int64_t e = lane; e < rows * N; e += 32) {
-                            const int64_t n = e / rows, mm = r0 + (e - n * rows);
-                            float v;
-                            if (a.ws_det) {  // the segments' slots in segment order
-                                v = 0.f;
-                                for (int64_t sg = 0; sg < nseg; ++sg) v += __ldcg(a.ws_det + (sg * M + mm) * 16 + n);
-                            } else {
-                                v = __ldcg(a.ws + mm * 16 + n);
-                                a.ws[mm * 16 + n] = 0.f;
-                            }
-                            Yh[n * M + mm] = __float2half_rn(v);
-                        }
-                        if (lane == 0) a.counters[t] = 0u;
-                    }
-                }
             }
             sc += NG;
             if (sc >= SC) { sc -= SC; pc ^= 1u; }
@@ -791,8 +759,8 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
         }
     }
 
-    // the next kernel may start launching (it waits for this grid's
-    // completion and memory before it touches what this grid writes)
+    // the finishing kernel may start launching (it waits for this grid's
+    // completion and memory before it reads the workspace)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (failed && lane == 0) {
         wait_prior_grids();
@@ -808,10 +776,10 @@ spmm_narrow_kernel(const __grid_constant__ CUtensorMap tmX, const NarrowArgs a)
     }
 }
 
-// Finishing kernel of the int8 variant (fp16 converts its split tiles in the
-// product kernel): Y of the tiles split between CTAs or of several runs,
-// from the int32 workspace (which it clears).  One thread per (row, column
-// < N).
+// Finishing kernel: Y of the tiles whose steps are split between CTAs (and,
+// int8, of the tiles of several runs), from the workspace (which it clears)
+// or, deterministically, from the segments' slots added in segment order.
+// One thread per (row, column < N).
 template <bool I8>
 __global__ void __launch_bounds__(256)
 spmm_narrow_finish_kernel(void* __restrict__ Y, float* __restrict__ ws, const float* __restrict__ ws_det,
@@ -940,7 +908,6 @@ bsp_status_t launch_narrow(const bsp_decode_problem& p, const void* X, int64_t N
     a.P = P;
     a.ws = (float*)p.ws;
     a.ws_det = I8 ? nullptr : p.ws_det;
-    a.counters = p.counters;
     a.err = p.err;
     a.spin_cap = bsp_spin_cap();
     // C ring: as many stages as fit, each sized for the densest GT
@@ -966,10 +933,8 @@ bsp_status_t launch_narrow(const bsp_decode_problem& p, const void* X, int64_t N
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, spmm_narrow_kernel<I8>, map, a) != cudaSuccess) return BSP_ERR_CUDA;
     }
-    // fp16 converts its split tiles in the product kernel (last arriver);
-    // int8 tiles split between CTAs or of more than one run are converted by
-    // the finishing kernel
-    if (!I8 || (!any_split(tiles, KT, T, P) && KT <= (int64_t)RUN_I8)) return BSP_OK;
+    // int8 tiles of more than one run go through the workspace too
+    if (!any_split(tiles, KT, T, P) && !(I8 && KT > (int64_t)RUN_I8)) return BSP_OK;
     // the tiles split between CTAs: converted by a programmatic dependent
     // kernel (launched while the product kernel drains; it waits for it)
     cudaLaunchConfig_t cfg = {};

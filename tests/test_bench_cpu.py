@@ -89,12 +89,19 @@ def test_spmspv_bytes_follow_the_oracle_fetch_accounting():
     assert bench.cbc_spmspv_bytes(W, x) == expect
 
 
-def test_step_launch_count_includes_the_finishing_kernel():
-    """gpu_launches counts one launch per decode call and two for the
-    column-index spMspV call, whose finishing kernel runs whenever the
-    GTile columns are split (FC2's 320 GTile columns, one per warp)."""
+def test_step_launch_count_includes_the_finishing_kernels():
+    """gpu_launches counts a finishing kernel after every narrow and
+    column-index spMspV call: on a 152-SM GB300 (304 narrow CTAs) every
+    layer of the step has a tile whose steps are shared by two CTAs of the
+    balanced partition, and FC2's 320 GTile columns make 160 spMspV splits."""
+    P = 2 * 152
+    for _, M, K in bench.LAYERS:
+        KT, tiles = K // 64, -(-M // 128)
+        T = tiles * KT
+        owner = lambda x: ((x + 1) * min(P, T) - 1) // T  # noqa: E731  (the partition's owner of step x)
+        assert any(owner(t * KT) != owner((t + 1) * KT - 1) for t in range(tiles))
     fc2_cols = dict((l[0], l) for l in bench.LAYERS)["fc2"][2] // 64
-    assert fc2_cols > 1
+    assert -(-fc2_cols // 2) > 1
     per_step = sum(bench.LAUNCHES_PER_CALL[bench.step_kernel((name, N))]
                    for N in bench.NS for name, _, _ in bench.LAYERS) + bench.LAUNCHES_PER_CALL["spmspv_cbc_kernel"]
-    assert per_step == 16 * 1 + 2
+    assert per_step == 8 * 1 + 8 * 2 + 2
