@@ -146,15 +146,18 @@ bsp_status_t bsp_spmm(bsp_handle_t h, const void *X, int64_t N, void *Y,
 
 /*
  * Deterministic split-K (on = 1) or the default atomic one (on = 0).
- * The decode kernels split the K range of a row strip over several CTAs.
- * By default the fp16 partial sums meet through fp32 atomic adds, so the
- * rounding order, and with it the last bit of an fp16 output, may change
- * from call to call.  With on = 1 each split stores its partial sums to a
- * slot of its own and the last CTA of the strip adds the slots in split
- * order: the same inputs give bit-identical outputs on every call on the
- * same GPU model (the split count depends on the SM count).  int8 is
- * exact either way; the prefill kernel (fp16, N > BSP_DECODE_MAX_N) does
- * not split K and is deterministic either way.  The first switch-on
+ * The decode kernels (bsp_spmm with N <= BSP_DECODE_MAX_N, bsp_spmspv) split
+ * the K range of a row strip or tile over several CTAs.  By default the
+ * fp16 partial sums meet through fp32 atomic adds, so the rounding order,
+ * and with it the last bit of an fp16 output, may change from call to
+ * call.  With on = 1 each split stores its partial sums to a slot of its
+ * own and the slots are added in split order (by the last CTA of the strip
+ * in the CUDA-core kernels, by the finishing kernel after the tcgen05 and
+ * column-index kernels): the same inputs give bit-identical outputs on
+ * every call on the same GPU model (the split count depends on the SM
+ * count).  int8 is exact either way; the prefill kernel (fp16,
+ * N > BSP_DECODE_MAX_N) adds its two K halves in a fixed order and is
+ * deterministic either way.  The first switch-on
  * allocates the slots (splits x BSP_DECODE_MAX_N x M fp32) on the handle's
  * device; later calls do not allocate.  Not safe to call while another
  * thread uses the handle.  BSP_ERR_INVALID_ARG for a bad handle or an `on`
