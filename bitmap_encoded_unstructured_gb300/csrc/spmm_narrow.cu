@@ -101,7 +101,7 @@ constexpr int DEC_WARPS = 4 * NG;
 constexpr int CPROD = 0, MMAW = 1, BPROD = 2, DEC0 = 3;
 constexpr int WARPS = DEC0 + DEC_WARPS;
 constexpr int THREADS = WARPS * 32;
-constexpr uint32_t kSleepNs = 1000;        // suspend hint of the waiting polls
+[[maybe_unused]] constexpr uint32_t kSleepNs = 1000;  // suspend hint of the waiting polls (BSP_NARROW_WAIT=0)
 // longest sleep between the polls of a waiting producer, MMA issuer, decoder
 #ifndef BSP_NARROW_SLEEP_PROD
 #define BSP_NARROW_SLEEP_PROD 256
