@@ -105,3 +105,28 @@ def test_step_launch_count_includes_the_finishing_kernels():
     per_step = sum(bench.LAUNCHES_PER_CALL[bench.step_kernel((name, N))]
                    for N in bench.NS for name, _, _ in bench.LAYERS) + bench.LAUNCHES_PER_CALL["spmspv_cbc_kernel"]
     assert per_step == 8 * 1 + 8 * 2 + 2
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference (the oracle on the host's cores, no GPU)
+    prints one JSON line with the keys the driver reads, the reference-arm
+    additions included (impl, cpu_baseline with kind/cores/sample and the
+    line's value, e2e with zero transfer bytes)."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["metric"] == bench.METRIC and d["config"]["workload"] == bench._config()["workload"]
+    c = d["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["cores"] >= 1 and c["sample"] and c["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
