@@ -84,3 +84,32 @@ def test_int8_and_fetch_accounting():
     allb = cbc.fetched_bytes(e, np.ones(128, dtype=bool))
     assert none == 4 * e["NGT"] * 64
     assert allb == cbc.storage_bytes(e) - 4 * (e["NGT"] + 1)
+
+
+def test_fetch_accounting_partial_activity_by_brute_force():
+    """A partial activation pattern on a 2 x 3 grid of GTiles (K = 150, so
+    the third GTile column is ragged): the bytes the column-skipping product
+    reads, counted from the dense W alone.  Each GTile contributes its 64
+    ColInfo words; each active column k of GTile row gi adds its four bitmap
+    words and the nonzeros of W[256 gi : 256 (gi + 1), k].  The two GTile
+    rows have different densities, so charging a column to the wrong GTile
+    (a row-for-column slip in the tiling) changes the total."""
+    M, K = 512, 150
+    W = synth.weights_f16(M, K, 0.5, "uniform", 11)
+    W[256:, :] = np.where(np.arange(K) % 3 == 0, W[256:, :], 0).astype(np.uint16)
+    rng = np.random.default_rng(12)
+    x_active = rng.random(K) < 0.3
+    e = cbc.encode(W)
+    assert e["NGT"] == 6
+    expect = 4 * 6 * 64
+    for gi in range(2):
+        for k in range(K):
+            if x_active[k]:
+                expect += 8 * 4 + 2 * int(np.count_nonzero(W[256 * gi:256 * (gi + 1), k]))
+    assert cbc.fetched_bytes(e, x_active) == expect
+    # the columns of the zero padding past K never count as active
+    act = cbc.active_columns(x_active, e)
+    assert act.shape == (6 * 64,)
+    assert not act.reshape(2, 3, 64)[:, 2, K - 128:].any()
+    assert (act.reshape(2, 3, 64)[0].reshape(-1)[:K] == x_active).all()
+    assert (act.reshape(2, 3, 64)[1].reshape(-1)[:K] == x_active).all()
